@@ -1,0 +1,189 @@
+"""CPU fp64 oracle for single-token MLA decode -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py``
+may import this package.  The product library never loads it and shares no code
+with it.  The arithmetic lives in ``mla_oracle.c`` (plain C, fp64, optional OpenMP
+over batch rows); this module compiles it with gcc on first use and calls it through
+ctypes with host (CPU) buffers.
+
+Functions and what pins each one (see ``tests/test_oracle.py``):
+
+* ``e4m3`` / ``e2m1`` / ``e8m0`` / ``bf16`` decoders -- exhaustive code tables against
+  PyTorch's own float8 / e8m0 / bf16 conversions and against the OCP MX e2m1 value table.
+* ``attend`` / ``decode`` -- closed forms (one cached token returns its V; identical keys
+  or q = 0 return the mean of V; a constant V column is returned unchanged; exact
+  two-token logits through a rope feature), the log-sum-exp closed form, brute force on
+  tiny inputs, cross-encoding consistency (fp8 / MXFP4 caches vs the bf16 cache holding
+  their decoded values) and the pages' 0.1/0.1 quantisation tolerance.
+* ``combine`` -- the merge of per-range partial results reproduces the full-range result.
+* ``split_range`` -- the ranges of all splits tile [0, L) in BN-rounded chunks.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "mla_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+NH, D, DV = 16, 576, 512
+KV_BF16, KV_FP8, KV_MXFP4 = 0, 1, 2
+
+
+def build(force: bool = False) -> str:
+    """Compile mla_oracle.c into a shared library (gcc -O2 -fopenmp)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-fopenmp", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        lib = ctypes.CDLL(build())
+        dbl, vp, i64, c_int = ctypes.c_double, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        for name in ("mla_oracle_e4m3", "mla_oracle_e2m1", "mla_oracle_e8m0"):
+            getattr(lib, name).restype = dbl
+            getattr(lib, name).argtypes = [c_int]
+        lib.mla_oracle_bf16.restype = dbl
+        lib.mla_oracle_bf16.argtypes = [ctypes.c_uint16]
+        lib.mla_oracle_dequant_row.restype = None
+        lib.mla_oracle_dequant_row.argtypes = [c_int, vp, vp, i64, vp]
+        lib.mla_oracle_attend.restype = c_int
+        lib.mla_oracle_attend.argtypes = [vp, c_int, vp, vp, i64, i64, vp, vp]
+        lib.mla_oracle_decode.restype = c_int
+        lib.mla_oracle_decode.argtypes = [vp, c_int, vp, vp, vp, c_int, vp, vp, c_int]
+        lib.mla_oracle_combine.restype = None
+        lib.mla_oracle_combine.argtypes = [c_int, vp, vp, vp, vp]
+        lib.mla_oracle_split_range.restype = None
+        lib.mla_oracle_split_range.argtypes = [i64, c_int, c_int, c_int,
+                                               ctypes.POINTER(i64), ctypes.POINTER(i64)]
+        lib.mla_oracle_max_threads.restype = c_int
+        lib.mla_oracle_max_threads.argtypes = []
+        _lib = lib
+        return lib
+
+
+def _np(x, dtype=None):
+    """torch tensor / numpy array -> contiguous host numpy array (no arithmetic)."""
+    if x is None:
+        return None
+    if hasattr(x, "detach"):
+        import torch
+        t = x.detach().cpu().contiguous()
+        if t.dtype == torch.bfloat16:
+            t = t.view(torch.int16)
+        x = t.numpy()
+    a = np.ascontiguousarray(x)
+    if dtype is not None:
+        a = a.view(dtype) if a.dtype.itemsize == np.dtype(dtype).itemsize else a.astype(dtype)
+    return a
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def e4m3(code: int) -> float:
+    return _load().mla_oracle_e4m3(int(code))
+
+
+def e2m1(code: int) -> float:
+    return _load().mla_oracle_e2m1(int(code))
+
+
+def e8m0(code: int) -> float:
+    return _load().mla_oracle_e8m0(int(code))
+
+
+def bf16(bits: int) -> float:
+    return _load().mla_oracle_bf16(int(bits) & 0xFFFF)
+
+
+def _kv_args(kv, kv_scale, kv_dtype):
+    if kv_dtype == KV_BF16:
+        return _np(kv, np.uint16), None
+    if kv_dtype == KV_FP8:
+        return _np(kv, np.uint8), _np(kv_scale, np.float32)
+    if kv_dtype == KV_MXFP4:
+        return _np(kv, np.uint8), _np(kv_scale, np.uint8)
+    raise ValueError(kv_dtype)
+
+
+def dequant_rows(kv, kv_scale, kv_dtype, rows) -> np.ndarray:
+    """Decoded rows (fp64 [len(rows), 576])."""
+    lib = _load()
+    k, s = _kv_args(kv, kv_scale, kv_dtype)
+    out = np.zeros((len(rows), D), dtype=np.float64)
+    for i, r in enumerate(rows):
+        lib.mla_oracle_dequant_row(kv_dtype, _ptr(k), _ptr(s), int(r), _ptr(out[i]))
+    return out
+
+
+def attend(q_b, kv, kv_scale, kv_dtype, r0: int, r1: int):
+    """One batch row (q_b: bf16 [16, 576]) over cached rows [r0, r1) ->
+    (o fp64 [16, 512], lse fp64 [16])."""
+    lib = _load()
+    qa = _np(q_b, np.uint16).reshape(NH, D)
+    k, s = _kv_args(kv, kv_scale, kv_dtype)
+    o = np.zeros((NH, DV), dtype=np.float64)
+    lse = np.zeros((NH,), dtype=np.float64)
+    rc = lib.mla_oracle_attend(_ptr(qa), kv_dtype, _ptr(k), _ptr(s), int(r0), int(r1), _ptr(o), _ptr(lse))
+    if rc:
+        raise MemoryError("oracle attend failed")
+    return o, lse
+
+
+def decode(q, kv, kv_scale, kv_indptr, kv_dtype, nthreads: int = 0):
+    """Whole decode -> (out fp64 [B, 16, 512], lse fp64 [B, 16])."""
+    lib = _load()
+    qa = _np(q, np.uint16)
+    B = qa.shape[0]
+    k, s = _kv_args(kv, kv_scale, kv_dtype)
+    ip = _np(kv_indptr, np.int32)
+    out = np.zeros((B, NH, DV), dtype=np.float64)
+    lse = np.zeros((B, NH), dtype=np.float64)
+    rc = lib.mla_oracle_decode(_ptr(qa), kv_dtype, _ptr(k), _ptr(s), _ptr(ip), B, _ptr(out), _ptr(lse),
+                               int(nthreads))
+    if rc:
+        raise MemoryError("oracle decode failed")
+    return out, lse
+
+
+def combine(o_parts, lse_parts):
+    """Merge partial results of one batch row: o_parts [ns, 16, 512], lse_parts [ns, 16]."""
+    lib = _load()
+    o_parts = np.ascontiguousarray(o_parts, dtype=np.float64)
+    lse_parts = np.ascontiguousarray(lse_parts, dtype=np.float64)
+    ns = o_parts.shape[0]
+    out = np.zeros((NH, DV), dtype=np.float64)
+    lse = np.zeros((NH,), dtype=np.float64)
+    lib.mla_oracle_combine(ns, _ptr(o_parts), _ptr(lse_parts), _ptr(out), _ptr(lse))
+    return out, lse
+
+
+def split_range(L: int, ns: int, bn: int, s: int):
+    lib = _load()
+    a, b = ctypes.c_int64(0), ctypes.c_int64(0)
+    lib.mla_oracle_split_range(int(L), int(ns), int(bn), int(s), ctypes.byref(a), ctypes.byref(b))
+    return a.value, b.value
+
+
+def max_threads() -> int:
+    return _load().mla_oracle_max_threads()
