@@ -1,0 +1,367 @@
+#!/usr/bin/env python3
+"""Benchmark of single-token MLA decode (split-KV) on GB300.
+
+One step = one ``mla_decode`` call (split kernel + combine kernel) over one batch of
+seeded synthetic inputs already resident in HBM.  Between timed calls a 256 MiB buffer
+is written to flush the 129 MB L2 (cold-cache timing, as the pages' own timing harness
+does).  Prints ONE JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config I] [--impl ours|reference]
+
+``--impl reference`` times the CPU fp64 oracle on the host cores on a bounded sample of
+the same workload (the only other place this script runs the oracle).
+Under torchrun (N > 1) every rank decodes its own replica of the workload (the batch is
+sharded, no collective on the data path) and rank 0 reports the aggregate.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = json.load(open(os.path.join(ROOT, "BASELINE.json")))["metric"] if os.path.exists(
+    os.path.join(ROOT, "BASELINE.json")) else "MLA decode KV-cache GB/s"
+DEFAULT_CONFIG = 2          # fp8-e4m3, batch 64 x 8192 tokens, split-KV + combine
+FLUSH_BYTES = 256 << 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", type=int, default=DEFAULT_CONFIG)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    return ap.parse_args()
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "mla_attention_decode_splitkv_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            h.update(name.encode())
+            h.update(open(os.path.join(csrc, name), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str):
+    """DRAM bytes per split-kernel launch from the committed ncu summary, if it was taken on
+    the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        d = json.load(open(path))
+        ent = d.get(workload)
+        if ent and ent.get("kernel_source_hash") == kernel_source_hash():
+            return float(ent["dram_bytes_per_launch"])
+    except Exception:
+        return None
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def oracle_sample_rate(inp, budget_s: float, max_rows: int = None):
+    """Times the CPU oracle on whole batch rows (copied to the host) for about budget_s
+    seconds of wall time.  Returns (GB/s of KV bytes, seconds, rows, threads)."""
+    import numpy as np  # noqa: F401
+    import oracle
+    from mla_attention_decode_splitkv_gb300 import synth
+
+    ip = inp.kv_indptr.cpu().tolist()
+    B = len(ip) - 1
+    order = list(range(B))
+    threads = oracle.max_threads()
+    # first, one row to size the sample
+    rows, total_bytes, t_total = 0, 0, 0.0
+    row_bytes = synth.KV_ROW_BYTES[inp.kv_dtype]
+    scale_cpu = None if inp.kv_scale is None else inp.kv_scale
+    while rows < B and (max_rows is None or rows < max_rows):
+        take = 1 if rows == 0 else max(1, min(B - rows, threads,
+                                              int((budget_s - t_total) / max(t_total / rows, 1e-3) * threads)))
+        sel = order[rows:rows + take]
+        lens = [ip[b + 1] - ip[b] for b in sel]
+        q = inp.q[sel].cpu()
+        kv = __import__("torch").cat([inp.kv[ip[b]:ip[b + 1]] for b in sel]).cpu()
+        sc = None
+        if inp.kv_dtype == synth.KV_FP8:
+            sc = scale_cpu.cpu()
+        elif inp.kv_dtype == synth.KV_MXFP4:
+            sc = __import__("torch").cat([scale_cpu[ip[b]:ip[b + 1]] for b in sel]).cpu()
+        sub_ip = synth.indptr_from_lengths(lens)
+        t0 = time.perf_counter()
+        oracle.decode(q, kv, sc, sub_ip, inp.kv_dtype, nthreads=threads)
+        t_total += time.perf_counter() - t0
+        rows += take
+        total_bytes += sum(lens) * row_bytes
+        if t_total >= budget_s:
+            break
+    return total_bytes / t_total / 1e9, t_total, rows, threads
+
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return
+    import torch
+    from mla_attention_decode_splitkv_gb300 import synth
+    spec = synth.CONFIGS[args.config]
+    inp = synth.make_config(args.config, device="cpu", keep_src=False) if spec.batch * (spec.kv_len or 4096) <= 600000 \
+        else synth.make_config(args.config, device="cuda" if torch.cuda.is_available() else "cpu", keep_src=False)
+    per_step_budget = max(0.5, 60.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        oracle_sample_rate(inp, per_step_budget / 4, max_rows=1)
+    rates, secs, nrows = [], 0.0, 0
+    threads = 1
+    for _ in range(args.steps):
+        r, t, n, threads = oracle_sample_rate(inp, per_step_budget)
+        rates.append(r)
+        secs += t
+        nrows += n
+    value = statistics.mean(rates)
+    kv_bytes = inp.kv_bytes()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": kv_bytes / (value * 1e9) * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_dict(spec, inp),
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{nrows} whole batch rows over {args.steps} steps ({secs:.1f} s of oracle time); "
+                                   f"ms_per_step extrapolates to the full batch"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_dict(spec, inp):
+    from mla_attention_decode_splitkv_gb300 import synth
+    lens = inp.lens
+    return {"workload": spec.name, "batch": spec.batch,
+            "kv_len": spec.kv_len if spec.kv_len else f"ragged U[1,8192], mean {sum(lens) / len(lens):.0f}",
+            "kv_dtype": synth.DTYPE_NAMES[spec.kv_dtype],
+            "num_splits": spec.num_splits if spec.num_splits else "balanced (persistent, one CTA per SM)",
+            "heads": 16, "head_dim": 576, "v_dim": 512, "kv_bytes_per_call": inp.kv_bytes(),
+            "l2": "flushed between timed calls (256 MiB write)"}
+
+
+def main():
+    args = parse()
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if args.impl == "ours" else "gloo")
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+        return
+
+    import torch
+    import mla_attention_decode_splitkv_gb300 as pkg
+    from mla_attention_decode_splitkv_gb300 import build as pkg_build
+    from mla_attention_decode_splitkv_gb300 import synth
+
+    pkg_build.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    spec = synth.CONFIGS[args.config]
+    inp = synth.make_config(args.config, device=dev, keep_src=False)
+    B = inp.batch
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    ns = spec.num_splits
+    pkg.reserve_workspace(pkg.workspace_slots(B, ns, sms))
+    out = torch.empty((B, 16, 512), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def call():
+        rc = pkg.mla_decode(inp.q, inp.kv, inp.kv_scale, inp.kv_indptr, out, B, ns, spec.kv_dtype, stream)
+        if rc != pkg.MLA_OK:
+            raise pkg.MLAError(rc, "mla_decode")
+
+    for _ in range(max(3, args.warmup)):
+        call()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
+    sampler.start()
+    t_soak = time.perf_counter()
+    while time.perf_counter() - t_soak < 0.6:      # load the GPU so clock samples exist
+        for _ in range(20):
+            call()
+        torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    pkg.profile_begin()
+    for i in range(args.steps):
+        flush.fill_(float(i))
+        evs[i][0].record(stream)
+        call()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    split_ms_sum, call_ms_sum, ncalls = pkg.profile_end()
+    if ws > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+    ms = statistics.mean(step_ms)
+    split_ms = split_ms_sum / max(1, ncalls)
+    if pkg.device_status(clear=True) != pkg.MLA_OK:
+        raise RuntimeError("kernel reported a pipeline timeout during the benchmark")
+
+    # ---- end to end: host (pinned) inputs -> device, decode, output -> host, every step
+    q_h = inp.q.cpu().pin_memory()
+    kv_h = inp.kv.cpu().pin_memory()
+    sc_h = None if inp.kv_scale is None else inp.kv_scale.cpu().pin_memory()
+    ip_h = inp.kv_indptr.cpu().pin_memory()
+    out_h = torch.empty((B, 16, 512), dtype=torch.bfloat16).pin_memory()
+    q_d, kv_d = torch.empty_like(inp.q), torch.empty_like(inp.kv)
+    sc_d = None if sc_h is None else torch.empty_like(inp.kv_scale)
+    ip_d = torch.empty_like(inp.kv_indptr)
+    h2d = q_h.numel() * 2 + kv_h.numel() * kv_h.element_size() + (0 if sc_h is None else sc_h.numel() * sc_h.element_size()) \
+        + ip_h.numel() * 4
+    d2h = out_h.numel() * 2
+
+    def e2e_step():
+        q_d.copy_(q_h, non_blocking=True)
+        kv_d.copy_(kv_h, non_blocking=True)
+        if sc_d is not None:
+            sc_d.copy_(sc_h, non_blocking=True)
+        ip_d.copy_(ip_h, non_blocking=True)
+        rc = pkg.mla_decode(q_d, kv_d, sc_d, ip_d, out, B, ns, spec.kv_dtype, stream)
+        if rc != pkg.MLA_OK:
+            raise pkg.MLAError(rc, "mla_decode")
+        out_h.copy_(out, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+    assert torch.equal(out_h, out.cpu())
+
+    # ---- aggregate over ranks (max time)
+    if ws > 1:
+        t = torch.tensor([ms, split_ms, e2e_ms], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms, split_ms, e2e_ms = t.tolist()
+    if rank != 0:
+        return
+    kv_bytes = inp.kv_bytes()
+    value = kv_bytes * ws / (ms * 1e-3) / 1e9
+    peak, peak_kind = peaks()
+    achieved = kv_bytes / (split_ms * 1e-3) / 1e9
+    launches_per_call = 1 if ns == 1 else 2
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "us_per_call": ms * 1e3, "frac_of_8tbs": value / ws / 8000.0,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": {0: "bf16", 1: "e4m3", 2: "e4m3"}[spec.kv_dtype],
+        "data": "synthetic (seeded N(0,1) q and KV, stored per the workload's cache encoding)",
+        "config": config_dict(spec, inp),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_kind": f"{peak_kind} (burst copy)", "kernel": "mla_split_kernel",
+                     "split_kernel_us": split_ms * 1e3, "algorithmic_bytes_per_launch": kv_bytes,
+                     "traffic": ncu_traffic(spec.name)},
+        "e2e": {"value": kv_bytes * ws / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * launches_per_call,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        r, t, n, threads = oracle_sample_rate(inp, 12.0)
+        line["cpu_baseline"] = {"value": r, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                                "sample": f"{n} whole batch rows of the workload ({t:.1f} s)"}
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

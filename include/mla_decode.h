@@ -1,0 +1,141 @@
+/*
+ * mla_decode.h -- C ABI of the GB300 (sm_103a) single-token MLA decode library.
+ *
+ * Operation (amd-mixed-mla submission 599694, `_bmm` path; geometry and sm_scale from
+ * the module constants of submissions 727205 / 700955 / 599694):
+ *   16 query heads share one latent KV head of width 576 (512 "nope" + 64 rope).
+ *   For batch row b, head h, over cached rows r in [kv_indptr[b], kv_indptr[b+1]):
+ *     s_r      = (1/sqrt(576)) * q[b,h,:] . Khat_r          Khat_r = dequantised row r
+ *     out[b,h] = sum_r softmax(s)_r * Khat_r[0:512]          (V = first 512 columns)
+ *   Page size 1: row index = token index, rows of one sequence are contiguous.
+ *
+ * Method: split-KV flash decoding (submission 727205 `mla_s1` + `mla_rd`, submission
+ * 700955 `mla_attn_v71` + `reduce_lse_v71`, submission 599694 `_flash_fp8_split_s1/_s2`):
+ * each sequence's rows are cut into splits, each split produces an online-softmax
+ * partial result (normalised output + log-sum-exp), and a combine step merges the
+ * partials by log-sum-exp weights.
+ *
+ * All pointers are DEVICE pointers unless stated otherwise.  The caller owns every
+ * buffer it passes; the library never frees or retains them past the call.  Calls are
+ * asynchronous on `stream` (a cudaStream_t; NULL = the legacy default stream): the
+ * library performs no host synchronisation and never reads device data on the host.
+ * Every entry point returns an mla_status (0 = success).
+ */
+#ifndef MLA_DECODE_H_
+#define MLA_DECODE_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MLA_NUM_HEADS 16
+#define MLA_HEAD_DIM 576
+#define MLA_V_DIM 512
+#define MLA_MX_BLOCK 32
+#define MLA_MX_PACKED_BYTES 288 /* bytes of e2m1 nibbles per cached row */
+#define MLA_MX_SCALES 18        /* e8m0 scales per cached row */
+
+/* KV-cache storage encodings.
+ *  BF16     : kv = bf16 [T][576].
+ *  FP8_E4M3 : kv = e4m3fn codes uint8 [T][576]; value = code * kv_scale[0] (one fp32 per
+ *             tensor; submission 599694 fp8 flash-decode dequantises this way).
+ *  MXFP4    : kv = uint8 [T][288], element 2i in the low nibble of byte i and 2i+1 in the
+ *             high nibble (submission 700955 `mla_attn_v74`); kv_scale = uint8 [T][18]
+ *             e8m0 block scales (value = e2m1 * 2^(E-127), one scale per 32 elements). */
+typedef enum { MLA_KV_BF16 = 0, MLA_KV_FP8_E4M3 = 1, MLA_KV_MXFP4 = 2 } mla_kv_dtype;
+
+typedef enum {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARG = -1, /* a host-side argument check failed; nothing was launched */
+  MLA_ERR_UNSUPPORTED = -2, /* device is not sm_103 / lacks the shared memory this needs */
+  MLA_ERR_CUDA = -3,        /* a CUDA runtime/driver call or a launch failed */
+  MLA_ERR_NO_MEMORY = -4,   /* the library's partial-result workspace could not grow */
+  MLA_ERR_TIMEOUT = -5      /* a kernel pipeline wait ran past its limit (device status) */
+} mla_status;
+
+/*
+ * mla_decode -- out[b,h,:] for every batch row b and head h.
+ *
+ *  q          bf16 [batch][16][576], contiguous, 16-byte aligned.
+ *  kv         cache rows, layout per kv_dtype above, contiguous, 16-byte aligned.
+ *  kv_scale   NULL for BF16; const float* [1] (device) for FP8_E4M3; const uint8_t*
+ *             [T][18] (device, row stride 18 bytes) for MXFP4.
+ *  kv_indptr  int32 [batch+1] (device): kv_indptr[0] = 0, non-decreasing, and every
+ *             kv_indptr[b+1] <= T (the number of rows in kv).  The library reads only
+ *             rows inside these ranges.  A violation is undefined behaviour (the library
+ *             cannot check device data without a host sync).
+ *  out        bf16 [batch][16][512] (device), written; 4-byte aligned.
+ *  batch      >= 1.
+ *  num_splits >= 1: cut every sequence into that many splits (BN = 128-token-rounded
+ *             chunks, submission 727205 `mla_s1` split rule; splits past the end are
+ *             empty; num_splits = 1 writes out directly with no combine step).
+ *             <= 0: the library balances the total token count of the batch evenly over
+ *             the GPU's SMs (one persistent CTA per SM, contiguous token ranges that may
+ *             span several sequences) and merges the pieces of each sequence.
+ *             At most 4096 splits.
+ *  kv_dtype   an mla_kv_dtype value.
+ *  stream     cudaStream_t or NULL.
+ * Empty sequences (kv_indptr[b] == kv_indptr[b+1]) produce zeros.
+ * Errors: MLA_ERR_INVALID_ARG before any launch for null/misaligned pointers, batch <= 0,
+ * an unknown kv_dtype or num_splits > 4096; MLA_ERR_UNSUPPORTED if the current device is
+ * not compute capability 10.3; MLA_ERR_NO_MEMORY if the workspace cannot grow;
+ * MLA_ERR_CUDA if a launch fails (the CUDA error is cleared and its name is available
+ * from mla_last_cuda_error()).
+ * The partial-result workspace is library-owned (one per device, grow-only, guarded by a
+ * mutex): growing it frees the old buffer with cudaFree, which synchronises the device.
+ */
+int mla_decode(const void* q, const void* kv, const void* kv_scale, const int32_t* kv_indptr,
+               void* out, int batch, int num_splits, int kv_dtype, void* stream);
+
+/*
+ * mla_decode_pick_splits -- host-only split-count heuristic for the uniform-split mode.
+ * Chooses ns in [1, min(ceil(kv_len_hint/128), 64)] maximising
+ *     wave_util(batch*ns CTAs over num_sms SMs, one CTA per SM) * L / (L + c*ns),
+ * where c (in tokens) is the cost of one extra split: writing and re-reading its fp32
+ * partial output (16 x 512 x 4 B x 2) plus a fixed pipeline fill, divided by the bytes of
+ * one cached row of kv_dtype.  (Shape of the analytic model of submission 700955,
+ * `_estimate_custom_splits`; constants derived here from the byte counts, no table.)
+ * Returns ns >= 1, or MLA_ERR_INVALID_ARG for batch <= 0, kv_len_hint < 0, num_sms <= 0
+ * or an unknown kv_dtype.
+ */
+int mla_decode_pick_splits(int batch, int kv_len_hint, int num_sms, int kv_dtype);
+
+/* Number of partial-result slots a call with these arguments needs (for sizing). */
+int mla_decode_workspace_slots(int batch, int num_splits, int num_sms);
+
+/* Grows the current device's workspace so that calls needing up to `slots` partial slots
+ * allocate nothing (useful before timing or graph capture).  Returns an mla_status. */
+int mla_decode_reserve_workspace(int slots);
+
+/* Frees the library's workspace on the current device (synchronises the device). */
+int mla_decode_release_workspace(void);
+
+/* Reads and (if clear != 0) resets the current device's kernel status word.  Synchronises
+ * the device.  Returns MLA_OK, or MLA_ERR_TIMEOUT if a pipeline wait in a kernel gave up
+ * since the last clear. */
+int mla_decode_device_status(int clear);
+
+/* Sets the time after which a kernel's pipeline wait gives up, sets the status word and
+ * lets the kernel return (default 2e9 ns).  For tests of the failure path. */
+void mla_decode_set_wait_limit_ns(unsigned long long ns);
+
+/* Timing hooks.  Between begin and end, every mla_decode call records CUDA events on its
+ * stream around its split kernel and around the whole call.  end() waits for those events
+ * and returns the summed split-kernel time, the summed call time (ms) and the number of
+ * calls recorded, then stops recording.  Returns an mla_status. */
+int mla_decode_profile_begin(void);
+int mla_decode_profile_end(double* split_ms, double* call_ms, int* calls);
+
+/* Static string for a status code; never NULL. */
+const char* mla_status_string(int status);
+
+/* Name of the last CUDA error the library saw on this thread ("" if none). */
+const char* mla_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_DECODE_H_ */

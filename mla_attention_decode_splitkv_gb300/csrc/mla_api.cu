@@ -1,0 +1,329 @@
+// mla_api.cu -- C ABI of the MLA decode library: argument checks, the split-count
+// heuristic, the per-device partial-result workspace, tensor-map encoding and launches.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+#include <mutex>
+#include <vector>
+
+#include "../../include/mla_decode.h"
+#include "mla_internal.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct Workspace {
+  float* part_o = nullptr;
+  float* part_lse = nullptr;
+  int* status = nullptr;
+  long long slots = 0;
+};
+
+std::mutex g_mu;
+Workspace g_ws[kMaxDevices];
+int g_sm_count[kMaxDevices];
+int g_cc[kMaxDevices];
+unsigned long long g_wait_limit_ns = 2000000000ull;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+thread_local const char* t_last_cuda_error = "";
+
+// Optional timing of each call's split kernel (events recorded on the call's stream).
+struct ProfRecord {
+  cudaEvent_t start, split_end, end;
+};
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+std::vector<ProfRecord> g_prof;
+
+int note_cuda(cudaError_t e) {
+  t_last_cuda_error = cudaGetErrorName(e);
+  return MLA_ERR_CUDA;
+}
+
+// Device properties cached per device id (SM count, compute capability).
+int device_info(int* dev_out, int* sms_out, int* cc_out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return note_cuda(e);
+  if (dev < 0 || dev >= kMaxDevices) return MLA_ERR_UNSUPPORTED;
+  if (g_sm_count[dev] == 0) {
+    int sms = 0, major = 0, minor = 0;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return note_cuda(e);
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess) return note_cuda(e);
+    if ((e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess) return note_cuda(e);
+    g_cc[dev] = major * 10 + minor;
+    g_sm_count[dev] = sms;
+  }
+  *dev_out = dev;
+  *sms_out = g_sm_count[dev];
+  *cc_out = g_cc[dev];
+  return MLA_OK;
+}
+
+// Grow-only workspace of `slots` partial results on device `dev` (caller holds g_mu).
+int ensure_workspace(int dev, long long slots) {
+  Workspace& w = g_ws[dev];
+  if (w.status == nullptr) {
+    cudaError_t e = cudaMalloc(&w.status, sizeof(int));
+    if (e != cudaSuccess) { w.status = nullptr; cudaGetLastError(); return MLA_ERR_NO_MEMORY; }
+    if ((e = cudaMemset(w.status, 0, sizeof(int))) != cudaSuccess) return note_cuda(e);
+  }
+  if (slots <= w.slots) return MLA_OK;
+  if (w.part_o) { cudaFree(w.part_o); w.part_o = nullptr; }
+  if (w.part_lse) { cudaFree(w.part_lse); w.part_lse = nullptr; }
+  w.slots = 0;
+  const size_t o_bytes = static_cast<size_t>(slots) * mla::kHeads * mla::kDimV * sizeof(float);
+  const size_t l_bytes = static_cast<size_t>(slots) * mla::kHeads * sizeof(float);
+  if (cudaMalloc(&w.part_o, o_bytes) != cudaSuccess || cudaMalloc(&w.part_lse, l_bytes) != cudaSuccess) {
+    cudaGetLastError();
+    if (w.part_o) cudaFree(w.part_o);
+    if (w.part_lse) cudaFree(w.part_lse);
+    w.part_o = nullptr;
+    w.part_lse = nullptr;
+    return MLA_ERR_NO_MEMORY;
+  }
+  w.slots = slots;
+  return MLA_OK;
+}
+
+long long slots_needed(int batch, int num_splits, int num_sms) {
+  if (num_splits == 1) return 0;
+  if (num_splits >= 2) return static_cast<long long>(batch) * num_splits;
+  return static_cast<long long>(batch) + num_sms - 1;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+int encode_kv_map(CUtensorMap* map, const void* kv, int kv_dtype) {
+  if (g_encode == nullptr) {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr) return MLA_ERR_UNSUPPORTED;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  // Rows: an upper bound; the kernel never addresses a row at or past kv_indptr[batch].
+  const cuuint64_t rows = 1ull << 30;
+  const bool bf = kv_dtype == MLA_KV_BF16;
+  cuuint64_t gdim[2] = {static_cast<cuuint64_t>(mla::kDim), rows};
+  cuuint64_t gstride[1] = {static_cast<cuuint64_t>(mla::kDim) * (bf ? 2 : 1)};
+  cuuint32_t box[2] = {bf ? 64u : 128u, static_cast<cuuint32_t>(mla::kBN)};
+  cuuint32_t estride[2] = {1, 1};
+  CUresult r = g_encode(map, bf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+                        const_cast<void*>(kv), gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* mla_status_string(int status) {
+  switch (status) {
+    case MLA_OK: return "MLA_OK";
+    case MLA_ERR_INVALID_ARG: return "MLA_ERR_INVALID_ARG";
+    case MLA_ERR_UNSUPPORTED: return "MLA_ERR_UNSUPPORTED";
+    case MLA_ERR_CUDA: return "MLA_ERR_CUDA";
+    case MLA_ERR_NO_MEMORY: return "MLA_ERR_NO_MEMORY";
+    case MLA_ERR_TIMEOUT: return "MLA_ERR_TIMEOUT";
+    default: return "MLA_UNKNOWN_STATUS";
+  }
+}
+
+const char* mla_last_cuda_error(void) { return t_last_cuda_error; }
+
+void mla_decode_set_wait_limit_ns(unsigned long long ns) { g_wait_limit_ns = ns ? ns : 1ull; }
+
+int mla_decode_pick_splits(int batch, int kv_len_hint, int num_sms, int kv_dtype) {
+  if (batch <= 0 || kv_len_hint < 0 || num_sms <= 0 || kv_dtype < 0 || kv_dtype > 2) return MLA_ERR_INVALID_ARG;
+  const double row_bytes = kv_dtype == MLA_KV_BF16 ? 1152.0 : (kv_dtype == MLA_KV_FP8_E4M3 ? 576.0 : 306.0);
+  // One extra split costs its fp32 partial output written and read back, plus a fixed
+  // pipeline fill (about one 128-row tile that is fetched before any math can start).
+  const double split_bytes = 2.0 * mla::kHeads * mla::kDimV * 4.0 + mla::kBN * row_bytes;
+  const double c = split_bytes / row_bytes;             // in tokens
+  const double L = kv_len_hint > 0 ? kv_len_hint : 1.0;
+  int max_ns = static_cast<int>((L + mla::kBN - 1) / mla::kBN);
+  if (max_ns > 64) max_ns = 64;
+  if (max_ns < 1) max_ns = 1;
+  int best = 1;
+  double best_score = -1.0;
+  for (int ns = 1; ns <= max_ns; ++ns) {
+    const double ctas = static_cast<double>(batch) * ns;
+    const double waves = std::ceil(ctas / num_sms);
+    const double util = ctas / (waves * num_sms);
+    const double eff = L / (L + c * (ns - 1));
+    const double score = util * eff;
+    if (score > best_score * (1.0 + 1e-9)) { best_score = score; best = ns; }
+  }
+  return best;
+}
+
+int mla_decode_workspace_slots(int batch, int num_splits, int num_sms) {
+  if (batch <= 0 || num_sms <= 0) return MLA_ERR_INVALID_ARG;
+  long long s = slots_needed(batch, num_splits, num_sms);
+  return s > 0x7fffffffLL ? MLA_ERR_INVALID_ARG : static_cast<int>(s);
+}
+
+int mla_decode_reserve_workspace(int slots) {
+  if (slots < 0) return MLA_ERR_INVALID_ARG;
+  int dev, sms, cc;
+  int rc = device_info(&dev, &sms, &cc);
+  if (rc) return rc;
+  std::lock_guard<std::mutex> lk(g_mu);
+  return ensure_workspace(dev, slots);
+}
+
+int mla_decode_release_workspace(void) {
+  int dev, sms, cc;
+  int rc = device_info(&dev, &sms, &cc);
+  if (rc) return rc;
+  std::lock_guard<std::mutex> lk(g_mu);
+  Workspace& w = g_ws[dev];
+  cudaError_t e = cudaDeviceSynchronize();
+  if (w.part_o) cudaFree(w.part_o);
+  if (w.part_lse) cudaFree(w.part_lse);
+  if (w.status) cudaFree(w.status);
+  w = Workspace();
+  return e == cudaSuccess ? MLA_OK : note_cuda(e);
+}
+
+int mla_decode_device_status(int clear) {
+  int dev, sms, cc;
+  int rc = device_info(&dev, &sms, &cc);
+  if (rc) return rc;
+  std::lock_guard<std::mutex> lk(g_mu);
+  Workspace& w = g_ws[dev];
+  if (w.status == nullptr) return MLA_OK;
+  int v = 0;
+  cudaError_t e = cudaMemcpy(&v, w.status, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return note_cuda(e);
+  if (clear && v && (e = cudaMemset(w.status, 0, sizeof(int))) != cudaSuccess) return note_cuda(e);
+  return (v & mla::kStatusTimeout) ? MLA_ERR_TIMEOUT : MLA_OK;
+}
+
+int mla_decode(const void* q, const void* kv, const void* kv_scale, const int32_t* kv_indptr, void* out, int batch,
+               int num_splits, int kv_dtype, void* stream) {
+  if (q == nullptr || kv == nullptr || kv_indptr == nullptr || out == nullptr) return MLA_ERR_INVALID_ARG;
+  if (batch <= 0 || num_splits > mla::kMaxSplits) return MLA_ERR_INVALID_ARG;
+  if (kv_dtype != MLA_KV_BF16 && kv_dtype != MLA_KV_FP8_E4M3 && kv_dtype != MLA_KV_MXFP4) return MLA_ERR_INVALID_ARG;
+  if (kv_dtype != MLA_KV_BF16 && kv_scale == nullptr) return MLA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(kv, 16) || !aligned(out, 8) || !aligned(kv_indptr, 4)) return MLA_ERR_INVALID_ARG;
+  if (kv_dtype == MLA_KV_FP8_E4M3 && !aligned(kv_scale, 4)) return MLA_ERR_INVALID_ARG;
+  if (kv_dtype == MLA_KV_MXFP4) return MLA_ERR_UNSUPPORTED;  // not built yet
+
+  int dev, sms, cc;
+  int rc = device_info(&dev, &sms, &cc);
+  if (rc) return rc;
+  if (cc != 103) return MLA_ERR_UNSUPPORTED;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int ns = num_splits >= 1 ? num_splits : 0;
+  const long long grid_ll = ns >= 1 ? static_cast<long long>(batch) * ns : sms;
+  if (grid_ll > 0x7fffffffLL) return MLA_ERR_INVALID_ARG;
+
+  Workspace ws;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    rc = ensure_workspace(dev, slots_needed(batch, ns, sms));
+    if (rc) return rc;
+    ws = g_ws[dev];
+  }
+
+  mla::DecodeParams p;
+  rc = encode_kv_map(&p.tmap, kv, kv_dtype);
+  if (rc) return rc;
+  p.q = static_cast<const uint16_t*>(q);
+  p.kv = static_cast<const uint8_t*>(kv);
+  p.kv_scale = kv_scale;
+  p.kv_indptr = kv_indptr;
+  p.out = static_cast<uint16_t*>(out);
+  p.part_o = ws.part_o;
+  p.part_lse = ws.part_lse;
+  p.status = ws.status;
+  p.batch = batch;
+  p.num_splits = ns;
+  p.num_ctas = static_cast<int>(grid_ll);
+  p.logit_scale_log2 = static_cast<float>((1.0 / std::sqrt(static_cast<double>(mla::kDim))) * 1.4426950408889634);
+  p.wait_limit_ns = g_wait_limit_ns;
+
+  ProfRecord rec{nullptr, nullptr, nullptr};
+  bool prof = false;
+  {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    prof = g_prof_on;
+  }
+  if (prof) {
+    cudaEventCreate(&rec.start);
+    cudaEventCreate(&rec.split_end);
+    cudaEventCreate(&rec.end);
+    cudaEventRecord(rec.start, st);
+  }
+  cudaError_t e = mla::launch_split(kv_dtype, p, static_cast<int>(grid_ll), st);
+  if (e != cudaSuccess) return note_cuda(e);
+  if (prof) cudaEventRecord(rec.split_end, st);
+  if (ns != 1) {
+    mla::CombineParams c;
+    c.kv_indptr = kv_indptr;
+    c.part_o = ws.part_o;
+    c.part_lse = ws.part_lse;
+    c.out = static_cast<uint16_t*>(out);
+    c.batch = batch;
+    c.num_splits = ns;
+    c.num_ctas = static_cast<int>(grid_ll);
+    e = mla::launch_combine(c, st);
+    if (e != cudaSuccess) return note_cuda(e);
+  }
+  if (prof) {
+    cudaEventRecord(rec.end, st);
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    g_prof.push_back(rec);
+  }
+  return MLA_OK;
+}
+
+int mla_decode_profile_begin(void) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  for (auto& r : g_prof) {
+    cudaEventDestroy(r.start);
+    cudaEventDestroy(r.split_end);
+    cudaEventDestroy(r.end);
+  }
+  g_prof.clear();
+  g_prof_on = true;
+  return MLA_OK;
+}
+
+int mla_decode_profile_end(double* split_ms, double* call_ms, int* calls) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  g_prof_on = false;
+  double s = 0.0, t = 0.0;
+  int n = 0;
+  int rc = MLA_OK;
+  for (auto& r : g_prof) {
+    float a = 0.f, b = 0.f;
+    cudaError_t e1 = cudaEventSynchronize(r.end);
+    cudaError_t e2 = cudaEventElapsedTime(&a, r.start, r.split_end);
+    cudaError_t e3 = cudaEventElapsedTime(&b, r.start, r.end);
+    if (e1 != cudaSuccess || e2 != cudaSuccess || e3 != cudaSuccess) {
+      rc = note_cuda(e1 != cudaSuccess ? e1 : (e2 != cudaSuccess ? e2 : e3));
+    } else {
+      s += a;
+      t += b;
+      ++n;
+    }
+    cudaEventDestroy(r.start);
+    cudaEventDestroy(r.split_end);
+    cudaEventDestroy(r.end);
+  }
+  g_prof.clear();
+  if (split_ms) *split_ms = s;
+  if (call_ms) *call_ms = t;
+  if (calls) *calls = n;
+  return rc;
+}
+
+}  // extern "C"

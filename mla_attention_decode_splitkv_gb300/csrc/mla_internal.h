@@ -1,0 +1,55 @@
+// mla_internal.h -- parameters shared by the host launcher and the device kernels.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace mla {
+
+constexpr int kHeads = 16;
+constexpr int kDim = 576;
+constexpr int kDimV = 512;
+constexpr int kBN = 128;           // cached tokens per tile (= UMMA M)
+constexpr int kMxBlock = 32;
+constexpr int kMxPacked = 288;     // bytes of e2m1 nibbles per row
+constexpr int kMxScales = 18;      // e8m0 scales per row
+constexpr int kMaxSplits = 4096;
+constexpr int kBalancedMinTokens = 256;  // fewest tokens a persistent CTA is given
+
+// Status bits of the device status word.
+constexpr int kStatusTimeout = 1;
+
+struct DecodeParams {
+  CUtensorMap tmap;                // KV rows as a 2D tensor (bf16 / fp8 caches)
+  const uint16_t* q;               // bf16 bits [batch][16][576]
+  const uint8_t* kv;               // raw cache base
+  const void* kv_scale;            // fp8: const float*; mxfp4: const uint8_t* [T][18]
+  const int32_t* kv_indptr;        // [batch + 1]
+  uint16_t* out;                   // bf16 bits [batch][16][512]
+  float* part_o;                   // [slots][16][512] normalised partial outputs
+  float* part_lse;                 // [slots][16]      log2-domain log-sum-exp of the partials
+  int* status;                     // device status word
+  int batch;
+  int num_splits;                  // >= 1: uniform splits per sequence; 0: balanced over CTAs
+  int num_ctas;                    // grid size (balanced mode: persistent CTAs)
+  float logit_scale_log2;          // sm_scale * log2(e)
+  unsigned long long wait_limit_ns;
+};
+
+struct CombineParams {
+  const int32_t* kv_indptr;
+  const float* part_o;
+  const float* part_lse;
+  uint16_t* out;
+  int batch;
+  int num_splits;                  // >= 2 uniform, 0 balanced
+  int num_ctas;                    // balanced mode grid of the split kernel
+};
+
+// Per-kv-dtype launch geometry (host side).
+int split_threads(int kv_dtype);
+size_t split_smem_bytes(int kv_dtype);
+cudaError_t launch_split(int kv_dtype, const DecodeParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
+
+}  // namespace mla

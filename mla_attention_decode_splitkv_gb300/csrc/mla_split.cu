@@ -1,0 +1,807 @@
+// mla_split.cu -- split-KV flash-decode kernel (tcgen05 / TMA, sm_103a) and the
+// log-sum-exp combine kernel for single-token MLA decode.
+//
+// Method (amd-mixed-mla submissions 727205 `mla_s1`/`mla_rd`, 700955 `mla_attn_v71`/
+// `reduce_lse_v71`, 599694 `_flash_fp8_split_s1`/`_s2`): every (sequence, split) pair
+// runs an online softmax over its cached rows and emits a normalised partial output plus
+// its log-sum-exp; a combine step merges the partials.  The GB300 design:
+//
+//  * "swap-AB" tensor-core formulation, so the 16 heads sit on the MMA's N side:
+//        S^T[128 tok x 16 h]   = K_tile[128 x 576] . Q^T          (UMMA M = 128 tokens)
+//        O^T[512 dim x 16 h]  += V_tile^T[512 x 128] . P^T        (4 UMMAs of M = 128 dims)
+//    K_tile and V_tile are the same shared-memory bytes (V = first 512 columns of a
+//    cached row): K-major for QK^T, MN-major for PV.  Accumulators live in TMEM.
+//  * fp8 caches feed the e4m3 tensor cores directly (kind::f8f6f4, no dequantisation);
+//    q and P are carried exactly-enough as two e4m3 terms (hi + lo/16) stacked on N, so
+//    N = 32 and the contraction error stays at the bf16 level.  The per-tensor kv_scale
+//    is folded into the logit multiplier and the final output.
+//  * bf16 caches use kind::f16 with bf16 q and P (N = 16).
+//  * KV rows stream HBM -> SMEM with 2D TMA (128B swizzle) through an mbarrier ring that
+//    one producer warp fills; one warp issues all MMAs; four warps run the online
+//    softmax (one token per thread, lanes of TMEM), the rare lazy O rescale in TMEM and
+//    the epilogue.
+//  * Online softmax in the log2 domain with a lazy reference maximum: O is rescaled only
+//    when a tile's maximum exceeds the reference by more than kTau (log2 units).
+//
+// Every pipeline wait is bounded: on timeout the kernel sets the device status word and
+// all roles leave their loops; in-flight copies and MMAs are drained (bounded) before the
+// tensor memory is released.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
+#include "mla_internal.h"
+#include "ptx.cuh"
+
+namespace mla {
+using namespace ptx;
+
+namespace {
+
+constexpr float kNegInf = -__builtin_huge_valf();
+
+// ---------------------------------------------------------------- per-dtype geometry
+template <int KV>
+struct Cfg;
+template <>
+struct Cfg<0> {                    // bf16 cache
+  static constexpr int kSlotBytes = 32768;   // two [128 x 64 bf16] SW128 boxes
+  static constexpr int kRing = 6;
+  static constexpr int kSPT = 5;             // slots per tile: 4 x 128 value dims + rope
+  static constexpr bool kOverlap = false;    // ring < 2 tiles: QK(t+1) waits for PV(t)
+  static constexpr int kN = 16;
+  static constexpr int kQBytes = 9 * 2048;   // 9 chunks of [16 rows x 128 B]
+  static constexpr int kTmemCols = 128;
+  static constexpr int kSCols = 16;
+  static constexpr int kOCols = 16;
+  static constexpr float kTau = 8.0f;
+  static constexpr int kThreads = 192;
+};
+template <>
+struct Cfg<1> {                    // fp8 e4m3 cache
+  static constexpr int kSlotBytes = 16384;   // one [128 x 128 B] SW128 box
+  static constexpr int kRing = 12;
+  static constexpr int kSPT = 5;
+  static constexpr bool kOverlap = true;     // QK(t+1) runs while softmax(t) works
+  static constexpr int kN = 32;              // 16 hi heads + 16 lo heads
+  static constexpr int kQBytes = 5 * 4096;   // 5 chunks of [32 rows x 128 B]
+  static constexpr int kTmemCols = 256;
+  static constexpr int kSCols = 32;
+  static constexpr int kOCols = 32;
+  static constexpr float kTau = 4.0f;        // P <= 16 -> 16 P <= 256 fits e4m3
+  static constexpr int kThreads = 192;
+};
+
+constexpr int kPBytes = 4096;      // one P^T buffer: [128 tokens x 32 B] SW32
+
+struct SharedState {
+  uint64_t full[16];
+  uint64_t empty[16];
+  uint64_t q_ready;
+  uint64_t s_full[2];
+  uint64_t s_free[2];
+  uint64_t p_full[2];
+  uint64_t pv_done[2];
+  uint64_t o_free;
+  uint64_t mma_done;
+  float red[2][4][16];
+  float lsum[4][16];
+  float qscale[16];
+  uint32_t tmem_base;
+  int abort;
+};
+
+template <int KV>
+constexpr size_t smem_bytes() {
+  return 1024 + (size_t)Cfg<KV>::kRing * Cfg<KV>::kSlotBytes + Cfg<KV>::kQBytes + 2 * kPBytes + sizeof(SharedState);
+}
+
+// ---------------------------------------------------------------- work decomposition
+struct Seg {
+  int b;       // batch row
+  int row0;    // kv_indptr[b]
+  int n_lo;    // token range [n_lo, n_hi) within the sequence
+  int n_hi;
+  int slot;    // partial-result slot (when !direct)
+  bool direct; // the range is the whole sequence: write the bf16 output directly
+};
+
+__device__ __forceinline__ int balanced_ctas(long long total, int G) {
+  long long need = (total + kBalancedMinTokens - 1) / kBalancedMinTokens;
+  if (need < 1) need = 1;
+  return static_cast<int>(need < G ? need : G);
+}
+__device__ __forceinline__ long long cta_lo(int c, long long total, int Ge) {
+  return static_cast<long long>(c) * total / Ge;
+}
+// Largest CTA index whose range starts at or before token x.
+__device__ __forceinline__ int cta_of_token(long long x, long long total, int Ge) {
+  int lo = 0, hi = Ge - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (cta_lo(mid, total, Ge) <= x) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
+// Enumerates the (sequence, token range) segments one CTA works on.
+//  uniform (num_splits >= 1): CTA = b * ns + s, one segment (possibly empty), chunk rule
+//     chunk = ceil(ceil(L/ns)/BN)*BN (amd-mixed-mla submission 727205, `mla_s1`).
+//  balanced (num_splits == 0): CTA c owns tokens [c*T/G, (c+1)*T/G) of the concatenated
+//     batch (T = kv_indptr[batch]); each sequence it touches is one non-empty segment;
+//     partial slot = b + c (unique: the (b, c) pairs form a monotone staircase).
+struct SegIter {
+  long long lo, hi;
+  int b, split, ns, cta;
+  bool uniform, done;
+
+  __device__ void init(const DecodeParams& p, int c) {
+    cta = c;
+    done = false;
+    if (p.num_splits >= 1) {
+      uniform = true;
+      ns = p.num_splits;
+      b = c / ns;
+      split = c % ns;
+      return;
+    }
+    uniform = false;
+    long long total = p.kv_indptr[p.batch];
+    int Ge = balanced_ctas(total, p.num_ctas);
+    if (total <= 0 || c >= Ge) { done = true; return; }
+    lo = cta_lo(c, total, Ge);
+    hi = cta_lo(c + 1, total, Ge);
+    int l = 0, h = p.batch - 1;                 // first b with kv_indptr[b+1] > lo
+    while (l < h) {
+      int mid = (l + h) >> 1;
+      if (p.kv_indptr[mid + 1] > lo) h = mid; else l = mid + 1;
+    }
+    b = l;
+  }
+
+  __device__ bool next(const DecodeParams& p, Seg& s) {
+    if (done) return false;
+    if (uniform) {
+      int r0 = p.kv_indptr[b];
+      long long L = static_cast<long long>(p.kv_indptr[b + 1]) - r0;
+      long long per = (L + ns - 1) / ns;
+      long long chunk = ((per + kBN - 1) / kBN) * kBN;
+      long long a = split * chunk, e = a + chunk;
+      if (a > L) a = L;
+      if (e > L) e = L;
+      s.b = b; s.row0 = r0; s.n_lo = (int)a; s.n_hi = (int)e;
+      s.slot = b * ns + split; s.direct = (ns == 1);
+      done = true;
+      return true;
+    }
+    while (b < p.batch) {
+      int r0 = p.kv_indptr[b], r1 = p.kv_indptr[b + 1];
+      if (r0 >= hi) break;
+      long long a = lo > r0 ? lo : r0, e = hi < r1 ? hi : r1;
+      int bb = b++;
+      if (e > a) {
+        s.b = bb; s.row0 = r0; s.n_lo = (int)(a - r0); s.n_hi = (int)(e - r0);
+        s.slot = bb + cta; s.direct = (a == r0 && e == r1);
+        return true;
+      }
+    }
+    done = true;
+    return false;
+  }
+};
+
+// The 128-row TMA window of tile t of a segment.  The window never extends past the
+// segment's last row (it is shifted back instead; rows before 0 are zero-filled by TMA),
+// so the kernel reads no row outside [0, kv_indptr[batch]).
+struct Window {
+  int y0;     // first cached row of the window (may be negative)
+  int shift;  // window row of the tile's first token
+  int cnt;    // valid tokens in the tile
+};
+__device__ __forceinline__ Window tile_window(const Seg& s, int t) {
+  int row_start = s.row0 + s.n_lo + t * kBN;
+  int row_hi = s.row0 + s.n_hi;
+  int y0 = min(row_start, row_hi - kBN);
+  Window w;
+  w.y0 = y0;
+  w.shift = row_start - y0;
+  w.cnt = min(kBN, row_hi - row_start);
+  return w;
+}
+
+__device__ __forceinline__ float bf16_bits_to_f(uint32_t b) { return __uint_as_float(b << 16); }
+
+__device__ __forceinline__ uint16_t f_to_bf16_bits(float f) {
+  __nv_bfloat16 h = __float2bfloat16_rn(f);
+  return *reinterpret_cast<uint16_t*>(&h);
+}
+
+__device__ __forceinline__ uint32_t pack_e4m3x2(float lo, float hi) {
+  return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3));
+}
+__device__ __forceinline__ float2 unpack_e4m3x2(uint32_t v) {
+  __half2_raw r = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(v & 0xFFFFu), __NV_E4M3);
+  __half2 h = *reinterpret_cast<__half2*>(&r);
+  return __half22float2(h);
+}
+
+// ---------------------------------------------------------------- q staging
+// bf16: Q[16 x 576] -> 9 K-major SW128 chunks [16 rows x 128 B].
+__device__ void stage_q_bf16(const DecodeParams& p, int b, uint8_t* qs, int ts) {
+  const uint4* src = reinterpret_cast<const uint4*>(p.q + static_cast<size_t>(b) * kHeads * kDim);
+  for (int i = ts; i < kHeads * 72; i += 128) {
+    int h = i / 72, pc = i % 72;
+    int c = pc >> 3, j = pc & 7;
+    uint4 v = __ldg(src + h * 72 + pc);
+    *reinterpret_cast<uint4*>(qs + c * 2048 + h * 128 + ((j ^ (h & 7)) << 4)) = v;
+  }
+}
+
+// fp8 path: per head h, q*2^a_h = hi + lo/16 with hi, lo e4m3 (exact for every bf16 q whose
+// scaled magnitude is >= 2^-6; a_h puts the head's max near 2^8).  Rows 0-15 of each
+// [32 x 128 B] chunk hold hi, rows 16-31 hold lo.  qscale[h] = 2^-a_h.
+__device__ void stage_q_fp8(const DecodeParams& p, int b, uint8_t* qs, float* qscale, int ts) {
+  const int h = ts >> 3, t8 = ts & 7;
+  const uint4* src = reinterpret_cast<const uint4*>(p.q + (static_cast<size_t>(b) * kHeads + h) * kDim + 72 * t8);
+  uint4 v[9];
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 9; ++i) {
+    v[i] = __ldg(src + i);
+    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      amax = fmaxf(amax, fabsf(bf16_bits_to_f(w[k] & 0xFFFFu)));
+      amax = fmaxf(amax, fabsf(bf16_bits_to_f(w[k] >> 16)));
+    }
+  }
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+  int e = 0;
+  frexpf(amax, &e);
+  const int a = amax > 0.f ? 8 - e : 0;
+  const float sc = ldexpf(1.0f, a);
+  if (t8 == 0) qscale[h] = ldexpf(1.0f, -a);
+#pragma unroll
+  for (int i = 0; i < 9; ++i) {
+    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+    uint32_t hi[2], lo[2];
+#pragma unroll
+    for (int k = 0; k < 4; k += 2) {
+      float y0 = bf16_bits_to_f(w[k] & 0xFFFFu) * sc, y1 = bf16_bits_to_f(w[k] >> 16) * sc;
+      float y2 = bf16_bits_to_f(w[k + 1] & 0xFFFFu) * sc, y3 = bf16_bits_to_f(w[k + 1] >> 16) * sc;
+      uint32_t h01 = pack_e4m3x2(y0, y1), h23 = pack_e4m3x2(y2, y3);
+      float2 d01 = unpack_e4m3x2(h01), d23 = unpack_e4m3x2(h23);
+      uint32_t l01 = pack_e4m3x2((y0 - d01.x) * 16.f, (y1 - d01.y) * 16.f);
+      uint32_t l23 = pack_e4m3x2((y2 - d23.x) * 16.f, (y3 - d23.y) * 16.f);
+      hi[k >> 1] = h01 | (h23 << 16);
+      lo[k >> 1] = l01 | (l23 << 16);
+    }
+    const int f0 = 72 * t8 + 8 * i;
+    const int c = f0 >> 7, jb = f0 & 127, piece = jb >> 4, half = (jb >> 3) & 1;
+    const int off = ((piece ^ (h & 7)) << 4) + half * 8;
+    *reinterpret_cast<uint2*>(qs + c * 4096 + h * 128 + off) = make_uint2(hi[0], hi[1]);
+    *reinterpret_cast<uint2*>(qs + c * 4096 + (16 + h) * 128 + off) = make_uint2(lo[0], lo[1]);
+  }
+}
+
+// ---------------------------------------------------------------- producer (1 thread)
+template <int KV>
+__device__ void run_producer(const DecodeParams& p, SharedState* sh, uint8_t* ring) {
+  using C = Cfg<KV>;
+  volatile int* abortf = &sh->abort;
+  SegIter it;
+  it.init(p, blockIdx.x);
+  Seg s;
+  uint32_t idx = 0;
+  bool ok = true;
+  while (ok && it.next(p, s)) {
+    const int n = s.n_hi - s.n_lo;
+    if (n <= 0) continue;
+    const int ntiles = (n + kBN - 1) / kBN;
+    for (int t = 0; t < ntiles && ok; ++t) {
+      const Window w = tile_window(s, t);
+      for (int c = 0; c < C::kSPT; ++c) {
+        const uint32_t slot = idx % C::kRing, use = idx / C::kRing;
+        if (!wait_bar(smem_u32(&sh->empty[slot]), (use & 1) ^ 1, abortf, p.status, p.wait_limit_ns)) {
+          ok = false;
+          break;
+        }
+        const uint32_t dst = smem_u32(ring + slot * C::kSlotBytes);
+        const uint32_t fb = smem_u32(&sh->full[slot]);
+        if constexpr (KV == 0) {
+          if (c < 4) {
+            mbar_arrive_expect_tx(fb, 32768);
+            tma_load_2d(dst, &p.tmap, 128 * c, w.y0, fb);
+            tma_load_2d(dst + 16384, &p.tmap, 128 * c + 64, w.y0, fb);
+          } else {
+            mbar_arrive_expect_tx(fb, 16384);
+            tma_load_2d(dst, &p.tmap, 512, w.y0, fb);
+          }
+        } else {
+          mbar_arrive_expect_tx(fb, 16384);
+          tma_load_2d(dst, &p.tmap, 128 * c, w.y0, fb);
+        }
+        ++idx;
+      }
+    }
+  }
+  if (!ok) {  // drain copies already issued so that none lands after the CTA exits
+    const uint32_t first = idx > (uint32_t)C::kRing ? idx - C::kRing : 0u;
+    for (uint32_t j = first; j < idx; ++j)
+      wait_bar(smem_u32(&sh->full[j % C::kRing]), (j / C::kRing) & 1, abortf, p.status, p.wait_limit_ns, false);
+  }
+}
+
+// ---------------------------------------------------------------- MMA issuer (1 thread)
+template <int KV>
+__device__ bool issue_qk(const DecodeParams& p, SharedState* sh, uint8_t* ring, uint32_t qaddr, uint32_t tmem,
+                         uint32_t g) {
+  using C = Cfg<KV>;
+  constexpr uint32_t idq = instr_desc(KV == 0 ? 1u : 0u, 0, 0, 128, C::kN);
+  volatile int* abortf = &sh->abort;
+  if (g >= 2 && !wait_bar(smem_u32(&sh->s_free[g & 1]), ((g >> 1) & 1) ^ 1, abortf, p.status, p.wait_limit_ns))
+    return false;
+  tc_fence_after();
+  const uint32_t d = tmem + (g & 1) * C::kSCols;
+  for (int c = 0; c < C::kSPT; ++c) {
+    const uint32_t idx = g * C::kSPT + c, slot = idx % C::kRing;
+    if (!wait_bar(smem_u32(&sh->full[slot]), (idx / C::kRing) & 1, abortf, p.status, p.wait_limit_ns)) return false;
+    tc_fence_after();
+    const uint32_t a = smem_u32(ring + slot * C::kSlotBytes);
+    if constexpr (KV == 0) {
+      const int nsub = c < 4 ? 2 : 1;
+      for (int j = 0; j < nsub; ++j)
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          mma_f16(d, smem_desc(a + j * 16384 + 32 * k, 16, 1024, kSwizzle128B),
+                  smem_desc(qaddr + (2 * c + j) * 2048 + 32 * k, 16, 1024, kSwizzle128B), idq, (c | j | k) != 0);
+    } else {
+      const int nk = c < 4 ? 4 : 2;
+      for (int k = 0; k < nk; ++k)
+        mma_f8(d, smem_desc(a + 32 * k, 16, 1024, kSwizzle128B),
+               smem_desc(qaddr + c * 4096 + 32 * k, 16, 1024, kSwizzle128B), idq, (c | k) != 0);
+    }
+    if (c == C::kSPT - 1) mma_commit(smem_u32(&sh->empty[slot]));  // rope slot: QK only
+  }
+  mma_commit(smem_u32(&sh->s_full[g & 1]));
+  return true;
+}
+
+template <int KV>
+__device__ bool issue_pv(const DecodeParams& p, SharedState* sh, uint8_t* ring, uint8_t* ps, uint32_t tmem,
+                         uint32_t g, bool first, int kseg) {
+  using C = Cfg<KV>;
+  constexpr uint32_t idp = instr_desc(KV == 0 ? 1u : 0u, 1, 1, 128, C::kN);
+  volatile int* abortf = &sh->abort;
+  if (!wait_bar(smem_u32(&sh->p_full[g & 1]), (g >> 1) & 1, abortf, p.status, p.wait_limit_ns)) return false;
+  if (first && kseg > 0 &&
+      !wait_bar(smem_u32(&sh->o_free), (kseg - 1) & 1, abortf, p.status, p.wait_limit_ns))
+    return false;
+  tc_fence_after();
+  const uint32_t pb = smem_u32(ps + (g & 1) * kPBytes);
+  for (int m = 0; m < 4; ++m) {
+    const uint32_t idx = g * C::kSPT + m, slot = idx % C::kRing;
+    const uint32_t a = smem_u32(ring + slot * C::kSlotBytes);
+    const uint32_t d = tmem + 2 * C::kSCols + m * C::kOCols;
+    if constexpr (KV == 0) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        mma_f16(d, smem_desc(a + 2048 * k, 16384, 1024, kSwizzle128B), smem_desc(pb + 512 * k, 0, 256, kSwizzle32B),
+                idp, !(first && k == 0));
+    } else {
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        mma_f8(d, smem_desc(a + 4096 * k, 16384, 1024, kSwizzle128B), smem_desc(pb + 1024 * k, 0, 256, kSwizzle32B),
+               idp, !(first && k == 0));
+    }
+    mma_commit(smem_u32(&sh->empty[slot]));
+  }
+  mma_commit(smem_u32(&sh->pv_done[g & 1]));
+  return true;
+}
+
+template <int KV>
+__device__ void run_mma(const DecodeParams& p, SharedState* sh, uint8_t* ring, uint8_t* qs, uint8_t* ps,
+                        uint32_t tmem) {
+  using C = Cfg<KV>;
+  volatile int* abortf = &sh->abort;
+  const uint32_t qaddr = smem_u32(qs);
+  SegIter it;
+  it.init(p, blockIdx.x);
+  Seg s;
+  uint32_t g = 0;
+  int kseg = 0;
+  bool ok = true, pend = false, pend_first = false;
+  uint32_t pend_g = 0;
+  int pend_k = 0;
+  while (ok && it.next(p, s)) {
+    const int n = s.n_hi - s.n_lo;
+    if (n <= 0) continue;
+    if (!wait_bar(smem_u32(&sh->q_ready), kseg & 1, abortf, p.status, p.wait_limit_ns)) { ok = false; break; }
+    const int ntiles = (n + kBN - 1) / kBN;
+    for (int t = 0; t < ntiles; ++t) {
+      if (!issue_qk<KV>(p, sh, ring, qaddr, tmem, g)) { ok = false; break; }
+      if (C::kOverlap) {
+        if (pend && !issue_pv<KV>(p, sh, ring, ps, tmem, pend_g, pend_first, pend_k)) { ok = false; break; }
+        pend = true;
+        pend_g = g;
+        pend_first = (t == 0);
+        pend_k = kseg;
+      } else if (!issue_pv<KV>(p, sh, ring, ps, tmem, g, t == 0, kseg)) {
+        ok = false;
+        break;
+      }
+      ++g;
+    }
+    ++kseg;
+  }
+  if (ok && C::kOverlap && pend) issue_pv<KV>(p, sh, ring, ps, tmem, pend_g, pend_first, pend_k);
+  // every MMA issued so far must finish before the tensor memory is released
+  mma_commit(smem_u32(&sh->mma_done));
+  wait_bar(smem_u32(&sh->mma_done), 0, abortf, p.status, p.wait_limit_ns, false);
+}
+
+// ---------------------------------------------------------------- softmax / epilogue (128 threads)
+template <int KV>
+__device__ void write_empty_result(const DecodeParams& p, const Seg& s, int ts) {
+  if (s.direct) {
+    uint32_t* o = reinterpret_cast<uint32_t*>(p.out + static_cast<size_t>(s.b) * kHeads * kDimV);
+    for (int i = ts; i < kHeads * kDimV / 2; i += 128) o[i] = 0u;
+  } else if (ts < kHeads) {
+    p.part_lse[s.slot * kHeads + ts] = kNegInf;
+  }
+}
+
+template <int KV>
+__device__ void run_softmax(const DecodeParams& p, SharedState* sh, uint8_t* qs, uint8_t* ps, uint32_t tmem) {
+  using C = Cfg<KV>;
+  volatile int* abortf = &sh->abort;
+  const int ts = threadIdx.x - 64;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int quarter = warp & 3;
+  const int row = quarter * 32 + lane;                     // token row of the tile = TMEM lane
+  const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+  const float kv_scale = (KV == 1) ? __ldg(reinterpret_cast<const float*>(p.kv_scale)) : 1.0f;
+  const float xscale = p.logit_scale_log2 * kv_scale;    // raw dot product -> log2-domain logit
+
+  SegIter it;
+  it.init(p, blockIdx.x);
+  Seg cur, nxt;
+  bool has_cur = it.next(p, cur);
+  if (has_cur && cur.n_hi > cur.n_lo) {
+    if (KV == 0) stage_q_bf16(p, cur.b, qs, ts); else stage_q_fp8(p, cur.b, qs, sh->qscale, ts);
+    fence_proxy_async_smem();
+    mbar_arrive(smem_u32(&sh->q_ready));
+  }
+  bar_sync(1, 128);  // qscale visible to all softmax threads
+  uint32_t g = 0;
+  bool ok = true;
+  while (ok && has_cur) {
+    const int n = cur.n_hi - cur.n_lo;
+    if (n <= 0) {
+      write_empty_result<KV>(p, cur, ts);
+      has_cur = it.next(p, cur);
+      continue;
+    }
+    const int ntiles = (n + kBN - 1) / kBN;
+    float mref[16], lpart[16];
+    bool has_nxt = false;
+    for (int t = 0; t < ntiles; ++t) {
+      const Window w = tile_window(cur, t);
+      bool okw = wait_bar(smem_u32(&sh->s_full[g & 1]), (g >> 1) & 1, abortf, p.status, p.wait_limit_ns);
+      okw = __all_sync(0xffffffffu, okw);
+      tc_fence_after();
+      uint32_t r[C::kSCols];
+      if (okw) {
+        const uint32_t ta = tmem + lane_base + (g & 1) * C::kSCols;
+        uint32_t (&r0)[16] = *reinterpret_cast<uint32_t(*)[16]>(&r[0]);
+        tmem_ld16(ta, r0);
+        if constexpr (C::kSCols == 32) {
+          uint32_t (&r1)[16] = *reinterpret_cast<uint32_t(*)[16]>(&r[C::kSCols - 16]);
+          tmem_ld16(ta + 16, r1);
+        }
+        tmem_wait_ld();
+      }
+      tc_fence_before();
+      mbar_arrive(smem_u32(&sh->s_free[g & 1]));
+      const bool valid = okw && row >= w.shift && row < w.shift + w.cnt;
+      float x[16];
+#pragma unroll
+      for (int h = 0; h < 16; ++h) {
+        float sdot;
+        if constexpr (KV == 0) sdot = __uint_as_float(r[h]);
+        else sdot = (__uint_as_float(r[h]) + __uint_as_float(r[16 + h]) * 0.0625f) * sh->qscale[h];
+        x[h] = valid ? sdot * xscale : kNegInf;
+      }
+      float* red = &sh->red[g & 1][quarter][0];
+#pragma unroll
+      for (int h = 0; h < 16; ++h) {
+        const float m = warp_max(x[h]);
+        if (lane == 0) red[h] = m;
+      }
+      ok = bar_and(1, 128, okw);
+      if (!ok) break;
+      float M[16];
+#pragma unroll
+      for (int h = 0; h < 16; ++h)
+        M[h] = fmaxf(fmaxf(sh->red[g & 1][0][h], sh->red[g & 1][1][h]), fmaxf(sh->red[g & 1][2][h], sh->red[g & 1][3][h]));
+      bool need = false;
+      if (t == 0) {
+#pragma unroll
+        for (int h = 0; h < 16; ++h) { mref[h] = M[h]; lpart[h] = 0.f; }
+      } else {
+#pragma unroll
+        for (int h = 0; h < 16; ++h) need |= (M[h] > mref[h] + C::kTau);
+      }
+      if (need) {  // lazy rescale of O^T in TMEM (uniform decision across the 128 threads)
+        float alpha[16];
+#pragma unroll
+        for (int h = 0; h < 16; ++h) {
+          const float nm = fmaxf(mref[h], M[h]);
+          alpha[h] = ex2(mref[h] - nm);
+          mref[h] = nm;
+          lpart[h] *= alpha[h];
+        }
+        const uint32_t gp = g - 1;
+        bool ok2 = wait_bar(smem_u32(&sh->pv_done[gp & 1]), (gp >> 1) & 1, abortf, p.status, p.wait_limit_ns);
+        ok2 = __all_sync(0xffffffffu, ok2);
+        if (ok2) {
+          tc_fence_after();
+#pragma unroll 1
+          for (int m = 0; m < 4; ++m) {
+#pragma unroll
+            for (int cb = 0; cb < C::kOCols; cb += 16) {
+              const uint32_t ta = tmem + lane_base + 2 * C::kSCols + m * C::kOCols + cb;
+              uint32_t v[16];
+              tmem_ld16(ta, v);
+              tmem_wait_ld();
+#pragma unroll
+              for (int j = 0; j < 16; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha[j]);
+              tmem_st16(ta, v);
+            }
+          }
+          tmem_wait_st();
+        }
+        ok = bar_and(1, 128, ok2);
+        if (!ok) break;
+      }
+      // P = 2^(x - mref) <= 2^kTau
+      float P[16];
+#pragma unroll
+      for (int h = 0; h < 16; ++h) P[h] = ex2(x[h] - mref[h]);
+      if (g >= 2) wait_bar(smem_u32(&sh->pv_done[g & 1]), ((g >> 1) & 1) ^ 1, abortf, p.status, p.wait_limit_ns);
+      uint8_t* prow = ps + (g & 1) * kPBytes + row * 32;
+      const int sw = (row >> 2) & 1;
+      uint32_t c0[4], c1[4];
+      if constexpr (KV == 0) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint16_t b0 = f_to_bf16_bits(P[2 * j]), b1 = f_to_bf16_bits(P[2 * j + 1]);
+          lpart[2 * j] += bf16_bits_to_f(b0);
+          lpart[2 * j + 1] += bf16_bits_to_f(b1);
+          const uint32_t wv = static_cast<uint32_t>(b0) | (static_cast<uint32_t>(b1) << 16);
+          if (j < 4) c0[j] = wv; else c1[j - 4] = wv;
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint32_t hw = 0, lw = 0;
+#pragma unroll
+          for (int k = 0; k < 4; k += 2) {
+            const int h = 4 * j + k;
+            const float y0 = P[h] * 16.f, y1 = P[h + 1] * 16.f;
+            const uint32_t hp = pack_e4m3x2(y0, y1);
+            const float2 hd = unpack_e4m3x2(hp);
+            const uint32_t lp = pack_e4m3x2((y0 - hd.x) * 16.f, (y1 - hd.y) * 16.f);
+            const float2 ld = unpack_e4m3x2(lp);
+            lpart[h] += (hd.x + ld.x * 0.0625f) * 0.0625f;
+            lpart[h + 1] += (hd.y + ld.y * 0.0625f) * 0.0625f;
+            hw |= hp << (8 * k);
+            lw |= lp << (8 * k);
+          }
+          c0[j] = hw;
+          c1[j] = lw;
+        }
+      }
+      *reinterpret_cast<uint4*>(prow + ((0 ^ sw) << 4)) = make_uint4(c0[0], c0[1], c0[2], c0[3]);
+      *reinterpret_cast<uint4*>(prow + ((1 ^ sw) << 4)) = make_uint4(c1[0], c1[1], c1[2], c1[3]);
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(smem_u32(&sh->p_full[g & 1]));
+      ++g;
+      if (t == ntiles - 1) {
+        // All QK MMAs of this segment are complete (s_full of its last tile was observed):
+        // the q buffer can take the next segment's queries.
+        has_nxt = it.next(p, nxt);
+        if (has_nxt && nxt.n_hi > nxt.n_lo) {
+          if (KV == 0) stage_q_bf16(p, nxt.b, qs, ts); else stage_q_fp8(p, nxt.b, qs, sh->qscale, ts);
+          fence_proxy_async_smem();
+          mbar_arrive(smem_u32(&sh->q_ready));
+        }
+      }
+    }
+    if (!ok) break;
+    // ---- epilogue: O = O^T / l, written directly (bf16) or as a partial (fp32 + lse)
+    const uint32_t gl = g - 1;
+    bool ok4 = wait_bar(smem_u32(&sh->pv_done[gl & 1]), (gl >> 1) & 1, abortf, p.status, p.wait_limit_ns);
+    ok4 = __all_sync(0xffffffffu, ok4);
+    tc_fence_after();
+#pragma unroll
+    for (int h = 0; h < 16; ++h) {
+      float v = lpart[h];
+      v += __shfl_xor_sync(0xffffffffu, v, 16);
+      v += __shfl_xor_sync(0xffffffffu, v, 8);
+      v += __shfl_xor_sync(0xffffffffu, v, 4);
+      v += __shfl_xor_sync(0xffffffffu, v, 2);
+      v += __shfl_xor_sync(0xffffffffu, v, 1);
+      if (lane == 0) sh->lsum[quarter][h] = v;
+    }
+    ok = bar_and(1, 128, ok4);
+    if (!ok) break;
+    float inv[16];
+#pragma unroll
+    for (int h = 0; h < 16; ++h) {
+      const float l = sh->lsum[0][h] + sh->lsum[1][h] + sh->lsum[2][h] + sh->lsum[3][h];
+      inv[h] = (KV == 1 ? kv_scale * 0.0625f : 1.0f) / l;
+      if (!cur.direct && ts == 0) p.part_lse[cur.slot * kHeads + h] = mref[h] + lg2(l);
+    }
+#pragma unroll 1
+    for (int m = 0; m < 4; ++m) {
+      const uint32_t ta = tmem + lane_base + 2 * C::kSCols + m * C::kOCols;
+      uint32_t v[C::kOCols];
+      uint32_t (&v0)[16] = *reinterpret_cast<uint32_t(*)[16]>(&v[0]);
+      tmem_ld16(ta, v0);
+      if constexpr (C::kOCols == 32) {
+        uint32_t (&v1)[16] = *reinterpret_cast<uint32_t(*)[16]>(&v[C::kOCols - 16]);
+        tmem_ld16(ta + 16, v1);
+      }
+      tmem_wait_ld();
+      const int d = 128 * m + row;
+#pragma unroll
+      for (int h = 0; h < 16; ++h) {
+        float o = __uint_as_float(v[h]);
+        if constexpr (KV == 1) o += __uint_as_float(v[16 + h]) * 0.0625f;
+        o *= inv[h];
+        if (cur.direct)
+          p.out[(static_cast<size_t>(cur.b) * kHeads + h) * kDimV + d] = f_to_bf16_bits(o);
+        else
+          p.part_o[(static_cast<size_t>(cur.slot) * kHeads + h) * kDimV + d] = o;
+      }
+    }
+    tc_fence_before();
+    mbar_arrive(smem_u32(&sh->o_free));
+    cur = nxt;
+    has_cur = has_nxt;
+  }
+}
+
+// ---------------------------------------------------------------- the kernel
+template <int KV>
+__global__ void __launch_bounds__(Cfg<KV>::kThreads, 1) mla_split_kernel(const __grid_constant__ DecodeParams p) {
+  using C = Cfg<KV>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* ring = base;
+  uint8_t* qs = ring + C::kRing * C::kSlotBytes;
+  uint8_t* ps = qs + C::kQBytes;
+  SharedState* sh = reinterpret_cast<SharedState*>(ps + 2 * kPBytes);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::kRing; ++i) {
+      mbar_init(smem_u32(&sh->full[i]), 1);
+      mbar_init(smem_u32(&sh->empty[i]), 1);
+    }
+    mbar_init(smem_u32(&sh->q_ready), 128);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&sh->s_full[i]), 1);
+      mbar_init(smem_u32(&sh->s_free[i]), 128);
+      mbar_init(smem_u32(&sh->p_full[i]), 128);
+      mbar_init(smem_u32(&sh->pv_done[i]), 1);
+    }
+    mbar_init(smem_u32(&sh->o_free), 128);
+    mbar_init(smem_u32(&sh->mma_done), 1);
+    sh->abort = 0;
+    fence_barrier_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&sh->tmem_base), C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sh->tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0) run_producer<KV>(p, sh, ring);
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) run_mma<KV>(p, sh, ring, qs, ps, tmem);
+    __syncwarp();
+  } else {
+    run_softmax<KV>(p, sh, qs, ps, tmem);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------- combine
+// Per (b, h): m = max_s lse_s, w_s = 2^(lse_s - m), out = sum w_s o_s / sum w_s (bf16, RNE).
+// Splits with lse = -inf carry no weight; a row with no weight at all is written as 0.
+__global__ void __launch_bounds__(128) mla_combine_kernel(const CombineParams p) {
+  const int b = blockIdx.x >> 4, h = blockIdx.x & 15, t = threadIdx.x;
+  uint2* dst = reinterpret_cast<uint2*>(p.out + (static_cast<size_t>(b) * kHeads + h) * kDimV) + t;
+  int s0, s1;
+  if (p.num_splits >= 1) {
+    s0 = b * p.num_splits;
+    s1 = s0 + p.num_splits;
+  } else {
+    const int r0 = p.kv_indptr[b], r1 = p.kv_indptr[b + 1];
+    if (r1 <= r0) { *dst = make_uint2(0u, 0u); return; }
+    const long long total = p.kv_indptr[p.batch];
+    const int Ge = balanced_ctas(total, p.num_ctas);
+    const int cf = cta_of_token(r0, total, Ge), cl = cta_of_token(static_cast<long long>(r1) - 1, total, Ge);
+    if (cf == cl) return;  // one CTA held the whole sequence and wrote it directly
+    s0 = b + cf;
+    s1 = b + cl + 1;
+  }
+  float m = kNegInf;
+  for (int s = s0; s < s1; ++s) m = fmaxf(m, __ldg(p.part_lse + s * kHeads + h));
+  if (m == kNegInf) { *dst = make_uint2(0u, 0u); return; }
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float ws = 0.f;
+  for (int s = s0; s < s1; ++s) {
+    const float l = __ldg(p.part_lse + s * kHeads + h);
+    if (l == kNegInf) continue;
+    const float w = ex2(l - m);
+    ws += w;
+    const float4 v = __ldg(reinterpret_cast<const float4*>(p.part_o + (static_cast<size_t>(s) * kHeads + h) * kDimV) + t);
+    acc.x += w * v.x; acc.y += w * v.y; acc.z += w * v.z; acc.w += w * v.w;
+  }
+  const float inv = 1.0f / ws;
+  const uint32_t lo = static_cast<uint32_t>(f_to_bf16_bits(acc.x * inv)) | (static_cast<uint32_t>(f_to_bf16_bits(acc.y * inv)) << 16);
+  const uint32_t hi = static_cast<uint32_t>(f_to_bf16_bits(acc.z * inv)) | (static_cast<uint32_t>(f_to_bf16_bits(acc.w * inv)) << 16);
+  *dst = make_uint2(lo, hi);
+}
+
+template <int KV>
+cudaError_t launch_split_t(const DecodeParams& p, int grid, cudaStream_t stream) {
+  static int configured_device = -1;  // attribute is per function; set once per device id
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (configured_device != dev) {
+    e = cudaFuncSetAttribute(mla_split_kernel<KV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem_bytes<KV>()));
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  mla_split_kernel<KV><<<grid, Cfg<KV>::kThreads, smem_bytes<KV>(), stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int split_threads(int kv_dtype) { return kv_dtype == 0 ? Cfg<0>::kThreads : Cfg<1>::kThreads; }
+size_t split_smem_bytes(int kv_dtype) { return kv_dtype == 0 ? smem_bytes<0>() : smem_bytes<1>(); }
+
+cudaError_t launch_split(int kv_dtype, const DecodeParams& p, int grid, cudaStream_t stream) {
+  if (kv_dtype == 0) return launch_split_t<0>(p, grid, stream);
+  if (kv_dtype == 1) return launch_split_t<1>(p, grid, stream);
+  return cudaErrorNotSupported;
+}
+
+cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream) {
+  mla_combine_kernel<<<p.batch * kHeads, 128, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

@@ -1,0 +1,123 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU fp64 oracle.
+
+Tolerance: bf16 output vs the oracle on the same (dequantised) cache, atol = rtol = 2e-2
+on every element.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from mla_attention_decode_splitkv_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+ATOL = RTOL = 2e-2
+
+
+@pytest.fixture(scope="module")
+def pkg():
+    import __graft_entry__
+    __graft_entry__.build()
+    import mla_attention_decode_splitkv_gb300 as p
+    return p
+
+
+def _check(got, ref, what=""):
+    got = got.float().cpu().numpy().astype(np.float64)
+    err = np.abs(got - ref)
+    bad = err > ATOL + RTOL * np.abs(ref)
+    assert not np.isnan(got).any(), f"{what}: NaN in output"
+    assert not bad.any(), (f"{what}: {int(bad.sum())} of {bad.size} elements outside tolerance, "
+                           f"max err {err.max():.4g} at {np.unravel_index(err.argmax(), err.shape)}")
+    return err.max()
+
+
+def _run(pkg, inp, ns):
+    g = inp.to("cuda")
+    out = pkg.decode(g.q, g.kv, g.kv_scale, g.kv_indptr, inp.kv_dtype, num_splits=ns)
+    torch.cuda.synchronize()
+    assert pkg.device_status(clear=True) == pkg.MLA_OK
+    return out
+
+
+SMALL = [
+    # (kv_dtype, lens): several tiles and a ragged tail, plus short and single-token rows
+    (synth.KV_BF16, [1, 200, 300]),
+    (synth.KV_BF16, [1024, 77]),
+    (synth.KV_FP8, [1, 129, 1000, 2048]),
+    (synth.KV_FP8, [128, 256, 5, 383]),
+]
+
+
+@pytest.mark.parametrize("kv_dtype,lens", SMALL)
+@pytest.mark.parametrize("ns", [1, 2, 3, 7, 0])
+def test_small_cases_match_oracle(pkg, kv_dtype, lens, ns):
+    inp = synth.make_inputs(len(lens), lens, kv_dtype, seed=100 + sum(lens) + ns)
+    out = _run(pkg, inp, ns)
+    ref, _ = oracle.decode(inp.q, inp.kv, inp.kv_scale, inp.kv_indptr, kv_dtype)
+    _check(out, ref, f"dtype {kv_dtype} lens {lens} ns {ns}")
+
+
+@pytest.mark.parametrize("kv_dtype", [synth.KV_BF16, synth.KV_FP8])
+@pytest.mark.parametrize("ns", [1, 3, 0])
+def test_empty_and_single_token_sequences(pkg, kv_dtype, ns):
+    lens = [0, 1, 0, 300, 1]
+    inp = synth.make_inputs(len(lens), lens, kv_dtype, seed=9 + ns)
+    out = _run(pkg, inp, ns)
+    ref, _ = oracle.decode(inp.q, inp.kv, inp.kv_scale, inp.kv_indptr, kv_dtype)
+    _check(out, ref, f"empty/single ns {ns}")
+    assert torch.count_nonzero(out[0]) == 0 and torch.count_nonzero(out[2]) == 0
+
+
+@pytest.mark.parametrize("kv_dtype", [synth.KV_BF16, synth.KV_FP8])
+def test_split_count_invariance(pkg, kv_dtype):
+    inp = synth.make_inputs(2, [3000, 1500], kv_dtype, seed=31)
+    ref, _ = oracle.decode(inp.q, inp.kv, inp.kv_scale, inp.kv_indptr, kv_dtype)
+    outs = {ns: _run(pkg, inp, ns) for ns in (1, 2, 3, 7, 24, 0)}
+    for ns, o in outs.items():
+        _check(o, ref, f"ns {ns}")
+    base = outs[1].float()
+    for ns, o in outs.items():
+        assert torch.allclose(o.float(), base, atol=1e-2, rtol=1e-2), ns
+
+
+@pytest.mark.parametrize("kv_dtype", [synth.KV_BF16, synth.KV_FP8])
+def test_growing_logits_force_rescales(pkg, kv_dtype):
+    # Keys whose projection onto q grows along the sequence: the running maximum rises
+    # every tile, so the lazy O rescale path runs repeatedly.
+    L = 1200
+    g = torch.Generator().manual_seed(5)
+    q = torch.randn((1, 16, 576), generator=g).to(torch.bfloat16)
+    base = torch.randn((L, 576), generator=g) * 0.5
+    ramp = torch.linspace(0.0, 3.0, L).unsqueeze(1)
+    src = (base + ramp * q[0, 0].float().unsqueeze(0) / q[0, 0].float().norm() * 24.0 / 24.0 * 6.0).to(torch.bfloat16)
+    if kv_dtype == synth.KV_BF16:
+        kv, scale = src, None
+    else:
+        kv, scale = synth.quantize_fp8_per_tensor(src)
+    inp = synth.DecodeInputs(q, src, kv, scale, synth.indptr_from_lengths([L]), kv_dtype, [L])
+    ref, lse = oracle.decode(inp.q, inp.kv, inp.kv_scale, inp.kv_indptr, kv_dtype)
+    for ns in (1, 0):
+        _check(_run(pkg, inp, ns), ref, f"rescale ns {ns}")
+
+
+@pytest.mark.parametrize("cfg", [0, 1, 2, 4])
+def test_workload_configs_sampled_rows(pkg, cfg):
+    """Full-size workloads on the GPU in the bench's launch configuration; the oracle checks
+    sampled batch rows (first, last, and a few seeded ones)."""
+    spec = synth.CONFIGS[cfg]
+    inp = synth.make_config(cfg, device="cuda", keep_src=False)
+    out = pkg.decode(inp.q, inp.kv, inp.kv_scale, inp.kv_indptr, inp.kv_dtype, num_splits=spec.num_splits)
+    torch.cuda.synchronize()
+    assert pkg.device_status(clear=True) == pkg.MLA_OK
+    B = inp.batch
+    rows = sorted({0, B - 1} | set(np.random.default_rng(cfg).choice(B, size=min(B, 3), replace=False).tolist()))
+    ip = inp.kv_indptr.cpu().tolist()
+    scale = None if inp.kv_scale is None else inp.kv_scale.cpu()
+    for b in rows:
+        kv_rows = inp.kv[ip[b]:ip[b + 1]].cpu()
+        o, _ = oracle.attend(inp.q[b].cpu(), kv_rows, scale, inp.kv_dtype, 0, ip[b + 1] - ip[b])
+        _check(out[b], o, f"config {cfg} row {b}")
