@@ -45,6 +45,8 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--quick", action="store_true",
+                    help="timed steps only (no clock soak, e2e or CPU baseline); for profiler runs")
     return ap.parse_args()
 
 
@@ -266,12 +268,13 @@ def main():
         call()
     torch.cuda.synchronize()
     sampler = ClockSampler(local if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
-    sampler.start()
-    t_soak = time.perf_counter()
-    while time.perf_counter() - t_soak < 0.6:      # load the GPU so clock samples exist
-        for _ in range(20):
-            call()
-        torch.cuda.synchronize()
+    if not args.quick:
+        sampler.start()
+        t_soak = time.perf_counter()
+        while time.perf_counter() - t_soak < 0.6:      # load the GPU so clock samples exist
+            for _ in range(20):
+                call()
+            torch.cuda.synchronize()
     if ws > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -292,6 +295,12 @@ def main():
     split_ms = split_ms_sum / max(1, ncalls)
     if pkg.device_status(clear=True) != pkg.MLA_OK:
         raise RuntimeError("kernel reported a pipeline timeout during the benchmark")
+    if args.quick:
+        if rank == 0:
+            print(json.dumps({"workload": spec.name, "us_per_call": ms * 1e3, "split_kernel_us": split_ms * 1e3,
+                              "kv_bytes_per_call": inp.kv_bytes(),
+                              "split_gbs": inp.kv_bytes() / (split_ms * 1e-3) / 1e9}), flush=True)
+        return
 
     # ---- end to end: host (pinned) inputs -> device, decode, output -> host, every step
     q_h = inp.q.cpu().pin_memory()

@@ -214,7 +214,7 @@ int mla_decode(const void* q, const void* kv, const void* kv_scale, const int32_
   if (kv_dtype != MLA_KV_BF16 && kv_scale == nullptr) return MLA_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(kv, 16) || !aligned(out, 8) || !aligned(kv_indptr, 4)) return MLA_ERR_INVALID_ARG;
   if (kv_dtype == MLA_KV_FP8_E4M3 && !aligned(kv_scale, 4)) return MLA_ERR_INVALID_ARG;
-  if (kv_dtype == MLA_KV_MXFP4) return MLA_ERR_UNSUPPORTED;  // not built yet
+  if (kv_dtype == MLA_KV_MXFP4 && !aligned(kv_scale, 2)) return MLA_ERR_INVALID_ARG;
 
   int dev, sms, cc;
   int rc = device_info(&dev, &sms, &cc);
@@ -234,8 +234,10 @@ int mla_decode(const void* q, const void* kv, const void* kv_scale, const int32_
   }
 
   mla::DecodeParams p;
-  rc = encode_kv_map(&p.tmap, kv, kv_dtype);
-  if (rc) return rc;
+  if (kv_dtype != MLA_KV_MXFP4) {  // MXFP4 rows are fetched with plain bulk copies
+    rc = encode_kv_map(&p.tmap, kv, kv_dtype);
+    if (rc) return rc;
+  }
   p.q = static_cast<const uint16_t*>(q);
   p.kv = static_cast<const uint8_t*>(kv);
   p.kv_scale = kv_scale;

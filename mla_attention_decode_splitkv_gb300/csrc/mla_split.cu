@@ -72,7 +72,26 @@ struct Cfg<1> {                    // fp8 e4m3 cache
   static constexpr int kThreads = 192;
 };
 
+template <>
+struct Cfg<2> {                    // MXFP4 cache: dequantised to an e4m3 carrier in SMEM
+  static constexpr int kSlotBytes = 16384;
+  static constexpr int kRing = 8;
+  static constexpr int kSPT = 5;
+  static constexpr bool kOverlap = false;    // ring < 2 tiles
+  static constexpr int kN = 32;
+  static constexpr int kQBytes = 5 * 4096;
+  static constexpr int kTmemCols = 256;
+  static constexpr int kSCols = 32;
+  static constexpr int kOCols = 32;
+  static constexpr float kTau = 4.0f;
+  static constexpr int kThreads = 320;       // + 4 dequant warps
+};
+
 constexpr int kPBytes = 4096;      // one P^T buffer: [128 tokens x 32 B] SW32
+constexpr int kRawRows = 64;       // MXFP4 raw staging: half a tile of packed rows
+constexpr int kRawStages = 3;
+constexpr int kRawBytes = kRawRows * kMxPacked;   // 18432
+constexpr int kLutCount = 14;      // e2m1 -> e4m3 tables for block shifts 0..-12, then zero
 
 struct SharedState {
   uint64_t full[16];
@@ -87,13 +106,23 @@ struct SharedState {
   float red[2][4][16];
   float lsum[4][16];
   float qscale[16];
+  uint64_t raw_full[kRawStages];   // MXFP4 only
+  uint64_t raw_empty[kRawStages];
+  uint64_t etok_full[4];
+  int etok[4][128];                // per-row max block exponent of the last 4 tiles
+  uint2 lut[kLutCount];            // 8 e4m3 bytes per block shift
   uint32_t tmem_base;
   int abort;
 };
 
 template <int KV>
-constexpr size_t smem_bytes() {
-  return 1024 + (size_t)Cfg<KV>::kRing * Cfg<KV>::kSlotBytes + Cfg<KV>::kQBytes + 2 * kPBytes + sizeof(SharedState);
+__host__ __device__ constexpr size_t raw_bytes() {
+  return KV == 2 ? (size_t)kRawStages * kRawBytes : 0;
+}
+template <int KV>
+__host__ __device__ constexpr size_t smem_bytes() {
+  return 1024 + (size_t)Cfg<KV>::kRing * Cfg<KV>::kSlotBytes + Cfg<KV>::kQBytes + 2 * kPBytes + raw_bytes<KV>() +
+         sizeof(SharedState);
 }
 
 // ---------------------------------------------------------------- work decomposition
@@ -198,10 +227,11 @@ struct Window {
   int shift;  // window row of the tile's first token
   int cnt;    // valid tokens in the tile
 };
+template <int KV>
 __device__ __forceinline__ Window tile_window(const Seg& s, int t) {
   int row_start = s.row0 + s.n_lo + t * kBN;
   int row_hi = s.row0 + s.n_hi;
-  int y0 = min(row_start, row_hi - kBN);
+  int y0 = KV == 2 ? row_start : min(row_start, row_hi - kBN);
   Window w;
   w.y0 = y0;
   w.shift = row_start - y0;
@@ -287,6 +317,46 @@ __device__ void stage_q_fp8(const DecodeParams& p, int b, uint8_t* qs, float* qs
 }
 
 // ---------------------------------------------------------------- producer (1 thread)
+// MXFP4: packed rows of each tile in two 64-row halves, copied with exact-size bulk copies
+// (rows [row_start, row_start + cnt) only, so nothing outside the sequence is read).
+__device__ void run_producer_mx(const DecodeParams& p, SharedState* sh, uint8_t* raw) {
+  volatile int* abortf = &sh->abort;
+  SegIter it;
+  it.init(p, blockIdx.x);
+  Seg s;
+  uint32_t ridx = 0;
+  bool ok = true;
+  while (ok && it.next(p, s)) {
+    const int n = s.n_hi - s.n_lo;
+    if (n <= 0) continue;
+    const int ntiles = (n + kBN - 1) / kBN;
+    for (int t = 0; t < ntiles && ok; ++t) {
+      const Window w = tile_window<2>(s, t);
+      for (int half = 0; half * kRawRows < w.cnt; ++half) {
+        const uint32_t st = ridx % kRawStages;
+        if (!wait_bar(smem_u32(&sh->raw_empty[st]), ((ridx / kRawStages) & 1) ^ 1, abortf, p.status,
+                      p.wait_limit_ns)) {
+          ok = false;
+          break;
+        }
+        const int rows = min(kRawRows, w.cnt - half * kRawRows);
+        const uint32_t bytes = static_cast<uint32_t>(rows) * kMxPacked;
+        const uint32_t fb = smem_u32(&sh->raw_full[st]);
+        mbar_arrive_expect_tx(fb, bytes);
+        bulk_load(smem_u32(raw + st * kRawBytes), p.kv + static_cast<size_t>(w.y0 + half * kRawRows) * kMxPacked,
+                  bytes, fb);
+        ++ridx;
+      }
+    }
+  }
+  if (!ok) {
+    const uint32_t first = ridx > (uint32_t)kRawStages ? ridx - kRawStages : 0u;
+    for (uint32_t j = first; j < ridx; ++j)
+      wait_bar(smem_u32(&sh->raw_full[j % kRawStages]), (j / kRawStages) & 1, abortf, p.status, p.wait_limit_ns,
+               false);
+  }
+}
+
 template <int KV>
 __device__ void run_producer(const DecodeParams& p, SharedState* sh, uint8_t* ring) {
   using C = Cfg<KV>;
@@ -301,7 +371,7 @@ __device__ void run_producer(const DecodeParams& p, SharedState* sh, uint8_t* ri
     if (n <= 0) continue;
     const int ntiles = (n + kBN - 1) / kBN;
     for (int t = 0; t < ntiles && ok; ++t) {
-      const Window w = tile_window(s, t);
+      const Window w = tile_window<KV>(s, t);
       for (int c = 0; c < C::kSPT; ++c) {
         const uint32_t slot = idx % C::kRing, use = idx / C::kRing;
         if (!wait_bar(smem_u32(&sh->empty[slot]), (use & 1) ^ 1, abortf, p.status, p.wait_limit_ns)) {
@@ -334,12 +404,112 @@ __device__ void run_producer(const DecodeParams& p, SharedState* sh, uint8_t* ri
   }
 }
 
+// ---------------------------------------------------------------- MXFP4 dequantisation (128 threads)
+// Row i of a tile (thread i) becomes 576 e4m3 carrier bytes: block j of 32 elements is
+// e2m1 * 2^(E_j - e_i) with e_i = max_j E_j, looked up per nibble in an 8-entry table for
+// the shift E_j - e_i (exact for shifts >= -8, e4m3-rounded below, zero below -12).
+// The row factor 2^(e_i - 127) is applied by the softmax to the logits and to P.
+// Layout: the same K-major SW128 chunks the TMA writes for fp8 caches.
+__device__ __forceinline__ uint32_t e2m1x4_to_e4m3x4(uint32_t nib16, uint2 lut) {
+  const uint32_t mag = __byte_perm(lut.x, lut.y, nib16 & 0x7777u);
+  const uint32_t sgn = __byte_perm(0x8000u, 0u, (nib16 >> 3) & 0x1111u);
+  return mag | sgn;
+}
+
+__device__ void run_dequant(const DecodeParams& p, SharedState* sh, uint8_t* ring, uint8_t* raw) {
+  using C = Cfg<2>;
+  volatile int* abortf = &sh->abort;
+  const int di = threadIdx.x - 192;        // carrier row of the tile
+  const int half = di >> 6;
+  const uint8_t* scales = static_cast<const uint8_t*>(p.kv_scale);
+  if (di < kLutCount * 8) {
+    const int k = di >> 3, c = di & 7;
+    const float mag = (c < 2) ? 0.5f * c : ldexpf(1.0f + 0.5f * (c & 1), (c >> 1) - 1);
+    const uint32_t code = (k >= 13) ? 0u
+        : static_cast<uint32_t>(__nv_cvt_float_to_fp8(ldexpf(mag, -k), __NV_SATFINITE, __NV_E4M3));
+    reinterpret_cast<uint8_t*>(&sh->lut[0])[k * 8 + c] = static_cast<uint8_t>(code);
+  }
+  bar_sync(2, 128);
+  SegIter it;
+  it.init(p, blockIdx.x);
+  Seg s;
+  uint32_t g = 0, ridx = 0;
+  bool ok = true;
+  while (ok && it.next(p, s)) {
+    const int n = s.n_hi - s.n_lo;
+    if (n <= 0) continue;
+    const int ntiles = (n + kBN - 1) / kBN;
+    for (int t = 0; t < ntiles; ++t) {
+      const Window w = tile_window<2>(s, t);
+      const bool live = di < w.cnt;
+      uint32_t sc[9];
+      if (live) {
+        const uint16_t* sp = reinterpret_cast<const uint16_t*>(scales + static_cast<size_t>(w.y0 + di) * kMxScales);
+#pragma unroll
+        for (int j = 0; j < 9; ++j) sc[j] = __ldg(sp + j);
+      }
+      for (int c = 0; c < C::kSPT && ok; ++c) {
+        const uint32_t idx = g * C::kSPT + c;
+        ok = wait_bar(smem_u32(&sh->empty[idx % C::kRing]), ((idx / C::kRing) & 1) ^ 1, abortf, p.status,
+                      p.wait_limit_ns);
+      }
+      const bool has_half = half * kRawRows < w.cnt;
+      const uint32_t my_r = ridx + half;
+      if (ok && has_half)
+        ok = wait_bar(smem_u32(&sh->raw_full[my_r % kRawStages]), (my_r / kRawStages) & 1, abortf, p.status,
+                      p.wait_limit_ns);
+      if (!ok) break;
+      int emax = 127;
+      if (live) {
+        emax = 0;
+#pragma unroll
+        for (int j = 0; j < 9; ++j) emax = max(emax, max(static_cast<int>(sc[j] & 0xFF), static_cast<int>(sc[j] >> 8)));
+        const uint4* src = reinterpret_cast<const uint4*>(raw + (my_r % kRawStages) * kRawBytes + (di & 63) * kMxPacked);
+#pragma unroll 1
+        for (int c = 0; c < C::kSPT; ++c) {
+          uint8_t* dst = ring + ((g * C::kSPT + c) % C::kRing) * C::kSlotBytes + di * 128;
+          const int nblk = c < 4 ? 4 : 2;
+          for (int bk = 0; bk < nblk; ++bk) {
+            const int j = 4 * c + bk;                       // block (32 elements, 16 packed bytes)
+            const int e = static_cast<int>((sc[j >> 1] >> (8 * (j & 1))) & 0xFF);
+            const uint2 lut = sh->lut[min(emax - e, kLutCount - 1)];
+            const uint4 v = src[j];
+            const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+            uint32_t o[8];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              o[2 * q] = e2m1x4_to_e4m3x4(wv[q] & 0xFFFFu, lut);
+              o[2 * q + 1] = e2m1x4_to_e4m3x4(wv[q] >> 16, lut);
+            }
+            const int pp = 2 * bk;
+            *reinterpret_cast<uint4*>(dst + ((pp ^ (di & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4*>(dst + (((pp + 1) ^ (di & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+          }
+        }
+      } else {
+        for (int c = 0; c < C::kSPT; ++c) {
+          uint4* dst = reinterpret_cast<uint4*>(ring + ((g * C::kSPT + c) % C::kRing) * C::kSlotBytes + di * 128);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) dst[q] = make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+      if (has_half) mbar_arrive(smem_u32(&sh->raw_empty[my_r % kRawStages]));
+      sh->etok[g & 3][di] = emax;
+      fence_proxy_async_smem();
+      for (int c = 0; c < C::kSPT; ++c) mbar_arrive(smem_u32(&sh->full[(g * C::kSPT + c) % C::kRing]));
+      mbar_arrive(smem_u32(&sh->etok_full[g & 3]));
+      ridx += (w.cnt > kRawRows) ? 2u : 1u;
+      ++g;
+    }
+  }
+}
+
 // ---------------------------------------------------------------- MMA issuer (1 thread)
 template <int KV>
 __device__ bool issue_qk(const DecodeParams& p, SharedState* sh, uint8_t* ring, uint32_t qaddr, uint32_t tmem,
                          uint32_t g) {
   using C = Cfg<KV>;
-  constexpr uint32_t idq = instr_desc(KV == 0 ? 1u : 0u, 0, 0, 128, C::kN);
+  constexpr uint32_t idq = instr_desc(KV == 0 ? 1u : 0u, 0, 0, 128, C::kN);  // bf16 | e4m3
   volatile int* abortf = &sh->abort;
   if (g >= 2 && !wait_bar(smem_u32(&sh->s_free[g & 1]), ((g >> 1) & 1) ^ 1, abortf, p.status, p.wait_limit_ns))
     return false;
@@ -463,7 +633,8 @@ __device__ void run_softmax(const DecodeParams& p, SharedState* sh, uint8_t* qs,
   const int quarter = warp & 3;
   const int row = quarter * 32 + lane;                     // token row of the tile = TMEM lane
   const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-  const float kv_scale = (KV == 1) ? __ldg(reinterpret_cast<const float*>(p.kv_scale)) : 1.0f;
+  float kv_scale = 1.0f;
+  if constexpr (KV == 1) kv_scale = __ldg(reinterpret_cast<const float*>(p.kv_scale));
   const float xscale = p.logit_scale_log2 * kv_scale;    // raw dot product -> log2-domain logit
 
   SegIter it;
@@ -471,7 +642,7 @@ __device__ void run_softmax(const DecodeParams& p, SharedState* sh, uint8_t* qs,
   Seg cur, nxt;
   bool has_cur = it.next(p, cur);
   if (has_cur && cur.n_hi > cur.n_lo) {
-    if (KV == 0) stage_q_bf16(p, cur.b, qs, ts); else stage_q_fp8(p, cur.b, qs, sh->qscale, ts);
+    if constexpr (KV == 0) stage_q_bf16(p, cur.b, qs, ts); else stage_q_fp8(p, cur.b, qs, sh->qscale, ts);
     fence_proxy_async_smem();
     mbar_arrive(smem_u32(&sh->q_ready));
   }
@@ -489,7 +660,7 @@ __device__ void run_softmax(const DecodeParams& p, SharedState* sh, uint8_t* qs,
     float mref[16], lpart[16];
     bool has_nxt = false;
     for (int t = 0; t < ntiles; ++t) {
-      const Window w = tile_window(cur, t);
+      const Window w = tile_window<KV>(cur, t);
       bool okw = wait_bar(smem_u32(&sh->s_full[g & 1]), (g >> 1) & 1, abortf, p.status, p.wait_limit_ns);
       okw = __all_sync(0xffffffffu, okw);
       tc_fence_after();
@@ -507,13 +678,23 @@ __device__ void run_softmax(const DecodeParams& p, SharedState* sh, uint8_t* qs,
       tc_fence_before();
       mbar_arrive(smem_u32(&sh->s_free[g & 1]));
       const bool valid = okw && row >= w.shift && row < w.shift + w.cnt;
+      // MXFP4 rows carry a power-of-two factor 2^eadd (eadd = e_row - 127): logits are
+      // scaled by it, P is weighted by it (w = x + eadd) and the softmax sum is not.
+      float eadd = 0.f, xs = xscale;
+      if constexpr (KV == 2) {
+        bool oke = wait_bar(smem_u32(&sh->etok_full[g & 3]), (g >> 2) & 1, abortf, p.status, p.wait_limit_ns);
+        okw = okw && oke;
+        const int e = sh->etok[g & 3][row];
+        eadd = static_cast<float>(e - 127);
+        xs = ldexpf(xscale, e - 127);
+      }
       float x[16];
 #pragma unroll
       for (int h = 0; h < 16; ++h) {
         float sdot;
         if constexpr (KV == 0) sdot = __uint_as_float(r[h]);
         else sdot = (__uint_as_float(r[h]) + __uint_as_float(r[16 + h]) * 0.0625f) * sh->qscale[h];
-        x[h] = valid ? sdot * xscale : kNegInf;
+        x[h] = valid ? sdot * xs + eadd : kNegInf;
       }
       float* red = &sh->red[g & 1][quarter][0];
 #pragma unroll
@@ -585,6 +766,7 @@ __device__ void run_softmax(const DecodeParams& p, SharedState* sh, uint8_t* qs,
           if (j < 4) c0[j] = wv; else c1[j - 4] = wv;
         }
       } else {
+        const float einv = ldexpf(0.0625f, -static_cast<int>(eadd));   // 2^-eadd / 16
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           uint32_t hw = 0, lw = 0;
@@ -596,8 +778,8 @@ __device__ void run_softmax(const DecodeParams& p, SharedState* sh, uint8_t* qs,
             const float2 hd = unpack_e4m3x2(hp);
             const uint32_t lp = pack_e4m3x2((y0 - hd.x) * 16.f, (y1 - hd.y) * 16.f);
             const float2 ld = unpack_e4m3x2(lp);
-            lpart[h] += (hd.x + ld.x * 0.0625f) * 0.0625f;
-            lpart[h + 1] += (hd.y + ld.y * 0.0625f) * 0.0625f;
+            lpart[h] += (hd.x + ld.x * 0.0625f) * einv;
+            lpart[h + 1] += (hd.y + ld.y * 0.0625f) * einv;
             hw |= hp << (8 * k);
             lw |= lp << (8 * k);
           }
@@ -616,7 +798,7 @@ __device__ void run_softmax(const DecodeParams& p, SharedState* sh, uint8_t* qs,
         // the q buffer can take the next segment's queries.
         has_nxt = it.next(p, nxt);
         if (has_nxt && nxt.n_hi > nxt.n_lo) {
-          if (KV == 0) stage_q_bf16(p, nxt.b, qs, ts); else stage_q_fp8(p, nxt.b, qs, sh->qscale, ts);
+          if constexpr (KV == 0) stage_q_bf16(p, nxt.b, qs, ts); else stage_q_fp8(p, nxt.b, qs, sh->qscale, ts);
           fence_proxy_async_smem();
           mbar_arrive(smem_u32(&sh->q_ready));
         }
@@ -644,7 +826,7 @@ __device__ void run_softmax(const DecodeParams& p, SharedState* sh, uint8_t* qs,
 #pragma unroll
     for (int h = 0; h < 16; ++h) {
       const float l = sh->lsum[0][h] + sh->lsum[1][h] + sh->lsum[2][h] + sh->lsum[3][h];
-      inv[h] = (KV == 1 ? kv_scale * 0.0625f : 1.0f) / l;
+      inv[h] = (KV == 0 ? 1.0f : kv_scale * 0.0625f) / l;
       if (!cur.direct && ts == 0) p.part_lse[cur.slot * kHeads + h] = mref[h] + lg2(l);
     }
 #pragma unroll 1
@@ -686,13 +868,21 @@ __global__ void __launch_bounds__(Cfg<KV>::kThreads, 1) mla_split_kernel(const _
   uint8_t* ring = base;
   uint8_t* qs = ring + C::kRing * C::kSlotBytes;
   uint8_t* ps = qs + C::kQBytes;
-  SharedState* sh = reinterpret_cast<SharedState*>(ps + 2 * kPBytes);
+  uint8_t* raw = ps + 2 * kPBytes;
+  SharedState* sh = reinterpret_cast<SharedState*>(raw + raw_bytes<KV>());
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kRing; ++i) {
-      mbar_init(smem_u32(&sh->full[i]), 1);
+      mbar_init(smem_u32(&sh->full[i]), KV == 2 ? 128 : 1);   // MXFP4: every dequant thread arrives
       mbar_init(smem_u32(&sh->empty[i]), 1);
+    }
+    if (KV == 2) {
+      for (int i = 0; i < kRawStages; ++i) {
+        mbar_init(smem_u32(&sh->raw_full[i]), 1);
+        mbar_init(smem_u32(&sh->raw_empty[i]), kRawRows);
+      }
+      for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&sh->etok_full[i]), 128);
     }
     mbar_init(smem_u32(&sh->q_ready), 128);
     for (int i = 0; i < 2; ++i) {
@@ -717,13 +907,17 @@ __global__ void __launch_bounds__(Cfg<KV>::kThreads, 1) mla_split_kernel(const _
   const uint32_t tmem = sh->tmem_base;
 
   if (warp == 0) {
-    if (lane == 0) run_producer<KV>(p, sh, ring);
+    if (lane == 0) {
+      if constexpr (KV == 2) run_producer_mx(p, sh, raw); else run_producer<KV>(p, sh, ring);
+    }
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) run_mma<KV>(p, sh, ring, qs, ps, tmem);
     __syncwarp();
-  } else {
+  } else if (warp < 6) {
     run_softmax<KV>(p, sh, qs, ps, tmem);
+  } else {
+    if constexpr (KV == 2) run_dequant(p, sh, ring, raw);
   }
   tc_fence_before();
   __syncthreads();
@@ -790,12 +984,17 @@ cudaError_t launch_split_t(const DecodeParams& p, int grid, cudaStream_t stream)
 
 }  // namespace
 
-int split_threads(int kv_dtype) { return kv_dtype == 0 ? Cfg<0>::kThreads : Cfg<1>::kThreads; }
-size_t split_smem_bytes(int kv_dtype) { return kv_dtype == 0 ? smem_bytes<0>() : smem_bytes<1>(); }
+int split_threads(int kv_dtype) {
+  return kv_dtype == 0 ? Cfg<0>::kThreads : (kv_dtype == 1 ? Cfg<1>::kThreads : Cfg<2>::kThreads);
+}
+size_t split_smem_bytes(int kv_dtype) {
+  return kv_dtype == 0 ? smem_bytes<0>() : (kv_dtype == 1 ? smem_bytes<1>() : smem_bytes<2>());
+}
 
 cudaError_t launch_split(int kv_dtype, const DecodeParams& p, int grid, cudaStream_t stream) {
   if (kv_dtype == 0) return launch_split_t<0>(p, grid, stream);
   if (kv_dtype == 1) return launch_split_t<1>(p, grid, stream);
+  if (kv_dtype == 2) return launch_split_t<2>(p, grid, stream);
   return cudaErrorNotSupported;
 }
 

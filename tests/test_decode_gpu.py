@@ -49,7 +49,10 @@ SMALL = [
     (synth.KV_BF16, [1024, 77]),
     (synth.KV_FP8, [1, 129, 1000, 2048]),
     (synth.KV_FP8, [128, 256, 5, 383]),
+    (synth.KV_MXFP4, [1, 129, 1000, 2048]),
+    (synth.KV_MXFP4, [64, 65, 127, 383]),
 ]
+DTYPES = [synth.KV_BF16, synth.KV_FP8, synth.KV_MXFP4]
 
 
 @pytest.mark.parametrize("kv_dtype,lens", SMALL)
@@ -61,7 +64,7 @@ def test_small_cases_match_oracle(pkg, kv_dtype, lens, ns):
     _check(out, ref, f"dtype {kv_dtype} lens {lens} ns {ns}")
 
 
-@pytest.mark.parametrize("kv_dtype", [synth.KV_BF16, synth.KV_FP8])
+@pytest.mark.parametrize("kv_dtype", DTYPES)
 @pytest.mark.parametrize("ns", [1, 3, 0])
 def test_empty_and_single_token_sequences(pkg, kv_dtype, ns):
     lens = [0, 1, 0, 300, 1]
@@ -72,7 +75,7 @@ def test_empty_and_single_token_sequences(pkg, kv_dtype, ns):
     assert torch.count_nonzero(out[0]) == 0 and torch.count_nonzero(out[2]) == 0
 
 
-@pytest.mark.parametrize("kv_dtype", [synth.KV_BF16, synth.KV_FP8])
+@pytest.mark.parametrize("kv_dtype", DTYPES)
 def test_split_count_invariance(pkg, kv_dtype):
     inp = synth.make_inputs(2, [3000, 1500], kv_dtype, seed=31)
     ref, _ = oracle.decode(inp.q, inp.kv, inp.kv_scale, inp.kv_indptr, kv_dtype)
@@ -84,7 +87,7 @@ def test_split_count_invariance(pkg, kv_dtype):
         assert torch.allclose(o.float(), base, atol=1e-2, rtol=1e-2), ns
 
 
-@pytest.mark.parametrize("kv_dtype", [synth.KV_BF16, synth.KV_FP8])
+@pytest.mark.parametrize("kv_dtype", DTYPES)
 def test_growing_logits_force_rescales(pkg, kv_dtype):
     # Keys whose projection onto q grows along the sequence: the running maximum rises
     # every tile, so the lazy O rescale path runs repeatedly.
@@ -96,15 +99,17 @@ def test_growing_logits_force_rescales(pkg, kv_dtype):
     src = (base + ramp * q[0, 0].float().unsqueeze(0) / q[0, 0].float().norm() * 24.0 / 24.0 * 6.0).to(torch.bfloat16)
     if kv_dtype == synth.KV_BF16:
         kv, scale = src, None
-    else:
+    elif kv_dtype == synth.KV_FP8:
         kv, scale = synth.quantize_fp8_per_tensor(src)
+    else:
+        kv, scale = synth.quantize_mxfp4(src)
     inp = synth.DecodeInputs(q, src, kv, scale, synth.indptr_from_lengths([L]), kv_dtype, [L])
     ref, lse = oracle.decode(inp.q, inp.kv, inp.kv_scale, inp.kv_indptr, kv_dtype)
     for ns in (1, 0):
         _check(_run(pkg, inp, ns), ref, f"rescale ns {ns}")
 
 
-@pytest.mark.parametrize("cfg", [0, 1, 2, 4])
+@pytest.mark.parametrize("cfg", [0, 1, 2, 3, 4])
 def test_workload_configs_sampled_rows(pkg, cfg):
     """Full-size workloads on the GPU in the bench's launch configuration; the oracle checks
     sampled batch rows (first, last, and a few seeded ones)."""
@@ -121,3 +126,20 @@ def test_workload_configs_sampled_rows(pkg, cfg):
         kv_rows = inp.kv[ip[b]:ip[b + 1]].cpu()
         o, _ = oracle.attend(inp.q[b].cpu(), kv_rows, scale, inp.kv_dtype, 0, ip[b + 1] - ip[b])
         _check(out[b], o, f"config {cfg} row {b}")
+
+
+def test_mxfp4_wide_block_exponent_spread(pkg):
+    """Rows whose 18 blocks span many binades: blocks 2^-4 .. 2^-14 below the row's largest
+    exercise every shift table of the e4m3 carrier, including the rounded and flushed ones."""
+    L = 700
+    g = torch.Generator().manual_seed(77)
+    src = torch.randn((L, 576), generator=g)
+    for j in range(18):
+        src[:, 32 * j:32 * (j + 1)] *= 2.0 ** (-((j * 3 + torch.arange(L) % 5) % 15).float().unsqueeze(1))
+    src = src.to(torch.bfloat16)
+    kv, scale = synth.quantize_mxfp4(src)
+    q = torch.randn((1, 16, 576), generator=g).to(torch.bfloat16)
+    inp = synth.DecodeInputs(q, src, kv, scale, synth.indptr_from_lengths([L]), synth.KV_MXFP4, [L])
+    ref, _ = oracle.decode(inp.q, inp.kv, inp.kv_scale, inp.kv_indptr, synth.KV_MXFP4)
+    for ns in (1, 0):
+        _check(_run(pkg, inp, ns), ref, f"mxfp4 spread ns {ns}")

@@ -1,0 +1,116 @@
+"""Host-side checks of the C-ABI library (no GPU needed): it loads, exports every symbol
+declared in include/*.h, rejects bad arguments before touching the device, and its
+split-count heuristic and workspace sizing follow their documented rules."""
+import ctypes
+import glob
+import math
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from mla_attention_decode_splitkv_gb300 import build
+    path = build.build()
+    from mla_attention_decode_splitkv_gb300 import _lib
+    return _lib.load(path)
+
+
+def _declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(mla_[A-Za-z0-9_]+)\s*\(", text, re.M):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = _declared_functions()
+    assert "mla_decode" in names and len(names) >= 8
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+    from mla_attention_decode_splitkv_gb300 import _lib
+    assert set(_lib.EXPORTED) == set(names)
+
+
+def test_status_strings(lib):
+    for code, name in [(0, b"MLA_OK"), (-1, b"MLA_ERR_INVALID_ARG"), (-2, b"MLA_ERR_UNSUPPORTED"),
+                       (-3, b"MLA_ERR_CUDA"), (-4, b"MLA_ERR_NO_MEMORY"), (-5, b"MLA_ERR_TIMEOUT")]:
+        assert lib.mla_status_string(code) == name
+    assert lib.mla_status_string(12345) == b"MLA_UNKNOWN_STATUS"
+
+
+def _call(lib, q=256, kv=512, scale=1024, ip=2048, out=4096, batch=2, ns=0, dtype=1):
+    vp = ctypes.c_void_p
+    return lib.mla_decode(vp(q) if q else None, vp(kv) if kv else None, vp(scale) if scale else None,
+                          vp(ip) if ip else None, vp(out) if out else None, batch, ns, dtype, None)
+
+
+def test_argument_checks_precede_any_device_work(lib):
+    INV = -1
+    assert _call(lib, q=0) == INV
+    assert _call(lib, kv=0) == INV
+    assert _call(lib, ip=0) == INV
+    assert _call(lib, out=0) == INV
+    assert _call(lib, batch=0) == INV
+    assert _call(lib, batch=-3) == INV
+    assert _call(lib, dtype=3) == INV
+    assert _call(lib, dtype=-1) == INV
+    assert _call(lib, scale=0, dtype=1) == INV          # fp8 needs its scale
+    assert _call(lib, scale=0, dtype=2) == INV          # MXFP4 needs its block scales
+    assert _call(lib, q=258) == INV                     # q not 16-byte aligned
+    assert _call(lib, kv=520) == INV                    # kv not 16-byte aligned
+    assert _call(lib, out=4100) == INV                  # out not 8-byte aligned
+    assert _call(lib, ns=4097) == INV
+
+
+def test_valid_call_without_a_gpu_fails_cleanly(lib):
+    try:
+        import torch
+        if torch.cuda.is_available():
+            pytest.skip("a GPU is present")
+    except ImportError:
+        pass
+    rc = _call(lib, scale=0, dtype=0)
+    assert rc in (-2, -3)  # MLA_ERR_UNSUPPORTED or MLA_ERR_CUDA, never a crash
+
+
+def _model(batch, L, sms, row_bytes, ns):
+    c = (2 * 16 * 512 * 4 + 128 * row_bytes) / row_bytes
+    ctas = batch * ns
+    util = ctas / (math.ceil(ctas / sms) * sms)
+    return util * L / (L + c * (ns - 1))
+
+
+@pytest.mark.parametrize("dtype,row_bytes", [(0, 1152), (1, 576), (2, 306)])
+def test_pick_splits_maximises_the_documented_model(lib, dtype, row_bytes):
+    for batch in (1, 4, 32, 64, 128, 151, 152, 153, 256, 1000):
+        for L in (1, 100, 1024, 4000, 8192, 65536):
+            for sms in (148, 152):
+                ns = lib.mla_decode_pick_splits(batch, L, sms, dtype)
+                hi = max(1, min(64, math.ceil(L / 128)))
+                assert 1 <= ns <= hi
+                best = max(_model(batch, L, sms, row_bytes, k) for k in range(1, hi + 1))
+                assert _model(batch, L, sms, row_bytes, ns) >= best * (1 - 1e-9)
+    assert lib.mla_decode_pick_splits(1000, 8192, 152, dtype) == 1 or dtype == 0
+    assert lib.mla_decode_pick_splits(1, 65536, 152, dtype) > 8
+
+
+def test_pick_splits_rejects_bad_arguments(lib):
+    assert lib.mla_decode_pick_splits(0, 10, 152, 1) == -1
+    assert lib.mla_decode_pick_splits(4, -1, 152, 1) == -1
+    assert lib.mla_decode_pick_splits(4, 10, 0, 1) == -1
+    assert lib.mla_decode_pick_splits(4, 10, 152, 7) == -1
+
+
+def test_workspace_slot_counts(lib):
+    assert lib.mla_decode_workspace_slots(64, 1, 152) == 0
+    assert lib.mla_decode_workspace_slots(64, 7, 152) == 64 * 7
+    assert lib.mla_decode_workspace_slots(64, 0, 152) == 64 + 151
+    assert lib.mla_decode_workspace_slots(0, 0, 152) == -1
