@@ -48,7 +48,6 @@ struct Cfg<0> {                    // bf16 cache
   static constexpr int kSlotBytes = 32768;   // two [128 x 64 bf16] SW128 boxes
   static constexpr int kRing = 6;
   static constexpr int kSPT = 5;             // slots per tile: 4 x 128 value dims + rope
-  static constexpr bool kOverlap = false;    // ring < 2 tiles: QK(t+1) waits for PV(t)
   static constexpr int kN = 16;
   static constexpr int kQBytes = 9 * 2048;   // 9 chunks of [16 rows x 128 B]
   static constexpr int kTmemCols = 128;
@@ -62,7 +61,6 @@ struct Cfg<1> {                    // fp8 e4m3 cache
   static constexpr int kSlotBytes = 16384;   // one [128 x 128 B] SW128 box
   static constexpr int kRing = 12;
   static constexpr int kSPT = 5;
-  static constexpr bool kOverlap = true;     // QK(t+1) runs while softmax(t) works
   static constexpr int kN = 32;              // 16 hi heads + 16 lo heads
   static constexpr int kQBytes = 5 * 4096;   // 5 chunks of [32 rows x 128 B]
   static constexpr int kTmemCols = 256;
@@ -77,7 +75,6 @@ struct Cfg<2> {                    // MXFP4 cache: dequantised to an e4m3 carrie
   static constexpr int kSlotBytes = 16384;
   static constexpr int kRing = 8;
   static constexpr int kSPT = 5;
-  static constexpr bool kOverlap = false;    // ring < 2 tiles
   static constexpr int kN = 32;
   static constexpr int kQBytes = 5 * 4096;
   static constexpr int kTmemCols = 256;
@@ -505,54 +502,40 @@ __device__ void run_dequant(const DecodeParams& p, SharedState* sh, uint8_t* rin
 }
 
 // ---------------------------------------------------------------- MMA issuer (1 thread)
+// Issue the QK^T MMAs of chunk c (one ring slot) of tile g into S buffer g%2.
 template <int KV>
-__device__ bool issue_qk(const DecodeParams& p, SharedState* sh, uint8_t* ring, uint32_t qaddr, uint32_t tmem,
-                         uint32_t g) {
+__device__ __forceinline__ void qk_chunk(SharedState* sh, uint8_t* ring, uint32_t qaddr, uint32_t tmem, uint32_t g,
+                                         int c) {
   using C = Cfg<KV>;
-  constexpr uint32_t idq = instr_desc(KV == 0 ? 1u : 0u, 0, 0, 128, C::kN);  // bf16 | e4m3
-  volatile int* abortf = &sh->abort;
-  if (g >= 2 && !wait_bar(smem_u32(&sh->s_free[g & 1]), ((g >> 1) & 1) ^ 1, abortf, p.status, p.wait_limit_ns))
-    return false;
-  tc_fence_after();
+  constexpr uint32_t idq = instr_desc(KV == 0 ? 1u : 0u, 0, 0, 128, C::kN);  // bf16 | e4m3, K-major A and B
   const uint32_t d = tmem + (g & 1) * C::kSCols;
-  for (int c = 0; c < C::kSPT; ++c) {
-    const uint32_t idx = g * C::kSPT + c, slot = idx % C::kRing;
-    if (!wait_bar(smem_u32(&sh->full[slot]), (idx / C::kRing) & 1, abortf, p.status, p.wait_limit_ns)) return false;
-    tc_fence_after();
-    const uint32_t a = smem_u32(ring + slot * C::kSlotBytes);
-    if constexpr (KV == 0) {
-      const int nsub = c < 4 ? 2 : 1;
-      for (int j = 0; j < nsub; ++j)
+  const uint32_t slot = (g * C::kSPT + c) % C::kRing;
+  const uint32_t a = smem_u32(ring + slot * C::kSlotBytes);
+  if constexpr (KV == 0) {
+    const int nsub = c < 4 ? 2 : 1;
+    for (int j = 0; j < nsub; ++j)
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          mma_f16(d, smem_desc(a + j * 16384 + 32 * k, 16, 1024, kSwizzle128B),
-                  smem_desc(qaddr + (2 * c + j) * 2048 + 32 * k, 16, 1024, kSwizzle128B), idq, (c | j | k) != 0);
-    } else {
-      const int nk = c < 4 ? 4 : 2;
-      for (int k = 0; k < nk; ++k)
-        mma_f8(d, smem_desc(a + 32 * k, 16, 1024, kSwizzle128B),
-               smem_desc(qaddr + c * 4096 + 32 * k, 16, 1024, kSwizzle128B), idq, (c | k) != 0);
-    }
-    if (c == C::kSPT - 1) mma_commit(smem_u32(&sh->empty[slot]));  // rope slot: QK only
+      for (int k = 0; k < 4; ++k)
+        mma_f16(d, smem_desc(a + j * 16384 + 32 * k, 16, 1024, kSwizzle128B),
+                smem_desc(qaddr + (2 * c + j) * 2048 + 32 * k, 16, 1024, kSwizzle128B), idq, (c | j | k) != 0);
+  } else {
+    const int nk = c < 4 ? 4 : 2;
+    for (int k = 0; k < nk; ++k)
+      mma_f8(d, smem_desc(a + 32 * k, 16, 1024, kSwizzle128B),
+             smem_desc(qaddr + c * 4096 + 32 * k, 16, 1024, kSwizzle128B), idq, (c | k) != 0);
   }
-  mma_commit(smem_u32(&sh->s_full[g & 1]));
-  return true;
+  if (c == C::kSPT - 1) mma_commit(smem_u32(&sh->empty[slot]));  // rope slot: QK only
 }
 
+// Issue the PV MMAs of tile g (P^T from buffer g%2) and release its value slots.
 template <int KV>
-__device__ bool issue_pv(const DecodeParams& p, SharedState* sh, uint8_t* ring, uint8_t* ps, uint32_t tmem,
-                         uint32_t g, bool first, int kseg) {
+__device__ __forceinline__ void pv_tile(SharedState* sh, uint8_t* ring, uint8_t* ps, uint32_t tmem, uint32_t g,
+                                        bool first) {
   using C = Cfg<KV>;
-  constexpr uint32_t idp = instr_desc(KV == 0 ? 1u : 0u, 1, 1, 128, C::kN);
-  volatile int* abortf = &sh->abort;
-  if (!wait_bar(smem_u32(&sh->p_full[g & 1]), (g >> 1) & 1, abortf, p.status, p.wait_limit_ns)) return false;
-  if (first && kseg > 0 &&
-      !wait_bar(smem_u32(&sh->o_free), (kseg - 1) & 1, abortf, p.status, p.wait_limit_ns))
-    return false;
-  tc_fence_after();
+  constexpr uint32_t idp = instr_desc(KV == 0 ? 1u : 0u, 1, 1, 128, C::kN);  // MN-major A (V^T) and B (P^T)
   const uint32_t pb = smem_u32(ps + (g & 1) * kPBytes);
   for (int m = 0; m < 4; ++m) {
-    const uint32_t idx = g * C::kSPT + m, slot = idx % C::kRing;
+    const uint32_t slot = (g * C::kSPT + m) % C::kRing;
     const uint32_t a = smem_u32(ring + slot * C::kSlotBytes);
     const uint32_t d = tmem + 2 * C::kSCols + m * C::kOCols;
     if constexpr (KV == 0) {
@@ -569,9 +552,13 @@ __device__ bool issue_pv(const DecodeParams& p, SharedState* sh, uint8_t* ring, 
     mma_commit(smem_u32(&sh->empty[slot]));
   }
   mma_commit(smem_u32(&sh->pv_done[g & 1]));
-  return true;
 }
 
+// The MMA issuer never blocks on one condition while another group of MMAs is ready: it
+// polls (non-blocking) for the next PV (P of the oldest pending tile ready) and for the
+// next QK chunk (its ring slot full), PV first so that value slots return to the producer
+// as early as possible.  QK may run up to three tiles ahead of PV (S is double-buffered,
+// so QK(g) also waits for the softmax to release S(g-2)).
 template <int KV>
 __device__ void run_mma(const DecodeParams& p, SharedState* sh, uint8_t* ring, uint8_t* qs, uint8_t* ps,
                         uint32_t tmem) {
@@ -581,33 +568,79 @@ __device__ void run_mma(const DecodeParams& p, SharedState* sh, uint8_t* ring, u
   SegIter it;
   it.init(p, blockIdx.x);
   Seg s;
-  uint32_t g = 0;
-  int kseg = 0;
-  bool ok = true, pend = false, pend_first = false;
-  uint32_t pend_g = 0;
-  int pend_k = 0;
-  while (ok && it.next(p, s)) {
-    const int n = s.n_hi - s.n_lo;
-    if (n <= 0) continue;
-    if (!wait_bar(smem_u32(&sh->q_ready), kseg & 1, abortf, p.status, p.wait_limit_ns)) { ok = false; break; }
-    const int ntiles = (n + kBN - 1) / kBN;
-    for (int t = 0; t < ntiles; ++t) {
-      if (!issue_qk<KV>(p, sh, ring, qaddr, tmem, g)) { ok = false; break; }
-      if (C::kOverlap) {
-        if (pend && !issue_pv<KV>(p, sh, ring, ps, tmem, pend_g, pend_first, pend_k)) { ok = false; break; }
-        pend = true;
-        pend_g = g;
-        pend_first = (t == 0);
-        pend_k = kseg;
-      } else if (!issue_pv<KV>(p, sh, ring, ps, tmem, g, t == 0, kseg)) {
-        ok = false;
+  int kseg = -1, seg_tiles = 0, t_in_seg = 0;
+  bool more = false;
+  while (it.next(p, s)) {                       // first non-empty segment
+    if (s.n_hi > s.n_lo) { more = true; break; }
+  }
+  if (more) { kseg = 0; seg_tiles = (s.n_hi - s.n_lo + kBN - 1) / kBN; }
+  uint32_t qk_g = 0, pv_g = 0;
+  int qk_c = 0;
+  bool qk_open = false;
+  bool pv_first[4];
+  int pv_seg[4];
+  uint32_t idle = 0;
+  uint64_t t_idle = 0;
+  while (more || pv_g < qk_g) {
+    bool prog = false;
+    if (pv_g < qk_g) {
+      const int slot4 = pv_g & 3;
+      const bool first = pv_first[slot4];
+      const int k = pv_seg[slot4];
+      if (mbar_test(smem_u32(&sh->p_full[pv_g & 1]), (pv_g >> 1) & 1) &&
+          (!(first && k > 0) || mbar_test(smem_u32(&sh->o_free), (k - 1) & 1))) {
+        tc_fence_after();
+        pv_tile<KV>(sh, ring, ps, tmem, pv_g, first);
+        ++pv_g;
+        prog = true;
+      }
+    }
+    if (more) {
+      if (!qk_open && qk_g - pv_g < 4 &&
+          (t_in_seg != 0 || mbar_test(smem_u32(&sh->q_ready), kseg & 1)) &&
+          (qk_g < 2 || mbar_test(smem_u32(&sh->s_free[qk_g & 1]), ((qk_g >> 1) & 1) ^ 1))) {
+        qk_open = true;
+      }
+      if (qk_open) {
+        while (qk_c < C::kSPT) {
+          const uint32_t idx = qk_g * C::kSPT + qk_c;
+          if (!mbar_test(smem_u32(&sh->full[idx % C::kRing]), (idx / C::kRing) & 1)) break;
+          tc_fence_after();
+          qk_chunk<KV>(sh, ring, qaddr, tmem, qk_g, qk_c);
+          ++qk_c;
+          prog = true;
+        }
+        if (qk_c == C::kSPT) {
+          mma_commit(smem_u32(&sh->s_full[qk_g & 1]));
+          pv_first[qk_g & 3] = (t_in_seg == 0);
+          pv_seg[qk_g & 3] = kseg;
+          ++qk_g;
+          qk_c = 0;
+          qk_open = false;
+          if (++t_in_seg == seg_tiles) {
+            t_in_seg = 0;
+            more = false;
+            while (it.next(p, s)) {
+              if (s.n_hi > s.n_lo) { more = true; break; }
+            }
+            if (more) { ++kseg; seg_tiles = (s.n_hi - s.n_lo + kBN - 1) / kBN; }
+          }
+        }
+      }
+    }
+    if (prog) {
+      idle = 0;
+    } else if ((++idle & 63) == 0) {
+      if (*abortf) break;
+      const uint64_t now = globaltimer();
+      if (idle == 64) t_idle = now;
+      else if (now - t_idle > p.wait_limit_ns) {
+        *abortf = 1;
+        atomicOr(p.status, kStatusTimeout);
         break;
       }
-      ++g;
     }
-    ++kseg;
   }
-  if (ok && C::kOverlap && pend) issue_pv<KV>(p, sh, ring, ps, tmem, pend_g, pend_first, pend_k);
   // every MMA issued so far must finish before the tensor memory is released
   mma_commit(smem_u32(&sh->mma_done));
   wait_bar(smem_u32(&sh->mma_done), 0, abortf, p.status, p.wait_limit_ns, false);

@@ -121,9 +121,12 @@ def test_workload_configs_sampled_rows(pkg, cfg):
     B = inp.batch
     rows = sorted({0, B - 1} | set(np.random.default_rng(cfg).choice(B, size=min(B, 3), replace=False).tolist()))
     ip = inp.kv_indptr.cpu().tolist()
-    scale = None if inp.kv_scale is None else inp.kv_scale.cpu()
     for b in rows:
         kv_rows = inp.kv[ip[b]:ip[b + 1]].cpu()
+        if inp.kv_dtype == synth.KV_MXFP4:
+            scale = inp.kv_scale[ip[b]:ip[b + 1]].cpu()       # per-row block scales follow the rows
+        else:
+            scale = None if inp.kv_scale is None else inp.kv_scale.cpu()
         o, _ = oracle.attend(inp.q[b].cpu(), kv_rows, scale, inp.kv_dtype, 0, ip[b + 1] - ip[b])
         _check(out[b], o, f"config {cfg} row {b}")
 
