@@ -128,6 +128,36 @@ void mla_decode_set_wait_limit_ns(unsigned long long ns);
 int mla_decode_profile_begin(void);
 int mla_decode_profile_end(double* split_ms, double* call_ms, int* calls);
 
+/*
+ * mla_decode_noalloc -- the same decode as mla_decode, with the same arguments, for callers
+ * that must not allocate device memory on the decode path (a serving engine or plugin host
+ * whose own pool owns every device allocation, or a latency-critical loop that cannot
+ * afford cudaMalloc / cudaFree, the latter synchronising the whole device).  The pages
+ * have no counterpart: this is a deployment variant of mla_decode.
+ *
+ * Scratch (split partial results and the kernel status word) lives in a fixed array
+ * inside the library's device code instead of a cudaMalloc'd workspace: every GPU that
+ * loads the library holds it (about MLA_NOALLOC_MAX_SLOTS x 32.8 KB, 16.8 MB) until the
+ * process exits.  The call allocates nothing: no cudaMalloc, no cudaFree, no allocating
+ * library routine.
+ *  - Limit: the call needs batch*num_splits partial slots (num_splits >= 2), none
+ *    (num_splits == 1), or batch + SMs - 1 (num_splits <= 0); more than
+ *    MLA_NOALLOC_MAX_SLOTS returns MLA_ERR_NO_MEMORY before any launch.
+ *  - The first call on each device (with that device current) looks up the array's device
+ *    address once (cudaGetSymbolAddress) and caches it; make that first call before any
+ *    stream capture.
+ *  - All calls share the one array, which keeps the previous call's contents; the call
+ *    clears the status word it needs at zero (stream-ordered).  Calls that overlap on the
+ *    GPU (different streams with no ordering between them) race on the array: serialise
+ *    them on one stream or order them with events.
+ *  - A pipeline timeout inside these kernels is recorded only in the array's status word,
+ *    which mla_decode_device_status does not read.
+ * Errors as mla_decode, plus MLA_ERR_NO_MEMORY when the scratch is too small.
+ */
+#define MLA_NOALLOC_MAX_SLOTS 512
+int mla_decode_noalloc(const void* q, const void* kv, const void* kv_scale, const int32_t* kv_indptr,
+                       void* out, int batch, int num_splits, int kv_dtype, void* stream);
+
 /* Static string for a status code; never NULL. */
 const char* mla_status_string(int status);
 

@@ -29,6 +29,7 @@ EXPORTED = (
     "mla_decode_set_wait_limit_ns",
     "mla_decode_profile_begin",
     "mla_decode_profile_end",
+    "mla_decode_noalloc",
     "mla_status_string",
     "mla_last_cuda_error",
 )
@@ -76,6 +77,8 @@ def load(path: str = LIB_PATH):
         lib.mla_decode_profile_end.restype = c_int
         lib.mla_decode_profile_end.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double),
                                                ctypes.POINTER(c_int)]
+        lib.mla_decode_noalloc.restype = c_int
+        lib.mla_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, c_int, c_int, c_int, vp]
         lib.mla_status_string.restype = ctypes.c_char_p
         lib.mla_status_string.argtypes = [c_int]
         lib.mla_last_cuda_error.restype = ctypes.c_char_p
@@ -161,3 +164,11 @@ def profile_end():
     if rc != MLA_OK:
         raise MLAError(rc, "mla_decode_profile_end")
     return a.value, b.value, n.value
+
+
+def mla_decode_noalloc(q, kv, kv_scale, kv_indptr, out, batch: int, num_splits: int, kv_dtype: int,
+                       stream=None) -> int:
+    """Raw C-ABI call of the allocation-free variant (device tensors); returns the status."""
+    lib = load()
+    return lib.mla_decode_noalloc(_ptr(q), _ptr(kv), _ptr(kv_scale), _ptr(kv_indptr), _ptr(out), int(batch),
+                                  int(num_splits), int(kv_dtype), _stream_handle(stream))

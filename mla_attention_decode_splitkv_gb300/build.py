@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libmla_decode.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["mla_split.cu", "mla_api.cu"]
+SOURCES = ["mla_split.cu", "mla_api.cu", "mla_noalloc.cu"]
 
 
 def _nvcc() -> str:

@@ -1,0 +1,144 @@
+// mla_noalloc.cu -- mla_decode_noalloc: the same decode as mla_decode, for callers that
+// must not allocate device memory.
+//
+// Some callers cannot call cudaMalloc on the decode path: a serving engine or plugin host
+// that owns every device allocation through its own pre-sized pool and forbids stray ones,
+// or a latency-critical loop that cannot afford cudaMalloc/cudaFree (cudaFree synchronises
+// the whole device).  mla_decode grows a library-owned workspace with cudaMalloc on first
+// use; this entry point instead keeps its scratch (the split partial results and the
+// kernel status word) in a fixed-size array that lives in the library's device module.
+//
+// The array is a file-scope static __device__ object, so every GPU that loads this library
+// holds kNoallocScratchBytes of it until the process exits.  Host code cannot use the
+// array's name as a device address: on the first call on each device (with that device
+// current) the address is looked up once with cudaGetSymbolAddress and cached.  That first
+// call therefore does one-time set-up work and should happen before any stream capture.
+// All calls share the one array and it keeps the previous call's contents, so calls that
+// overlap on the GPU (different streams, no ordering between them) race on it.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/mla_decode.h"
+#include "mla_internal.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr size_t kSlotBytes = static_cast<size_t>(mla::kHeads) * mla::kDimV * sizeof(float);   // partial O
+constexpr size_t kLseBytes = static_cast<size_t>(mla::kHeads) * sizeof(float);                 // partial lse
+constexpr size_t kStatusBytes = 256;
+constexpr size_t kNoallocScratchBytes =
+    static_cast<size_t>(MLA_NOALLOC_MAX_SLOTS) * (kSlotBytes + kLseBytes) + kStatusBytes;
+
+// Layout: [status word (256 B)] [partial O: slots x 16 x 512 fp32] [partial lse: slots x 16 fp32]
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
+
+std::mutex g_mu;
+void* g_addr[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+// KV rows as a 2D tensor for the TMA loads (bf16: 64-element boxes, fp8: 128-byte boxes;
+// 128 rows; 128-byte swizzle).  The row count is an upper bound: the kernel never
+// addresses a row at or past kv_indptr[batch].
+int encode_map(CUtensorMap* map, const void* kv, int kv_dtype) {
+  if (g_encode == nullptr) {
+    cudaDriverEntryPointQueryResult qr;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &qr) != cudaSuccess ||
+        qr != cudaDriverEntryPointSuccess || fn == nullptr)
+      return MLA_ERR_UNSUPPORTED;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  const bool bf = kv_dtype == MLA_KV_BF16;
+  cuuint64_t gdim[2] = {static_cast<cuuint64_t>(mla::kDim), 1ull << 30};
+  cuuint64_t gstride[1] = {static_cast<cuuint64_t>(mla::kDim) * (bf ? 2 : 1)};
+  cuuint32_t box[2] = {bf ? 64u : 128u, static_cast<cuuint32_t>(mla::kBN)};
+  cuuint32_t estride[2] = {1, 1};
+  CUresult r = g_encode(map, bf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+                        const_cast<void*>(kv), gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" int mla_decode_noalloc(const void* q, const void* kv, const void* kv_scale, const int32_t* kv_indptr,
+                                  void* out, int batch, int num_splits, int kv_dtype, void* stream) {
+  if (q == nullptr || kv == nullptr || kv_indptr == nullptr || out == nullptr) return MLA_ERR_INVALID_ARG;
+  if (batch <= 0 || num_splits > mla::kMaxSplits) return MLA_ERR_INVALID_ARG;
+  if (kv_dtype != MLA_KV_BF16 && kv_dtype != MLA_KV_FP8_E4M3 && kv_dtype != MLA_KV_MXFP4) return MLA_ERR_INVALID_ARG;
+  if (kv_dtype != MLA_KV_BF16 && kv_scale == nullptr) return MLA_ERR_INVALID_ARG;
+  auto aligned = [](const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; };
+  if (!aligned(q, 16) || !aligned(kv, 16) || !aligned(out, 8) || !aligned(kv_indptr, 4)) return MLA_ERR_INVALID_ARG;
+  if (kv_dtype == MLA_KV_FP8_E4M3 && !aligned(kv_scale, 4)) return MLA_ERR_INVALID_ARG;
+  if (kv_dtype == MLA_KV_MXFP4 && !aligned(kv_scale, 2)) return MLA_ERR_INVALID_ARG;
+
+  int dev = 0, sms = 0, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MLA_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  if (major * 10 + minor != 103) return MLA_ERR_UNSUPPORTED;
+
+  const int ns = num_splits >= 1 ? num_splits : 0;
+  const long long grid = ns >= 1 ? static_cast<long long>(batch) * ns : sms;
+  const long long slots = ns == 1 ? 0 : (ns >= 2 ? static_cast<long long>(batch) * ns : static_cast<long long>(batch) + sms - 1);
+  if (slots > MLA_NOALLOC_MAX_SLOTS || grid > 0x7fffffffLL) return MLA_ERR_NO_MEMORY;  // beyond the fixed scratch
+
+  void* base = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_addr[dev] == nullptr) {
+      void* ptr = nullptr;
+      if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) {
+        cudaGetLastError();
+        return MLA_ERR_CUDA;
+      }
+      g_addr[dev] = ptr;
+    }
+    base = g_addr[dev];
+  }
+  unsigned char* b = static_cast<unsigned char*>(base);
+  int* status = reinterpret_cast<int*>(b);
+  float* part_o = reinterpret_cast<float*>(b + kStatusBytes);
+  float* part_lse = reinterpret_cast<float*>(b + kStatusBytes + static_cast<size_t>(MLA_NOALLOC_MAX_SLOTS) * kSlotBytes);
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // The status word must start each call at zero (the kernels only ever set bits in it).
+  if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess) { cudaGetLastError(); return MLA_ERR_CUDA; }
+
+  mla::DecodeParams p;
+  if (kv_dtype != MLA_KV_MXFP4) {
+    const int rc = encode_map(&p.tmap, kv, kv_dtype);
+    if (rc) return rc;
+  }
+  p.q = static_cast<const uint16_t*>(q);
+  p.kv = static_cast<const uint8_t*>(kv);
+  p.kv_scale = kv_scale;
+  p.kv_indptr = kv_indptr;
+  p.out = static_cast<uint16_t*>(out);
+  p.part_o = part_o;
+  p.part_lse = part_lse;
+  p.status = status;
+  p.batch = batch;
+  p.num_splits = ns;
+  p.num_ctas = static_cast<int>(grid);
+  p.logit_scale_log2 = static_cast<float>((1.0 / std::sqrt(static_cast<double>(mla::kDim))) * 1.4426950408889634);
+  p.wait_limit_ns = 2000000000ull;
+  if (mla::launch_split(kv_dtype, p, static_cast<int>(grid), st) != cudaSuccess) { cudaGetLastError(); return MLA_ERR_CUDA; }
+  if (ns != 1) {
+    mla::CombineParams c;
+    c.kv_indptr = kv_indptr;
+    c.part_o = part_o;
+    c.part_lse = part_lse;
+    c.out = static_cast<uint16_t*>(out);
+    c.batch = batch;
+    c.num_splits = ns;
+    c.num_ctas = static_cast<int>(grid);
+    if (mla::launch_combine(c, st) != cudaSuccess) { cudaGetLastError(); return MLA_ERR_CUDA; }
+  }
+  return MLA_OK;
+}
