@@ -9,7 +9,7 @@
 #include <mutex>
 #include <vector>
 
-#include "../../include/mla_decode.h"
+#include "mla_decode.h"
 #include "mla_internal.h"
 
 namespace {

@@ -21,7 +21,7 @@
 #include <cstdint>
 #include <mutex>
 
-#include "../../include/mla_decode.h"
+#include "mla_decode.h"
 #include "mla_internal.h"
 
 namespace {

@@ -54,7 +54,7 @@ struct Cfg<0> {                    // bf16 cache
   static constexpr int kSCols = 16;
   static constexpr int kOCols = 16;
   static constexpr float kTau = 8.0f;
-  static constexpr int kThreads = 192;
+  static constexpr int kThreads = 224;
 };
 template <>
 struct Cfg<1> {                    // fp8 e4m3 cache
@@ -67,7 +67,7 @@ struct Cfg<1> {                    // fp8 e4m3 cache
   static constexpr int kSCols = 32;
   static constexpr int kOCols = 32;
   static constexpr float kTau = 4.0f;        // P <= 16 -> 16 P <= 256 fits e4m3
-  static constexpr int kThreads = 192;
+  static constexpr int kThreads = 224;
 };
 
 template <>
@@ -81,7 +81,7 @@ struct Cfg<2> {                    // MXFP4 cache: dequantised to an e4m3 carrie
   static constexpr int kSCols = 32;
   static constexpr int kOCols = 32;
   static constexpr float kTau = 4.0f;
-  static constexpr int kThreads = 320;       // + 4 dequant warps
+  static constexpr int kThreads = 352;       // + 4 dequant warps
 };
 
 constexpr int kPBytes = 4096;      // one P^T buffer: [128 tokens x 32 B] SW32
@@ -100,6 +100,7 @@ struct SharedState {
   uint64_t pv_done[2];
   uint64_t o_free;
   uint64_t mma_done;
+  uint64_t mma_done2;
   float red[2][4][16];
   float lsum[4][16];
   float qscale[16];
@@ -416,7 +417,7 @@ __device__ __forceinline__ uint32_t e2m1x4_to_e4m3x4(uint32_t nib16, uint2 lut) 
 __device__ void run_dequant(const DecodeParams& p, SharedState* sh, uint8_t* ring, uint8_t* raw) {
   using C = Cfg<2>;
   volatile int* abortf = &sh->abort;
-  const int di = threadIdx.x - 192;        // carrier row of the tile
+  const int di = threadIdx.x - 224;        // carrier row of the tile
   const int half = di >> 6;
   const uint8_t* scales = static_cast<const uint8_t*>(p.kv_scale);
   if (di < kLutCount * 8) {
@@ -502,148 +503,123 @@ __device__ void run_dequant(const DecodeParams& p, SharedState* sh, uint8_t* rin
 }
 
 // ---------------------------------------------------------------- MMA issuer (1 thread)
-// Issue the QK^T MMAs of chunk c (one ring slot) of tile g into S buffer g%2.
+// MMA issue.  Two single-thread issuers on separate warps keep the tensor core fed: one
+// issues every QK^T group, the other every PV group (independent accumulators), each
+// blocking only on its own barriers.  Shared-memory descriptors are built once; per MMA
+// only the 14-bit start-address field advances (one 64-bit add), so an MMA costs a few
+// instructions of issue.
+struct Descs {
+  uint64_t ring_k;   // K-major SW128 descriptor of ring slot 0 (sbo = 1024)
+  uint64_t ring_mn;  // MN-major SW128 descriptor of ring slot 0 (lbo = 16 KB, sbo = 1024)
+  uint64_t q;        // K-major SW128 descriptor of the q chunks
+  uint64_t p;        // MN-major SW32 descriptor of P buffer 0 (sbo = 256)
+};
+__device__ __forceinline__ Descs make_descs(uint8_t* ring, uint8_t* qs, uint8_t* ps) {
+  Descs d;
+  d.ring_k = smem_desc(smem_u32(ring), 16, 1024, kSwizzle128B);
+  d.ring_mn = smem_desc(smem_u32(ring), 16384, 1024, kSwizzle128B);
+  d.q = smem_desc(smem_u32(qs), 16, 1024, kSwizzle128B);
+  d.p = smem_desc(smem_u32(ps), 0, 256, kSwizzle32B);
+  return d;
+}
+// Byte offset -> descriptor start-address increment.
+__device__ __forceinline__ uint64_t dofs(uint32_t bytes) { return static_cast<uint64_t>(bytes >> 4); }
+
 template <int KV>
-__device__ __forceinline__ void qk_chunk(SharedState* sh, uint8_t* ring, uint32_t qaddr, uint32_t tmem, uint32_t g,
-                                         int c) {
+__device__ void run_mma_qk(const DecodeParams& p, SharedState* sh, const Descs& ds, uint32_t tmem) {
   using C = Cfg<KV>;
   constexpr uint32_t idq = instr_desc(KV == 0 ? 1u : 0u, 0, 0, 128, C::kN);  // bf16 | e4m3, K-major A and B
-  const uint32_t d = tmem + (g & 1) * C::kSCols;
-  const uint32_t slot = (g * C::kSPT + c) % C::kRing;
-  const uint32_t a = smem_u32(ring + slot * C::kSlotBytes);
-  if constexpr (KV == 0) {
-    const int nsub = c < 4 ? 2 : 1;
-    for (int j = 0; j < nsub; ++j)
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        mma_f16(d, smem_desc(a + j * 16384 + 32 * k, 16, 1024, kSwizzle128B),
-                smem_desc(qaddr + (2 * c + j) * 2048 + 32 * k, 16, 1024, kSwizzle128B), idq, (c | j | k) != 0);
-  } else {
-    const int nk = c < 4 ? 4 : 2;
-    for (int k = 0; k < nk; ++k)
-      mma_f8(d, smem_desc(a + 32 * k, 16, 1024, kSwizzle128B),
-             smem_desc(qaddr + c * 4096 + 32 * k, 16, 1024, kSwizzle128B), idq, (c | k) != 0);
-  }
-  if (c == C::kSPT - 1) mma_commit(smem_u32(&sh->empty[slot]));  // rope slot: QK only
-}
-
-// Issue the PV MMAs of tile g (P^T from buffer g%2) and release its value slots.
-template <int KV>
-__device__ __forceinline__ void pv_tile(SharedState* sh, uint8_t* ring, uint8_t* ps, uint32_t tmem, uint32_t g,
-                                        bool first) {
-  using C = Cfg<KV>;
-  constexpr uint32_t idp = instr_desc(KV == 0 ? 1u : 0u, 1, 1, 128, C::kN);  // MN-major A (V^T) and B (P^T)
-  const uint32_t pb = smem_u32(ps + (g & 1) * kPBytes);
-  for (int m = 0; m < 4; ++m) {
-    const uint32_t slot = (g * C::kSPT + m) % C::kRing;
-    const uint32_t a = smem_u32(ring + slot * C::kSlotBytes);
-    const uint32_t d = tmem + 2 * C::kSCols + m * C::kOCols;
-    if constexpr (KV == 0) {
-#pragma unroll
-      for (int k = 0; k < 8; ++k)
-        mma_f16(d, smem_desc(a + 2048 * k, 16384, 1024, kSwizzle128B), smem_desc(pb + 512 * k, 0, 256, kSwizzle32B),
-                idp, !(first && k == 0));
-    } else {
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        mma_f8(d, smem_desc(a + 4096 * k, 16384, 1024, kSwizzle128B), smem_desc(pb + 1024 * k, 0, 256, kSwizzle32B),
-               idp, !(first && k == 0));
-    }
-    mma_commit(smem_u32(&sh->empty[slot]));
-  }
-  mma_commit(smem_u32(&sh->pv_done[g & 1]));
-}
-
-// The MMA issuer never blocks on one condition while another group of MMAs is ready: it
-// polls (non-blocking) for the next PV (P of the oldest pending tile ready) and for the
-// next QK chunk (its ring slot full), PV first so that value slots return to the producer
-// as early as possible.  QK may run up to three tiles ahead of PV (S is double-buffered,
-// so QK(g) also waits for the softmax to release S(g-2)).
-template <int KV>
-__device__ void run_mma(const DecodeParams& p, SharedState* sh, uint8_t* ring, uint8_t* qs, uint8_t* ps,
-                        uint32_t tmem) {
-  using C = Cfg<KV>;
   volatile int* abortf = &sh->abort;
-  const uint32_t qaddr = smem_u32(qs);
   SegIter it;
   it.init(p, blockIdx.x);
   Seg s;
-  int kseg = -1, seg_tiles = 0, t_in_seg = 0;
-  bool more = false;
-  while (it.next(p, s)) {                       // first non-empty segment
-    if (s.n_hi > s.n_lo) { more = true; break; }
-  }
-  if (more) { kseg = 0; seg_tiles = (s.n_hi - s.n_lo + kBN - 1) / kBN; }
-  uint32_t qk_g = 0, pv_g = 0;
-  int qk_c = 0;
-  bool qk_open = false;
-  bool pv_first[4];
-  int pv_seg[4];
-  uint32_t idle = 0;
-  uint64_t t_idle = 0;
-  while (more || pv_g < qk_g) {
-    bool prog = false;
-    if (pv_g < qk_g) {
-      const int slot4 = pv_g & 3;
-      const bool first = pv_first[slot4];
-      const int k = pv_seg[slot4];
-      if (mbar_test(smem_u32(&sh->p_full[pv_g & 1]), (pv_g >> 1) & 1) &&
-          (!(first && k > 0) || mbar_test(smem_u32(&sh->o_free), (k - 1) & 1))) {
-        tc_fence_after();
-        pv_tile<KV>(sh, ring, ps, tmem, pv_g, first);
-        ++pv_g;
-        prog = true;
-      }
-    }
-    if (more) {
-      if (!qk_open && qk_g - pv_g < 4 &&
-          (t_in_seg != 0 || mbar_test(smem_u32(&sh->q_ready), kseg & 1)) &&
-          (qk_g < 2 || mbar_test(smem_u32(&sh->s_free[qk_g & 1]), ((qk_g >> 1) & 1) ^ 1))) {
-        qk_open = true;
-      }
-      if (qk_open) {
-        while (qk_c < C::kSPT) {
-          const uint32_t idx = qk_g * C::kSPT + qk_c;
-          if (!mbar_test(smem_u32(&sh->full[idx % C::kRing]), (idx / C::kRing) & 1)) break;
-          tc_fence_after();
-          qk_chunk<KV>(sh, ring, qaddr, tmem, qk_g, qk_c);
-          ++qk_c;
-          prog = true;
-        }
-        if (qk_c == C::kSPT) {
-          mma_commit(smem_u32(&sh->s_full[qk_g & 1]));
-          pv_first[qk_g & 3] = (t_in_seg == 0);
-          pv_seg[qk_g & 3] = kseg;
-          ++qk_g;
-          qk_c = 0;
-          qk_open = false;
-          if (++t_in_seg == seg_tiles) {
-            t_in_seg = 0;
-            more = false;
-            while (it.next(p, s)) {
-              if (s.n_hi > s.n_lo) { more = true; break; }
-            }
-            if (more) { ++kseg; seg_tiles = (s.n_hi - s.n_lo + kBN - 1) / kBN; }
-          }
-        }
-      }
-    }
-    if (prog) {
-      idle = 0;
-    } else if ((++idle & 63) == 0) {
-      if (*abortf) break;
-      const uint64_t now = globaltimer();
-      if (idle == 64) t_idle = now;
-      else if (now - t_idle > p.wait_limit_ns) {
-        *abortf = 1;
-        atomicOr(p.status, kStatusTimeout);
+  uint32_t g = 0;
+  int kseg = 0;
+  bool ok = true;
+  while (ok && it.next(p, s)) {
+    const int n = s.n_hi - s.n_lo;
+    if (n <= 0) continue;
+    ok = wait_bar(smem_u32(&sh->q_ready), kseg & 1, abortf, p.status, p.wait_limit_ns);
+    const int ntiles = (n + kBN - 1) / kBN;
+    for (int t = 0; ok && t < ntiles; ++t, ++g) {
+      if (g >= 2 && !(ok = wait_bar(smem_u32(&sh->s_free[g & 1]), ((g >> 1) & 1) ^ 1, abortf, p.status,
+                                    p.wait_limit_ns)))
         break;
+      const uint32_t d = tmem + (g & 1) * C::kSCols;
+#pragma unroll
+      for (int c = 0; c < C::kSPT; ++c) {
+        const uint32_t idx = g * C::kSPT + c, slot = idx % C::kRing;
+        if (!(ok = wait_bar(smem_u32(&sh->full[slot]), (idx / C::kRing) & 1, abortf, p.status, p.wait_limit_ns)))
+          break;
+        tc_fence_after();
+        const uint64_t a = ds.ring_k + dofs(slot * C::kSlotBytes);
+        if constexpr (KV == 0) {
+          const uint64_t b = ds.q + dofs(2 * c * 2048);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) mma_f16(d, a + dofs(32 * k), b + dofs(32 * k), idq, (c | k) != 0);
+          if (c < 4) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              mma_f16(d, a + dofs(16384 + 32 * k), b + dofs(2048 + 32 * k), idq, 1u);
+          }
+        } else {
+          const uint64_t b = ds.q + dofs(c * 4096);
+#pragma unroll
+          for (int k = 0; k < (c < 4 ? 4 : 2); ++k) mma_f8(d, a + dofs(32 * k), b + dofs(32 * k), idq, (c | k) != 0);
+        }
+        if (c == C::kSPT - 1) mma_commit(smem_u32(&sh->empty[slot]));  // rope slot: QK only
       }
+      if (ok) mma_commit(smem_u32(&sh->s_full[g & 1]));
     }
+    ++kseg;
   }
-  // every MMA issued so far must finish before the tensor memory is released
   mma_commit(smem_u32(&sh->mma_done));
   wait_bar(smem_u32(&sh->mma_done), 0, abortf, p.status, p.wait_limit_ns, false);
+}
+
+template <int KV>
+__device__ void run_mma_pv(const DecodeParams& p, SharedState* sh, const Descs& ds, uint32_t tmem) {
+  using C = Cfg<KV>;
+  constexpr uint32_t idp = instr_desc(KV == 0 ? 1u : 0u, 1, 1, 128, C::kN);  // MN-major A (V^T) and B (P^T)
+  volatile int* abortf = &sh->abort;
+  SegIter it;
+  it.init(p, blockIdx.x);
+  Seg s;
+  uint32_t g = 0;
+  int kseg = 0;
+  bool ok = true;
+  while (ok && it.next(p, s)) {
+    const int n = s.n_hi - s.n_lo;
+    if (n <= 0) continue;
+    const int ntiles = (n + kBN - 1) / kBN;
+    for (int t = 0; ok && t < ntiles; ++t, ++g) {
+      if (!(ok = wait_bar(smem_u32(&sh->p_full[g & 1]), (g >> 1) & 1, abortf, p.status, p.wait_limit_ns))) break;
+      if (t == 0 && kseg > 0 &&
+          !(ok = wait_bar(smem_u32(&sh->o_free), (kseg - 1) & 1, abortf, p.status, p.wait_limit_ns)))
+        break;
+      tc_fence_after();
+      const bool first = (t == 0);
+      const uint64_t b = ds.p + dofs((g & 1) * kPBytes);
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const uint32_t slot = (g * C::kSPT + m) % C::kRing;
+        const uint64_t a = ds.ring_mn + dofs(slot * C::kSlotBytes);
+        const uint32_t d = tmem + 2 * C::kSCols + m * C::kOCols;
+        if constexpr (KV == 0) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) mma_f16(d, a + dofs(2048 * k), b + dofs(512 * k), idp, !(first && k == 0));
+        } else {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) mma_f8(d, a + dofs(4096 * k), b + dofs(1024 * k), idp, !(first && k == 0));
+        }
+        mma_commit(smem_u32(&sh->empty[slot]));
+      }
+      mma_commit(smem_u32(&sh->pv_done[g & 1]));
+    }
+    ++kseg;
+  }
+  mma_commit(smem_u32(&sh->mma_done2));
+  wait_bar(smem_u32(&sh->mma_done2), 0, abortf, p.status, p.wait_limit_ns, false);
 }
 
 // ---------------------------------------------------------------- softmax / epilogue (128 threads)
@@ -661,7 +637,7 @@ template <int KV>
 __device__ void run_softmax(const DecodeParams& p, SharedState* sh, uint8_t* qs, uint8_t* ps, uint32_t tmem) {
   using C = Cfg<KV>;
   volatile int* abortf = &sh->abort;
-  const int ts = threadIdx.x - 64;
+  const int ts = threadIdx.x - 96;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quarter = warp & 3;
   const int row = quarter * 32 + lane;                     // token row of the tile = TMEM lane
@@ -926,6 +902,7 @@ __global__ void __launch_bounds__(Cfg<KV>::kThreads, 1) mla_split_kernel(const _
     }
     mbar_init(smem_u32(&sh->o_free), 128);
     mbar_init(smem_u32(&sh->mma_done), 1);
+    mbar_init(smem_u32(&sh->mma_done2), 1);
     sh->abort = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
@@ -945,9 +922,12 @@ __global__ void __launch_bounds__(Cfg<KV>::kThreads, 1) mla_split_kernel(const _
     }
     __syncwarp();
   } else if (warp == 1) {
-    if (lane == 0) run_mma<KV>(p, sh, ring, qs, ps, tmem);
+    if (lane == 0) run_mma_qk<KV>(p, sh, make_descs(ring, qs, ps), tmem);
     __syncwarp();
-  } else if (warp < 6) {
+  } else if (warp == 2) {
+    if (lane == 0) run_mma_pv<KV>(p, sh, make_descs(ring, qs, ps), tmem);
+    __syncwarp();
+  } else if (warp < 7) {
     run_softmax<KV>(p, sh, qs, ps, tmem);
   } else {
     if constexpr (KV == 2) run_dequant(p, sh, ring, raw);
