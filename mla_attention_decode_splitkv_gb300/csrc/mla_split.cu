@@ -54,7 +54,8 @@ struct Cfg<0> {                    // bf16 cache
   static constexpr int kSCols = 16;
   static constexpr int kOCols = 16;
   static constexpr float kTau = 8.0f;
-  static constexpr int kThreads = 224;
+  static constexpr int kSoftWarps = 8;
+  static constexpr int kThreads = 352;       // producer, QK issuer, PV issuer, 8 softmax warps
 };
 template <>
 struct Cfg<1> {                    // fp8 e4m3 cache
@@ -67,7 +68,8 @@ struct Cfg<1> {                    // fp8 e4m3 cache
   static constexpr int kSCols = 32;
   static constexpr int kOCols = 32;
   static constexpr float kTau = 4.0f;        // P <= 16 -> 16 P <= 256 fits e4m3
-  static constexpr int kThreads = 224;
+  static constexpr int kSoftWarps = 8;
+  static constexpr int kThreads = 352;       // producer, QK issuer, PV issuer, 8 softmax warps
 };
 
 template <>
@@ -81,7 +83,8 @@ struct Cfg<2> {                    // MXFP4 cache: dequantised to an e4m3 carrie
   static constexpr int kSCols = 32;
   static constexpr int kOCols = 32;
   static constexpr float kTau = 4.0f;
-  static constexpr int kThreads = 352;       // + 4 dequant warps
+  static constexpr int kSoftWarps = 4;
+  static constexpr int kThreads = 352;       // producer, QK, PV, 4 softmax warps, 4 dequant warps
 };
 
 constexpr int kPBytes = 4096;      // one P^T buffer: [128 tokens x 32 B] SW32
@@ -627,19 +630,29 @@ template <int KV>
 __device__ void write_empty_result(const DecodeParams& p, const Seg& s, int ts) {
   if (s.direct) {
     uint32_t* o = reinterpret_cast<uint32_t*>(p.out + static_cast<size_t>(s.b) * kHeads * kDimV);
-    for (int i = ts; i < kHeads * kDimV / 2; i += 128) o[i] = 0u;
+    for (int i = ts; i < kHeads * kDimV / 2; i += Cfg<KV>::kSoftWarps * 32) o[i] = 0u;
   } else if (ts < kHeads) {
     p.part_lse[s.slot * kHeads + ts] = kNegInf;
   }
 }
 
+// Softmax / epilogue warps.  Thread = one token of the tile (= one TMEM lane) for H heads:
+// kSoftWarps = 8 puts two warps on each TMEM lane quarter, each owning 8 heads (halving the
+// per-tile latency of this stage); kSoftWarps = 4 gives each thread all 16 heads.  The two
+// head groups never share a named barrier on a path the other may skip: every named
+// barrier below is reached by all softmax threads once per tile (or once per segment).
 template <int KV>
 __device__ void run_softmax(const DecodeParams& p, SharedState* sh, uint8_t* qs, uint8_t* ps, uint32_t tmem) {
   using C = Cfg<KV>;
+  constexpr int NW = C::kSoftWarps;
+  constexpr int NT = NW * 32;
+  constexpr int H = 64 / NW;                               // heads per thread: 16 or 8
   volatile int* abortf = &sh->abort;
   const int ts = threadIdx.x - 96;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quarter = warp & 3;
+  const int hg = (ts >> 5) >> 2;                           // head group (0 when H = 16)
+  const int h0 = hg * H;
   const int row = quarter * 32 + lane;                     // token row of the tile = TMEM lane
   const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
   float kv_scale = 1.0f;
@@ -650,12 +663,12 @@ __device__ void run_softmax(const DecodeParams& p, SharedState* sh, uint8_t* qs,
   it.init(p, blockIdx.x);
   Seg cur, nxt;
   bool has_cur = it.next(p, cur);
-  if (has_cur && cur.n_hi > cur.n_lo) {
+  if (has_cur && cur.n_hi > cur.n_lo && ts < 128) {
     if constexpr (KV == 0) stage_q_bf16(p, cur.b, qs, ts); else stage_q_fp8(p, cur.b, qs, sh->qscale, ts);
     fence_proxy_async_smem();
     mbar_arrive(smem_u32(&sh->q_ready));
   }
-  bar_sync(1, 128);  // qscale visible to all softmax threads
+  bar_sync(1, NT);  // qscale visible to all softmax threads
   uint32_t g = 0;
   bool ok = true;
   while (ok && has_cur) {
@@ -665,23 +678,22 @@ __device__ void run_softmax(const DecodeParams& p, SharedState* sh, uint8_t* qs,
       has_cur = it.next(p, cur);
       continue;
     }
+    float qx[H];                                           // per-head logit multiplier
+#pragma unroll
+    for (int h = 0; h < H; ++h) qx[h] = (KV == 0) ? xscale : sh->qscale[h0 + h] * xscale;
     const int ntiles = (n + kBN - 1) / kBN;
-    float mref[16], lpart[16];
+    float mref[H], lpart[H];
     bool has_nxt = false;
     for (int t = 0; t < ntiles; ++t) {
       const Window w = tile_window<KV>(cur, t);
       bool okw = wait_bar(smem_u32(&sh->s_full[g & 1]), (g >> 1) & 1, abortf, p.status, p.wait_limit_ns);
       okw = __all_sync(0xffffffffu, okw);
       tc_fence_after();
-      uint32_t r[C::kSCols];
+      uint32_t rh[H], rl[H];
       if (okw) {
-        const uint32_t ta = tmem + lane_base + (g & 1) * C::kSCols;
-        uint32_t (&r0)[16] = *reinterpret_cast<uint32_t(*)[16]>(&r[0]);
-        tmem_ld16(ta, r0);
-        if constexpr (C::kSCols == 32) {
-          uint32_t (&r1)[16] = *reinterpret_cast<uint32_t(*)[16]>(&r[C::kSCols - 16]);
-          tmem_ld16(ta + 16, r1);
-        }
+        const uint32_t ta = tmem + lane_base + (g & 1) * C::kSCols + h0;
+        tmem_ld<H>(ta, rh);
+        if constexpr (KV != 0) tmem_ld<H>(ta + 16, rl);
         tmem_wait_ld();
       }
       tc_fence_before();
@@ -689,46 +701,54 @@ __device__ void run_softmax(const DecodeParams& p, SharedState* sh, uint8_t* qs,
       const bool valid = okw && row >= w.shift && row < w.shift + w.cnt;
       // MXFP4 rows carry a power-of-two factor 2^eadd (eadd = e_row - 127): logits are
       // scaled by it, P is weighted by it (w = x + eadd) and the softmax sum is not.
-      float eadd = 0.f, xs = xscale;
+      float eadd = 0.f, rowf = 1.f;
       if constexpr (KV == 2) {
         bool oke = wait_bar(smem_u32(&sh->etok_full[g & 3]), (g >> 2) & 1, abortf, p.status, p.wait_limit_ns);
         okw = okw && oke;
         const int e = sh->etok[g & 3][row];
         eadd = static_cast<float>(e - 127);
-        xs = ldexpf(xscale, e - 127);
+        rowf = ldexpf(1.0f, e - 127);
       }
-      float x[16];
+      float x[H];
 #pragma unroll
-      for (int h = 0; h < 16; ++h) {
+      for (int h = 0; h < H; ++h) {
         float sdot;
-        if constexpr (KV == 0) sdot = __uint_as_float(r[h]);
-        else sdot = (__uint_as_float(r[h]) + __uint_as_float(r[16 + h]) * 0.0625f) * sh->qscale[h];
-        x[h] = valid ? sdot * xs + eadd : kNegInf;
+        if constexpr (KV == 0) sdot = __uint_as_float(rh[h]);
+        else sdot = fmaf(__uint_as_float(rl[h]), 0.0625f, __uint_as_float(rh[h])) * rowf;
+        x[h] = valid ? fmaf(sdot, qx[h], eadd) : kNegInf;
       }
-      float* red = &sh->red[g & 1][quarter][0];
+      float* red = &sh->red[g & 1][quarter][h0];
 #pragma unroll
-      for (int h = 0; h < 16; ++h) {
+      for (int h = 0; h < H; ++h) {
         const float m = warp_max(x[h]);
         if (lane == 0) red[h] = m;
       }
-      ok = bar_and(1, 128, okw);
+      ok = bar_and(1, NT, okw);
       if (!ok) break;
-      float M[16];
+      float M[H];
 #pragma unroll
-      for (int h = 0; h < 16; ++h)
-        M[h] = fmaxf(fmaxf(sh->red[g & 1][0][h], sh->red[g & 1][1][h]), fmaxf(sh->red[g & 1][2][h], sh->red[g & 1][3][h]));
+      for (int h4 = 0; h4 < H; h4 += 4) {
+        const float4 a = *reinterpret_cast<const float4*>(&sh->red[g & 1][0][h0 + h4]);
+        const float4 b = *reinterpret_cast<const float4*>(&sh->red[g & 1][1][h0 + h4]);
+        const float4 c = *reinterpret_cast<const float4*>(&sh->red[g & 1][2][h0 + h4]);
+        const float4 d = *reinterpret_cast<const float4*>(&sh->red[g & 1][3][h0 + h4]);
+        M[h4 + 0] = fmaxf(fmaxf(a.x, b.x), fmaxf(c.x, d.x));
+        M[h4 + 1] = fmaxf(fmaxf(a.y, b.y), fmaxf(c.y, d.y));
+        M[h4 + 2] = fmaxf(fmaxf(a.z, b.z), fmaxf(c.z, d.z));
+        M[h4 + 3] = fmaxf(fmaxf(a.w, b.w), fmaxf(c.w, d.w));
+      }
       bool need = false;
       if (t == 0) {
 #pragma unroll
-        for (int h = 0; h < 16; ++h) { mref[h] = M[h]; lpart[h] = 0.f; }
+        for (int h = 0; h < H; ++h) { mref[h] = M[h]; lpart[h] = 0.f; }
       } else {
 #pragma unroll
-        for (int h = 0; h < 16; ++h) need |= (M[h] > mref[h] + C::kTau);
+        for (int h = 0; h < H; ++h) need |= (M[h] > mref[h] + C::kTau);
       }
-      if (need) {  // lazy rescale of O^T in TMEM (uniform decision across the 128 threads)
-        float alpha[16];
+      if (need) {  // lazy rescale of this head group's O^T columns (uniform within the group)
+        float alpha[H];
 #pragma unroll
-        for (int h = 0; h < 16; ++h) {
+        for (int h = 0; h < H; ++h) {
           const float nm = fmaxf(mref[h], M[h]);
           alpha[h] = ex2(mref[h] - nm);
           mref[h] = nm;
@@ -742,43 +762,47 @@ __device__ void run_softmax(const DecodeParams& p, SharedState* sh, uint8_t* qs,
 #pragma unroll 1
           for (int m = 0; m < 4; ++m) {
 #pragma unroll
-            for (int cb = 0; cb < C::kOCols; cb += 16) {
-              const uint32_t ta = tmem + lane_base + 2 * C::kSCols + m * C::kOCols + cb;
-              uint32_t v[16];
-              tmem_ld16(ta, v);
+            for (int part = 0; part < (KV == 0 ? 1 : 2); ++part) {
+              const uint32_t ta = tmem + lane_base + 2 * C::kSCols + m * C::kOCols + part * 16 + h0;
+              uint32_t v[H];
+              tmem_ld<H>(ta, v);
               tmem_wait_ld();
 #pragma unroll
-              for (int j = 0; j < 16; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha[j]);
-              tmem_st16(ta, v);
+              for (int j = 0; j < H; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha[j]);
+              tmem_st<H>(ta, v);
             }
           }
           tmem_wait_st();
         }
-        ok = bar_and(1, 128, ok2);
-        if (!ok) break;
+        okw = okw && ok2;  // a failed wait aborts at the next tile's barrier
       }
-      // P = 2^(x - mref) <= 2^kTau
-      float P[16];
+      // P = 2^(w - mref) <= 2^kTau
+      float P[H];
 #pragma unroll
-      for (int h = 0; h < 16; ++h) P[h] = ex2(x[h] - mref[h]);
+      for (int h = 0; h < H; ++h) P[h] = ex2(x[h] - mref[h]);
       if (g >= 2) wait_bar(smem_u32(&sh->pv_done[g & 1]), ((g >> 1) & 1) ^ 1, abortf, p.status, p.wait_limit_ns);
       uint8_t* prow = ps + (g & 1) * kPBytes + row * 32;
       const int sw = (row >> 2) & 1;
-      uint32_t c0[4], c1[4];
       if constexpr (KV == 0) {
+        uint32_t wv[H / 2];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
+        for (int j = 0; j < H / 2; ++j) {
           const uint16_t b0 = f_to_bf16_bits(P[2 * j]), b1 = f_to_bf16_bits(P[2 * j + 1]);
           lpart[2 * j] += bf16_bits_to_f(b0);
           lpart[2 * j + 1] += bf16_bits_to_f(b1);
-          const uint32_t wv = static_cast<uint32_t>(b0) | (static_cast<uint32_t>(b1) << 16);
-          if (j < 4) c0[j] = wv; else c1[j - 4] = wv;
+          wv[j] = static_cast<uint32_t>(b0) | (static_cast<uint32_t>(b1) << 16);
         }
+        // heads [h0, h0 + H) are 16-byte chunk(s) h0/8 .. of the 32-byte row
+#pragma unroll
+        for (int c = 0; c < H / 8; ++c)
+          *reinterpret_cast<uint4*>(prow + (((h0 / 8 + c) ^ sw) << 4)) =
+              make_uint4(wv[4 * c], wv[4 * c + 1], wv[4 * c + 2], wv[4 * c + 3]);
       } else {
         const float einv = ldexpf(0.0625f, -static_cast<int>(eadd));   // 2^-eadd / 16
+        uint32_t hw[H / 4], lw[H / 4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          uint32_t hw = 0, lw = 0;
+        for (int j = 0; j < H / 4; ++j) {
+          uint32_t a = 0, b = 0;
 #pragma unroll
           for (int k = 0; k < 4; k += 2) {
             const int h = 4 * j + k;
@@ -787,17 +811,22 @@ __device__ void run_softmax(const DecodeParams& p, SharedState* sh, uint8_t* qs,
             const float2 hd = unpack_e4m3x2(hp);
             const uint32_t lp = pack_e4m3x2((y0 - hd.x) * 16.f, (y1 - hd.y) * 16.f);
             const float2 ld = unpack_e4m3x2(lp);
-            lpart[h] += (hd.x + ld.x * 0.0625f) * einv;
-            lpart[h + 1] += (hd.y + ld.y * 0.0625f) * einv;
-            hw |= hp << (8 * k);
-            lw |= lp << (8 * k);
+            lpart[h] += fmaf(ld.x, 0.0625f, hd.x) * einv;
+            lpart[h + 1] += fmaf(ld.y, 0.0625f, hd.y) * einv;
+            a |= hp << (8 * k);
+            b |= lp << (8 * k);
           }
-          c0[j] = hw;
-          c1[j] = lw;
+          hw[j] = a;
+          lw[j] = b;
+        }
+        if constexpr (H == 16) {
+          *reinterpret_cast<uint4*>(prow + ((0 ^ sw) << 4)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          *reinterpret_cast<uint4*>(prow + ((1 ^ sw) << 4)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        } else {
+          *reinterpret_cast<uint2*>(prow + ((0 ^ sw) << 4) + h0) = make_uint2(hw[0], hw[1]);
+          *reinterpret_cast<uint2*>(prow + ((1 ^ sw) << 4) + h0) = make_uint2(lw[0], lw[1]);
         }
       }
-      *reinterpret_cast<uint4*>(prow + ((0 ^ sw) << 4)) = make_uint4(c0[0], c0[1], c0[2], c0[3]);
-      *reinterpret_cast<uint4*>(prow + ((1 ^ sw) << 4)) = make_uint4(c1[0], c1[1], c1[2], c1[3]);
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(smem_u32(&sh->p_full[g & 1]));
@@ -806,7 +835,7 @@ __device__ void run_softmax(const DecodeParams& p, SharedState* sh, uint8_t* qs,
         // All QK MMAs of this segment are complete (s_full of its last tile was observed):
         // the q buffer can take the next segment's queries.
         has_nxt = it.next(p, nxt);
-        if (has_nxt && nxt.n_hi > nxt.n_lo) {
+        if (has_nxt && nxt.n_hi > nxt.n_lo && ts < 128) {
           if constexpr (KV == 0) stage_q_bf16(p, nxt.b, qs, ts); else stage_q_fp8(p, nxt.b, qs, sh->qscale, ts);
           fence_proxy_async_smem();
           mbar_arrive(smem_u32(&sh->q_ready));
@@ -820,45 +849,41 @@ __device__ void run_softmax(const DecodeParams& p, SharedState* sh, uint8_t* qs,
     ok4 = __all_sync(0xffffffffu, ok4);
     tc_fence_after();
 #pragma unroll
-    for (int h = 0; h < 16; ++h) {
+    for (int h = 0; h < H; ++h) {
       float v = lpart[h];
       v += __shfl_xor_sync(0xffffffffu, v, 16);
       v += __shfl_xor_sync(0xffffffffu, v, 8);
       v += __shfl_xor_sync(0xffffffffu, v, 4);
       v += __shfl_xor_sync(0xffffffffu, v, 2);
       v += __shfl_xor_sync(0xffffffffu, v, 1);
-      if (lane == 0) sh->lsum[quarter][h] = v;
+      if (lane == 0) sh->lsum[quarter][h0 + h] = v;
     }
-    ok = bar_and(1, 128, ok4);
+    ok = bar_and(1, NT, ok4);
     if (!ok) break;
-    float inv[16];
+    float inv[H];
 #pragma unroll
-    for (int h = 0; h < 16; ++h) {
-      const float l = sh->lsum[0][h] + sh->lsum[1][h] + sh->lsum[2][h] + sh->lsum[3][h];
+    for (int h = 0; h < H; ++h) {
+      const float l = sh->lsum[0][h0 + h] + sh->lsum[1][h0 + h] + sh->lsum[2][h0 + h] + sh->lsum[3][h0 + h];
       inv[h] = (KV == 0 ? 1.0f : kv_scale * 0.0625f) / l;
-      if (!cur.direct && ts == 0) p.part_lse[cur.slot * kHeads + h] = mref[h] + lg2(l);
+      if (!cur.direct && quarter == 0 && lane == 0) p.part_lse[cur.slot * kHeads + h0 + h] = mref[h] + lg2(l);
     }
 #pragma unroll 1
     for (int m = 0; m < 4; ++m) {
-      const uint32_t ta = tmem + lane_base + 2 * C::kSCols + m * C::kOCols;
-      uint32_t v[C::kOCols];
-      uint32_t (&v0)[16] = *reinterpret_cast<uint32_t(*)[16]>(&v[0]);
-      tmem_ld16(ta, v0);
-      if constexpr (C::kOCols == 32) {
-        uint32_t (&v1)[16] = *reinterpret_cast<uint32_t(*)[16]>(&v[C::kOCols - 16]);
-        tmem_ld16(ta + 16, v1);
-      }
+      const uint32_t ta = tmem + lane_base + 2 * C::kSCols + m * C::kOCols + h0;
+      uint32_t vh[H], vl[H];
+      tmem_ld<H>(ta, vh);
+      if constexpr (KV != 0) tmem_ld<H>(ta + 16, vl);
       tmem_wait_ld();
       const int d = 128 * m + row;
 #pragma unroll
-      for (int h = 0; h < 16; ++h) {
-        float o = __uint_as_float(v[h]);
-        if constexpr (KV == 1) o += __uint_as_float(v[16 + h]) * 0.0625f;
+      for (int h = 0; h < H; ++h) {
+        float o = __uint_as_float(vh[h]);
+        if constexpr (KV != 0) o = fmaf(__uint_as_float(vl[h]), 0.0625f, o);
         o *= inv[h];
         if (cur.direct)
-          p.out[(static_cast<size_t>(cur.b) * kHeads + h) * kDimV + d] = f_to_bf16_bits(o);
+          p.out[(static_cast<size_t>(cur.b) * kHeads + h0 + h) * kDimV + d] = f_to_bf16_bits(o);
         else
-          p.part_o[(static_cast<size_t>(cur.slot) * kHeads + h) * kDimV + d] = o;
+          p.part_o[(static_cast<size_t>(cur.slot) * kHeads + h0 + h) * kDimV + d] = o;
       }
     }
     tc_fence_before();
@@ -893,14 +918,15 @@ __global__ void __launch_bounds__(Cfg<KV>::kThreads, 1) mla_split_kernel(const _
       }
       for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&sh->etok_full[i]), 128);
     }
+    constexpr uint32_t kSoftThreads = C::kSoftWarps * 32;
     mbar_init(smem_u32(&sh->q_ready), 128);
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&sh->s_full[i]), 1);
-      mbar_init(smem_u32(&sh->s_free[i]), 128);
-      mbar_init(smem_u32(&sh->p_full[i]), 128);
+      mbar_init(smem_u32(&sh->s_free[i]), kSoftThreads);
+      mbar_init(smem_u32(&sh->p_full[i]), kSoftThreads);
       mbar_init(smem_u32(&sh->pv_done[i]), 1);
     }
-    mbar_init(smem_u32(&sh->o_free), 128);
+    mbar_init(smem_u32(&sh->o_free), kSoftThreads);
     mbar_init(smem_u32(&sh->mma_done), 1);
     mbar_init(smem_u32(&sh->mma_done2), 1);
     sh->abort = 0;
@@ -927,7 +953,7 @@ __global__ void __launch_bounds__(Cfg<KV>::kThreads, 1) mla_split_kernel(const _
   } else if (warp == 2) {
     if (lane == 0) run_mma_pv<KV>(p, sh, make_descs(ring, qs, ps), tmem);
     __syncwarp();
-  } else if (warp < 7) {
+  } else if (warp < 3 + C::kSoftWarps) {
     run_softmax<KV>(p, sh, qs, ps, tmem);
   } else {
     if constexpr (KV == 2) run_dequant(p, sh, ring, raw);
