@@ -26,6 +26,8 @@
 // Every pipeline wait is bounded: on timeout the kernel sets the device status word and
 // all roles leave their loops; in-flight copies and MMAs are drained (bounded) before the
 // tensor memory is released.
+#include <cstddef>
+
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -55,7 +57,7 @@ struct Cfg<0> {                    // bf16 cache
   static constexpr int kOCols = 16;
   static constexpr float kTau = 8.0f;
   static constexpr int kSoftWarps = 8;
-  static constexpr int kThreads = 352;       // producer, QK issuer, PV issuer, 8 softmax warps
+  static constexpr int kThreads = 384;       // producer, QK issuer, 2 PV issuers, 8 softmax warps
 };
 template <>
 struct Cfg<1> {                    // fp8 e4m3 cache
@@ -69,7 +71,7 @@ struct Cfg<1> {                    // fp8 e4m3 cache
   static constexpr int kOCols = 32;
   static constexpr float kTau = 4.0f;        // P <= 16 -> 16 P <= 256 fits e4m3
   static constexpr int kSoftWarps = 8;
-  static constexpr int kThreads = 352;       // producer, QK issuer, PV issuer, 8 softmax warps
+  static constexpr int kThreads = 384;       // producer, QK issuer, 2 PV issuers, 8 softmax warps
 };
 
 template <>
@@ -84,7 +86,7 @@ struct Cfg<2> {                    // MXFP4 cache: dequantised to an e4m3 carrie
   static constexpr int kOCols = 32;
   static constexpr float kTau = 4.0f;
   static constexpr int kSoftWarps = 4;
-  static constexpr int kThreads = 352;       // producer, QK, PV, 4 softmax warps, 4 dequant warps
+  static constexpr int kThreads = 384;       // producer, QK, 2 PV, 4 softmax warps, 4 dequant warps
 };
 
 constexpr int kPBytes = 4096;      // one P^T buffer: [128 tokens x 32 B] SW32
@@ -102,19 +104,23 @@ struct SharedState {
   uint64_t p_full[2];
   uint64_t pv_done[2];
   uint64_t o_free;
-  uint64_t mma_done;
-  uint64_t mma_done2;
-  float red[2][4][16];
-  float lsum[4][16];
-  float qscale[16];
+  uint64_t mma_done[3];
+  alignas(16) float red[2][4][16];  // read as float4
+  alignas(16) float lsum[4][16];
+  alignas(16) float qscale[16];
   uint64_t raw_full[kRawStages];   // MXFP4 only
   uint64_t raw_empty[kRawStages];
   uint64_t etok_full[4];
   int etok[4][128];                // per-row max block exponent of the last 4 tiles
   uint2 lut[kLutCount];            // 8 e4m3 bytes per block shift
+  long long seg_total;              // kv_indptr[batch] (balanced mode)
+  int seg_b0;                      // first sequence of this CTA (balanced mode)
   uint32_t tmem_base;
   int abort;
 };
+
+static_assert(offsetof(SharedState, red) % 16 == 0, "float4 reads of SharedState::red need 16-byte alignment");
+static_assert(offsetof(SharedState, lut) % 8 == 0, "uint2 reads of SharedState::lut need 8-byte alignment");
 
 template <int KV>
 __host__ __device__ constexpr size_t raw_bytes() {
@@ -154,6 +160,27 @@ __device__ __forceinline__ int cta_of_token(long long x, long long total, int Ge
   return lo;
 }
 
+// First b in [0, batch) with kv_indptr[b + 1] > lo (batch if none); called by a full warp.
+// Each round probes 32 evenly spaced entries at once, so a batch of B sequences costs
+// ceil(log32(B)) dependent loads instead of log2(B).
+__device__ int warp_first_seq(const int32_t* ip, int batch, long long lo) {
+  const int lane = threadIdx.x & 31;
+  int base = 0, count = batch;
+  while (count > 32) {
+    const int step = (count + 31) / 32;
+    const int bi = base + min(count - 1, lane * step + step - 1);
+    const bool f = lane * step < count && ip[bi + 1] > lo;
+    const unsigned m = __ballot_sync(0xffffffffu, f);
+    if (m == 0) return base + count;
+    const int c = __ffs(m) - 1;
+    base += c * step;
+    count = min(step, count - c * step);
+  }
+  const bool f = lane < count && ip[base + lane + 1] > lo;
+  const unsigned m = __ballot_sync(0xffffffffu, f);
+  return m ? base + __ffs(m) - 1 : base + count;
+}
+
 // Enumerates the (sequence, token range) segments one CTA works on.
 //  uniform (num_splits >= 1): CTA = b * ns + s, one segment (possibly empty), chunk rule
 //     chunk = ceil(ceil(L/ns)/BN)*BN (amd-mixed-mla submission 727205, `mla_s1`).
@@ -165,7 +192,9 @@ struct SegIter {
   int b, split, ns, cta;
   bool uniform, done;
 
-  __device__ void init(const DecodeParams& p, int c) {
+  // total / b0: kv_indptr[batch] and the CTA's first sequence (balanced mode), found once
+  // per CTA by warp_first_seq at kernel start.
+  __device__ void init(const DecodeParams& p, int c, long long total, int b0) {
     cta = c;
     done = false;
     if (p.num_splits >= 1) {
@@ -176,17 +205,11 @@ struct SegIter {
       return;
     }
     uniform = false;
-    long long total = p.kv_indptr[p.batch];
     int Ge = balanced_ctas(total, p.num_ctas);
     if (total <= 0 || c >= Ge) { done = true; return; }
     lo = cta_lo(c, total, Ge);
     hi = cta_lo(c + 1, total, Ge);
-    int l = 0, h = p.batch - 1;                 // first b with kv_indptr[b+1] > lo
-    while (l < h) {
-      int mid = (l + h) >> 1;
-      if (p.kv_indptr[mid + 1] > lo) h = mid; else l = mid + 1;
-    }
-    b = l;
+    b = b0;
   }
 
   __device__ bool next(const DecodeParams& p, Seg& s) {
@@ -323,7 +346,7 @@ __device__ void stage_q_fp8(const DecodeParams& p, int b, uint8_t* qs, float* qs
 __device__ void run_producer_mx(const DecodeParams& p, SharedState* sh, uint8_t* raw) {
   volatile int* abortf = &sh->abort;
   SegIter it;
-  it.init(p, blockIdx.x);
+  it.init(p, blockIdx.x, sh->seg_total, sh->seg_b0);
   Seg s;
   uint32_t ridx = 0;
   bool ok = true;
@@ -363,9 +386,9 @@ __device__ void run_producer(const DecodeParams& p, SharedState* sh, uint8_t* ri
   using C = Cfg<KV>;
   volatile int* abortf = &sh->abort;
   SegIter it;
-  it.init(p, blockIdx.x);
+  it.init(p, blockIdx.x, sh->seg_total, sh->seg_b0);
   Seg s;
-  uint32_t idx = 0;
+  uint32_t idx = 0, slot = 0, phase = 0;
   bool ok = true;
   while (ok && it.next(p, s)) {
     const int n = s.n_hi - s.n_lo;
@@ -374,8 +397,7 @@ __device__ void run_producer(const DecodeParams& p, SharedState* sh, uint8_t* ri
     for (int t = 0; t < ntiles && ok; ++t) {
       const Window w = tile_window<KV>(s, t);
       for (int c = 0; c < C::kSPT; ++c) {
-        const uint32_t slot = idx % C::kRing, use = idx / C::kRing;
-        if (!wait_bar(smem_u32(&sh->empty[slot]), (use & 1) ^ 1, abortf, p.status, p.wait_limit_ns)) {
+        if (!wait_bar(smem_u32(&sh->empty[slot]), phase ^ 1, abortf, p.status, p.wait_limit_ns)) {
           ok = false;
           break;
         }
@@ -395,6 +417,7 @@ __device__ void run_producer(const DecodeParams& p, SharedState* sh, uint8_t* ri
           tma_load_2d(dst, &p.tmap, 128 * c, w.y0, fb);
         }
         ++idx;
+        if (++slot == C::kRing) { slot = 0; phase ^= 1; }
       }
     }
   }
@@ -420,7 +443,7 @@ __device__ __forceinline__ uint32_t e2m1x4_to_e4m3x4(uint32_t nib16, uint2 lut) 
 __device__ void run_dequant(const DecodeParams& p, SharedState* sh, uint8_t* ring, uint8_t* raw) {
   using C = Cfg<2>;
   volatile int* abortf = &sh->abort;
-  const int di = threadIdx.x - 224;        // carrier row of the tile
+  const int di = threadIdx.x - 256;        // carrier row of the tile
   const int half = di >> 6;
   const uint8_t* scales = static_cast<const uint8_t*>(p.kv_scale);
   if (di < kLutCount * 8) {
@@ -432,7 +455,7 @@ __device__ void run_dequant(const DecodeParams& p, SharedState* sh, uint8_t* rin
   }
   bar_sync(2, 128);
   SegIter it;
-  it.init(p, blockIdx.x);
+  it.init(p, blockIdx.x, sh->seg_total, sh->seg_b0);
   Seg s;
   uint32_t g = 0, ridx = 0;
   bool ok = true;
@@ -534,9 +557,9 @@ __device__ void run_mma_qk(const DecodeParams& p, SharedState* sh, const Descs& 
   constexpr uint32_t idq = instr_desc(KV == 0 ? 1u : 0u, 0, 0, 128, C::kN);  // bf16 | e4m3, K-major A and B
   volatile int* abortf = &sh->abort;
   SegIter it;
-  it.init(p, blockIdx.x);
+  it.init(p, blockIdx.x, sh->seg_total, sh->seg_b0);
   Seg s;
-  uint32_t g = 0;
+  uint32_t g = 0, slot = 0, phase = 0;
   int kseg = 0;
   bool ok = true;
   while (ok && it.next(p, s)) {
@@ -551,9 +574,7 @@ __device__ void run_mma_qk(const DecodeParams& p, SharedState* sh, const Descs& 
       const uint32_t d = tmem + (g & 1) * C::kSCols;
 #pragma unroll
       for (int c = 0; c < C::kSPT; ++c) {
-        const uint32_t idx = g * C::kSPT + c, slot = idx % C::kRing;
-        if (!(ok = wait_bar(smem_u32(&sh->full[slot]), (idx / C::kRing) & 1, abortf, p.status, p.wait_limit_ns)))
-          break;
+        if (!(ok = wait_bar(smem_u32(&sh->full[slot]), phase, abortf, p.status, p.wait_limit_ns))) break;
         tc_fence_after();
         const uint64_t a = ds.ring_k + dofs(slot * C::kSlotBytes);
         if constexpr (KV == 0) {
@@ -562,8 +583,7 @@ __device__ void run_mma_qk(const DecodeParams& p, SharedState* sh, const Descs& 
           for (int k = 0; k < 4; ++k) mma_f16(d, a + dofs(32 * k), b + dofs(32 * k), idq, (c | k) != 0);
           if (c < 4) {
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-              mma_f16(d, a + dofs(16384 + 32 * k), b + dofs(2048 + 32 * k), idq, 1u);
+            for (int k = 0; k < 4; ++k) mma_f16(d, a + dofs(16384 + 32 * k), b + dofs(2048 + 32 * k), idq, 1u);
           }
         } else {
           const uint64_t b = ds.q + dofs(c * 4096);
@@ -571,24 +591,26 @@ __device__ void run_mma_qk(const DecodeParams& p, SharedState* sh, const Descs& 
           for (int k = 0; k < (c < 4 ? 4 : 2); ++k) mma_f8(d, a + dofs(32 * k), b + dofs(32 * k), idq, (c | k) != 0);
         }
         if (c == C::kSPT - 1) mma_commit(smem_u32(&sh->empty[slot]));  // rope slot: QK only
+        if (++slot == C::kRing) { slot = 0; phase ^= 1; }
       }
       if (ok) mma_commit(smem_u32(&sh->s_full[g & 1]));
     }
     ++kseg;
   }
-  mma_commit(smem_u32(&sh->mma_done));
-  wait_bar(smem_u32(&sh->mma_done), 0, abortf, p.status, p.wait_limit_ns, false);
+  mma_commit(smem_u32(&sh->mma_done[0]));
+  wait_bar(smem_u32(&sh->mma_done[0]), 0, abortf, p.status, p.wait_limit_ns, false);
 }
 
+// PV issuer `part` (0 or 1) issues the two 128-dim blocks 2*part, 2*part+1 of every tile.
 template <int KV>
-__device__ void run_mma_pv(const DecodeParams& p, SharedState* sh, const Descs& ds, uint32_t tmem) {
+__device__ void run_mma_pv(const DecodeParams& p, SharedState* sh, const Descs& ds, uint32_t tmem, int part) {
   using C = Cfg<KV>;
   constexpr uint32_t idp = instr_desc(KV == 0 ? 1u : 0u, 1, 1, 128, C::kN);  // MN-major A (V^T) and B (P^T)
   volatile int* abortf = &sh->abort;
   SegIter it;
-  it.init(p, blockIdx.x);
+  it.init(p, blockIdx.x, sh->seg_total, sh->seg_b0);
   Seg s;
-  uint32_t g = 0;
+  uint32_t g = 0, slot0 = 0;                      // ring slot of chunk 0 of tile g
   int kseg = 0;
   bool ok = true;
   while (ok && it.next(p, s)) {
@@ -604,8 +626,10 @@ __device__ void run_mma_pv(const DecodeParams& p, SharedState* sh, const Descs& 
       const bool first = (t == 0);
       const uint64_t b = ds.p + dofs((g & 1) * kPBytes);
 #pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        const uint32_t slot = (g * C::kSPT + m) % C::kRing;
+      for (int mm = 0; mm < 2; ++mm) {
+        const int m = 2 * part + mm;
+        uint32_t slot = slot0 + m;
+        if (slot >= C::kRing) slot -= C::kRing;
         const uint64_t a = ds.ring_mn + dofs(slot * C::kSlotBytes);
         const uint32_t d = tmem + 2 * C::kSCols + m * C::kOCols;
         if constexpr (KV == 0) {
@@ -617,12 +641,14 @@ __device__ void run_mma_pv(const DecodeParams& p, SharedState* sh, const Descs& 
         }
         mma_commit(smem_u32(&sh->empty[slot]));
       }
-      mma_commit(smem_u32(&sh->pv_done[g & 1]));
+      mma_commit(smem_u32(&sh->pv_done[g & 1]));   // completes once both PV issuers have committed
+      slot0 += C::kSPT;
+      if (slot0 >= C::kRing) slot0 -= C::kRing;
     }
     ++kseg;
   }
-  mma_commit(smem_u32(&sh->mma_done2));
-  wait_bar(smem_u32(&sh->mma_done2), 0, abortf, p.status, p.wait_limit_ns, false);
+  mma_commit(smem_u32(&sh->mma_done[1 + part]));
+  wait_bar(smem_u32(&sh->mma_done[1 + part]), 0, abortf, p.status, p.wait_limit_ns, false);
 }
 
 // ---------------------------------------------------------------- softmax / epilogue (128 threads)
@@ -648,7 +674,7 @@ __device__ void run_softmax(const DecodeParams& p, SharedState* sh, uint8_t* qs,
   constexpr int NT = NW * 32;
   constexpr int H = 64 / NW;                               // heads per thread: 16 or 8
   volatile int* abortf = &sh->abort;
-  const int ts = threadIdx.x - 96;
+  const int ts = threadIdx.x - 128;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int quarter = warp & 3;
   const int hg = (ts >> 5) >> 2;                           // head group (0 when H = 16)
@@ -660,7 +686,7 @@ __device__ void run_softmax(const DecodeParams& p, SharedState* sh, uint8_t* qs,
   const float xscale = p.logit_scale_log2 * kv_scale;    // raw dot product -> log2-domain logit
 
   SegIter it;
-  it.init(p, blockIdx.x);
+  it.init(p, blockIdx.x, sh->seg_total, sh->seg_b0);
   Seg cur, nxt;
   bool has_cur = it.next(p, cur);
   if (has_cur && cur.n_hi > cur.n_lo && ts < 128) {
@@ -924,11 +950,10 @@ __global__ void __launch_bounds__(Cfg<KV>::kThreads, 1) mla_split_kernel(const _
       mbar_init(smem_u32(&sh->s_full[i]), 1);
       mbar_init(smem_u32(&sh->s_free[i]), kSoftThreads);
       mbar_init(smem_u32(&sh->p_full[i]), kSoftThreads);
-      mbar_init(smem_u32(&sh->pv_done[i]), 1);
+      mbar_init(smem_u32(&sh->pv_done[i]), 2);   // one commit from each PV issuer
     }
     mbar_init(smem_u32(&sh->o_free), kSoftThreads);
-    mbar_init(smem_u32(&sh->mma_done), 1);
-    mbar_init(smem_u32(&sh->mma_done2), 1);
+    for (int i = 0; i < 3; ++i) mbar_init(smem_u32(&sh->mma_done[i]), 1);
     sh->abort = 0;
     fence_barrier_init();
     fence_proxy_async_smem();
@@ -936,6 +961,13 @@ __global__ void __launch_bounds__(Cfg<KV>::kThreads, 1) mla_split_kernel(const _
   if (warp == 1) {
     tmem_alloc(smem_u32(&sh->tmem_base), C::kTmemCols);
     tmem_relinquish();
+  }
+  if (warp == 0 && p.num_splits < 1) {
+    const long long total = p.kv_indptr[p.batch];
+    const int Ge = balanced_ctas(total, p.num_ctas);
+    int b0 = p.batch;
+    if (total > 0 && static_cast<int>(blockIdx.x) < Ge) b0 = warp_first_seq(p.kv_indptr, p.batch, cta_lo(blockIdx.x, total, Ge));
+    if (lane == 0) { sh->seg_total = total; sh->seg_b0 = b0; }
   }
   tc_fence_before();
   __syncthreads();
@@ -950,10 +982,10 @@ __global__ void __launch_bounds__(Cfg<KV>::kThreads, 1) mla_split_kernel(const _
   } else if (warp == 1) {
     if (lane == 0) run_mma_qk<KV>(p, sh, make_descs(ring, qs, ps), tmem);
     __syncwarp();
-  } else if (warp == 2) {
-    if (lane == 0) run_mma_pv<KV>(p, sh, make_descs(ring, qs, ps), tmem);
+  } else if (warp == 2 || warp == 3) {
+    if (lane == 0) run_mma_pv<KV>(p, sh, make_descs(ring, qs, ps), tmem, warp - 2);
     __syncwarp();
-  } else if (warp < 3 + C::kSoftWarps) {
+  } else if (warp < 4 + C::kSoftWarps) {
     run_softmax<KV>(p, sh, qs, ps, tmem);
   } else {
     if constexpr (KV == 2) run_dequant(p, sh, ring, raw);
