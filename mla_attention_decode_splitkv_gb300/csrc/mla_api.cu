@@ -20,7 +20,9 @@ struct Workspace {
   float* part_o = nullptr;
   float* part_lse = nullptr;
   int* status = nullptr;
+  int* seq_count = nullptr;   // per-sequence piece counters, zero between calls
   long long slots = 0;
+  long long counters = 0;
 };
 
 std::mutex g_mu;
@@ -37,7 +39,8 @@ struct ProfRecord {
 };
 std::mutex g_prof_mu;
 bool g_prof_on = false;
-std::vector<ProfRecord> g_prof;
+std::vector<ProfRecord> g_prof;   // event pool, reused across begin/end cycles
+size_t g_prof_n = 0;              // records used since begin
 
 int note_cuda(cudaError_t e) {
   t_last_cuda_error = cudaGetErrorName(e);
@@ -64,13 +67,24 @@ int device_info(int* dev_out, int* sms_out, int* cc_out) {
   return MLA_OK;
 }
 
-// Grow-only workspace of `slots` partial results on device `dev` (caller holds g_mu).
-int ensure_workspace(int dev, long long slots) {
+// Grow-only workspace of `slots` partial results and `counters` per-sequence counters on
+// device `dev` (caller holds g_mu).  Counters are zeroed when allocated; the kernel leaves
+// them at zero after every complete call.
+int ensure_workspace(int dev, long long slots, long long counters) {
   Workspace& w = g_ws[dev];
   if (w.status == nullptr) {
     cudaError_t e = cudaMalloc(&w.status, sizeof(int));
     if (e != cudaSuccess) { w.status = nullptr; cudaGetLastError(); return MLA_ERR_NO_MEMORY; }
     if ((e = cudaMemset(w.status, 0, sizeof(int))) != cudaSuccess) return note_cuda(e);
+  }
+  if (counters > w.counters) {
+    if (w.seq_count) { cudaFree(w.seq_count); w.seq_count = nullptr; }
+    w.counters = 0;
+    cudaError_t e = cudaMalloc(&w.seq_count, static_cast<size_t>(counters) * sizeof(int));
+    if (e != cudaSuccess) { w.seq_count = nullptr; cudaGetLastError(); return MLA_ERR_NO_MEMORY; }
+    if ((e = cudaMemset(w.seq_count, 0, static_cast<size_t>(counters) * sizeof(int))) != cudaSuccess) return note_cuda(e);
+    if ((e = cudaDeviceSynchronize()) != cudaSuccess) return note_cuda(e);
+    w.counters = counters;
   }
   if (slots <= w.slots) return MLA_OK;
   if (w.part_o) { cudaFree(w.part_o); w.part_o = nullptr; }
@@ -175,7 +189,7 @@ int mla_decode_reserve_workspace(int slots) {
   int rc = device_info(&dev, &sms, &cc);
   if (rc) return rc;
   std::lock_guard<std::mutex> lk(g_mu);
-  return ensure_workspace(dev, slots);
+  return ensure_workspace(dev, slots, slots);
 }
 
 int mla_decode_release_workspace(void) {
@@ -188,6 +202,7 @@ int mla_decode_release_workspace(void) {
   if (w.part_o) cudaFree(w.part_o);
   if (w.part_lse) cudaFree(w.part_lse);
   if (w.status) cudaFree(w.status);
+  if (w.seq_count) cudaFree(w.seq_count);
   w = Workspace();
   return e == cudaSuccess ? MLA_OK : note_cuda(e);
 }
@@ -228,7 +243,7 @@ int mla_decode(const void* q, const void* kv, const void* kv_scale, const int32_
   Workspace ws;
   {
     std::lock_guard<std::mutex> lk(g_mu);
-    rc = ensure_workspace(dev, slots_needed(batch, ns, sms));
+    rc = ensure_workspace(dev, slots_needed(batch, ns, sms), ns == 1 ? 0 : batch);
     if (rc) return rc;
     ws = g_ws[dev];
   }
@@ -246,6 +261,7 @@ int mla_decode(const void* q, const void* kv, const void* kv_scale, const int32_
   p.part_o = ws.part_o;
   p.part_lse = ws.part_lse;
   p.status = ws.status;
+  p.seq_count = ws.seq_count;
   p.batch = batch;
   p.num_splits = ns;
   p.num_ctas = static_cast<int>(grid_ll);
@@ -256,45 +272,31 @@ int mla_decode(const void* q, const void* kv, const void* kv_scale, const int32_
   bool prof = false;
   {
     std::lock_guard<std::mutex> lk(g_prof_mu);
-    prof = g_prof_on;
+    if (g_prof_on) {
+      if (g_prof_n == g_prof.size()) {
+        ProfRecord r{nullptr, nullptr, nullptr};
+        cudaEventCreate(&r.start);
+        cudaEventCreate(&r.split_end);
+        cudaEventCreate(&r.end);
+        g_prof.push_back(r);
+      }
+      rec = g_prof[g_prof_n++];
+      prof = true;
+    }
   }
-  if (prof) {
-    cudaEventCreate(&rec.start);
-    cudaEventCreate(&rec.split_end);
-    cudaEventCreate(&rec.end);
-    cudaEventRecord(rec.start, st);
-  }
+  if (prof) cudaEventRecord(rec.start, st);
   cudaError_t e = mla::launch_split(kv_dtype, p, static_cast<int>(grid_ll), st);
   if (e != cudaSuccess) return note_cuda(e);
-  if (prof) cudaEventRecord(rec.split_end, st);
-  if (ns != 1) {
-    mla::CombineParams c;
-    c.kv_indptr = kv_indptr;
-    c.part_o = ws.part_o;
-    c.part_lse = ws.part_lse;
-    c.out = static_cast<uint16_t*>(out);
-    c.batch = batch;
-    c.num_splits = ns;
-    c.num_ctas = static_cast<int>(grid_ll);
-    e = mla::launch_combine(c, st);
-    if (e != cudaSuccess) return note_cuda(e);
-  }
   if (prof) {
+    cudaEventRecord(rec.split_end, st);
     cudaEventRecord(rec.end, st);
-    std::lock_guard<std::mutex> lk(g_prof_mu);
-    g_prof.push_back(rec);
   }
   return MLA_OK;
 }
 
 int mla_decode_profile_begin(void) {
   std::lock_guard<std::mutex> lk(g_prof_mu);
-  for (auto& r : g_prof) {
-    cudaEventDestroy(r.start);
-    cudaEventDestroy(r.split_end);
-    cudaEventDestroy(r.end);
-  }
-  g_prof.clear();
+  g_prof_n = 0;
   g_prof_on = true;
   return MLA_OK;
 }
@@ -305,7 +307,8 @@ int mla_decode_profile_end(double* split_ms, double* call_ms, int* calls) {
   double s = 0.0, t = 0.0;
   int n = 0;
   int rc = MLA_OK;
-  for (auto& r : g_prof) {
+  for (size_t i = 0; i < g_prof_n; ++i) {
+    const ProfRecord& r = g_prof[i];
     float a = 0.f, b = 0.f;
     cudaError_t e1 = cudaEventSynchronize(r.end);
     cudaError_t e2 = cudaEventElapsedTime(&a, r.start, r.split_end);
@@ -317,11 +320,8 @@ int mla_decode_profile_end(double* split_ms, double* call_ms, int* calls) {
       t += b;
       ++n;
     }
-    cudaEventDestroy(r.start);
-    cudaEventDestroy(r.split_end);
-    cudaEventDestroy(r.end);
   }
-  g_prof.clear();
+  g_prof_n = 0;
   if (split_ms) *split_ms = s;
   if (call_ms) *call_ms = t;
   if (calls) *calls = n;

@@ -29,6 +29,7 @@ struct DecodeParams {
   float* part_o;                   // [slots][16][512] normalised partial outputs
   float* part_lse;                 // [slots][16]      log2-domain log-sum-exp of the partials
   int* status;                     // device status word
+  int* seq_count;                  // [batch] pieces written per sequence (zero between calls)
   int batch;
   int num_splits;                  // >= 1: uniform splits per sequence; 0: balanced over CTAs
   int num_ctas;                    // grid size (balanced mode: persistent CTAs)
@@ -36,20 +37,10 @@ struct DecodeParams {
   unsigned long long wait_limit_ns;
 };
 
-struct CombineParams {
-  const int32_t* kv_indptr;
-  const float* part_o;
-  const float* part_lse;
-  uint16_t* out;
-  int batch;
-  int num_splits;                  // >= 2 uniform, 0 balanced
-  int num_ctas;                    // balanced mode grid of the split kernel
-};
 
 // Per-kv-dtype launch geometry (host side).
 int split_threads(int kv_dtype);
 size_t split_smem_bytes(int kv_dtype);
 cudaError_t launch_split(int kv_dtype, const DecodeParams& p, int grid, cudaStream_t stream);
-cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
 
 }  // namespace mla

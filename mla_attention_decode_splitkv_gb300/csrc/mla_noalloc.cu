@@ -5,8 +5,9 @@
 // that owns every device allocation through its own pre-sized pool and forbids stray ones,
 // or a latency-critical loop that cannot afford cudaMalloc/cudaFree (cudaFree synchronises
 // the whole device).  mla_decode grows a library-owned workspace with cudaMalloc on first
-// use; this entry point instead keeps its scratch (the split partial results and the
-// kernel status word) in a fixed-size array that lives in the library's device module.
+// use; this entry point instead keeps its scratch (the split partial results, the
+// per-sequence piece counters and the kernel status word) in a fixed-size array that lives
+// in the library's device module.
 //
 // The array is a file-scope static __device__ object, so every GPU that loads this library
 // holds kNoallocScratchBytes of it until the process exits.  Host code cannot use the
@@ -30,10 +31,13 @@ constexpr int kMaxDevices = 64;
 constexpr size_t kSlotBytes = static_cast<size_t>(mla::kHeads) * mla::kDimV * sizeof(float);   // partial O
 constexpr size_t kLseBytes = static_cast<size_t>(mla::kHeads) * sizeof(float);                 // partial lse
 constexpr size_t kStatusBytes = 256;
+constexpr size_t kCounterBytes = static_cast<size_t>(MLA_NOALLOC_MAX_SLOTS) * sizeof(int);
 constexpr size_t kNoallocScratchBytes =
-    static_cast<size_t>(MLA_NOALLOC_MAX_SLOTS) * (kSlotBytes + kLseBytes) + kStatusBytes;
+    static_cast<size_t>(MLA_NOALLOC_MAX_SLOTS) * (kSlotBytes + kLseBytes) + kStatusBytes + kCounterBytes;
 
 // Layout: [status word (256 B)] [partial O: slots x 16 x 512 fp32] [partial lse: slots x 16 fp32]
+//         [piece counters: slots x int32; zero at load, left at zero by every complete call]
+// A call needing partial slots has batch <= slots, so the counters always fit.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
 std::mutex g_mu;
@@ -106,6 +110,8 @@ extern "C" int mla_decode_noalloc(const void* q, const void* kv, const void* kv_
   int* status = reinterpret_cast<int*>(b);
   float* part_o = reinterpret_cast<float*>(b + kStatusBytes);
   float* part_lse = reinterpret_cast<float*>(b + kStatusBytes + static_cast<size_t>(MLA_NOALLOC_MAX_SLOTS) * kSlotBytes);
+  int* seq_count = reinterpret_cast<int*>(b + kStatusBytes +
+                                          static_cast<size_t>(MLA_NOALLOC_MAX_SLOTS) * (kSlotBytes + kLseBytes));
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   // The status word must start each call at zero (the kernels only ever set bits in it).
   if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess) { cudaGetLastError(); return MLA_ERR_CUDA; }
@@ -123,22 +129,12 @@ extern "C" int mla_decode_noalloc(const void* q, const void* kv, const void* kv_
   p.part_o = part_o;
   p.part_lse = part_lse;
   p.status = status;
+  p.seq_count = seq_count;
   p.batch = batch;
   p.num_splits = ns;
   p.num_ctas = static_cast<int>(grid);
   p.logit_scale_log2 = static_cast<float>((1.0 / std::sqrt(static_cast<double>(mla::kDim))) * 1.4426950408889634);
   p.wait_limit_ns = 2000000000ull;
   if (mla::launch_split(kv_dtype, p, static_cast<int>(grid), st) != cudaSuccess) { cudaGetLastError(); return MLA_ERR_CUDA; }
-  if (ns != 1) {
-    mla::CombineParams c;
-    c.kv_indptr = kv_indptr;
-    c.part_o = part_o;
-    c.part_lse = part_lse;
-    c.out = static_cast<uint16_t*>(out);
-    c.batch = batch;
-    c.num_splits = ns;
-    c.num_ctas = static_cast<int>(grid);
-    if (mla::launch_combine(c, st) != cudaSuccess) { cudaGetLastError(); return MLA_ERR_CUDA; }
-  }
   return MLA_OK;
 }

@@ -115,6 +115,8 @@ struct SharedState {
   uint2 lut[kLutCount];            // 8 e4m3 bytes per block shift
   long long seg_total;              // kv_indptr[batch] (balanced mode)
   int seg_b0;                      // first sequence of this CTA (balanced mode)
+  int merge_slot0;                 // fused combine: first slot and piece count to merge
+  int merge_pieces;
   uint32_t tmem_base;
   int abort;
 };
@@ -190,7 +192,7 @@ __device__ int warp_first_seq(const int32_t* ip, int batch, long long lo) {
 struct SegIter {
   long long lo, hi;
   int b, split, ns, cta;
-  bool uniform, done;
+  bool uniform, done, last_cta;
 
   // total / b0: kv_indptr[batch] and the CTA's first sequence (balanced mode), found once
   // per CTA by warp_first_seq at kernel start.
@@ -206,9 +208,10 @@ struct SegIter {
     }
     uniform = false;
     int Ge = balanced_ctas(total, p.num_ctas);
-    if (total <= 0 || c >= Ge) { done = true; return; }
+    if (c >= Ge) { done = true; return; }
     lo = cta_lo(c, total, Ge);
     hi = cta_lo(c + 1, total, Ge);
+    last_cta = (c == Ge - 1);
     b = b0;
   }
 
@@ -227,14 +230,22 @@ struct SegIter {
       done = true;
       return true;
     }
+    // Non-empty sequences: the part inside [lo, hi).  An empty sequence at token position x
+    // belongs to the CTA with lo <= x < hi (the last CTA also owns x == total); it is
+    // returned as an empty direct segment so that its output row gets written as zeros.
     while (b < p.batch) {
       int r0 = p.kv_indptr[b], r1 = p.kv_indptr[b + 1];
-      if (r0 >= hi) break;
-      long long a = lo > r0 ? lo : r0, e = hi < r1 ? hi : r1;
+      if (r0 > hi || (r0 == hi && !last_cta)) break;
       int bb = b++;
-      if (e > a) {
-        s.b = bb; s.row0 = r0; s.n_lo = (int)(a - r0); s.n_hi = (int)(e - r0);
-        s.slot = bb + cta; s.direct = (a == r0 && e == r1);
+      if (r1 > r0) {
+        long long a = lo > r0 ? lo : r0, e = hi < r1 ? hi : r1;
+        if (e > a) {
+          s.b = bb; s.row0 = r0; s.n_lo = (int)(a - r0); s.n_hi = (int)(e - r0);
+          s.slot = bb + cta; s.direct = (a == r0 && e == r1);
+          return true;
+        }
+      } else if (r0 >= lo && (r0 < hi || last_cta)) {
+        s.b = bb; s.row0 = r0; s.n_lo = 0; s.n_hi = 0; s.slot = bb + cta; s.direct = true;
         return true;
       }
     }
@@ -484,37 +495,39 @@ __device__ void run_dequant(const DecodeParams& p, SharedState* sh, uint8_t* rin
                       p.wait_limit_ns);
       if (!ok) break;
       int emax = 127;
+      uint32_t slot = (g * C::kSPT) % C::kRing;     // ring slot of chunk 0 of this tile
       if (live) {
         emax = 0;
 #pragma unroll
         for (int j = 0; j < 9; ++j) emax = max(emax, max(static_cast<int>(sc[j] & 0xFF), static_cast<int>(sc[j] >> 8)));
         const uint4* src = reinterpret_cast<const uint4*>(raw + (my_r % kRawStages) * kRawBytes + (di & 63) * kMxPacked);
-#pragma unroll 1
+        // Fully unrolled over the 18 blocks so that the block scales stay in registers.
+#pragma unroll
         for (int c = 0; c < C::kSPT; ++c) {
-          uint8_t* dst = ring + ((g * C::kSPT + c) % C::kRing) * C::kSlotBytes + di * 128;
-          const int nblk = c < 4 ? 4 : 2;
-          for (int bk = 0; bk < nblk; ++bk) {
+          uint8_t* dst = ring + slot * C::kSlotBytes + di * 128;
+#pragma unroll
+          for (int bk = 0; bk < (c < 4 ? 4 : 2); ++bk) {
             const int j = 4 * c + bk;                       // block (32 elements, 16 packed bytes)
             const int e = static_cast<int>((sc[j >> 1] >> (8 * (j & 1))) & 0xFF);
             const uint2 lut = sh->lut[min(emax - e, kLutCount - 1)];
             const uint4 v = src[j];
-            const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-            uint32_t o[8];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              o[2 * q] = e2m1x4_to_e4m3x4(wv[q] & 0xFFFFu, lut);
-              o[2 * q + 1] = e2m1x4_to_e4m3x4(wv[q] >> 16, lut);
-            }
+            const uint32_t o0 = e2m1x4_to_e4m3x4(v.x & 0xFFFFu, lut), o1 = e2m1x4_to_e4m3x4(v.x >> 16, lut);
+            const uint32_t o2 = e2m1x4_to_e4m3x4(v.y & 0xFFFFu, lut), o3 = e2m1x4_to_e4m3x4(v.y >> 16, lut);
+            const uint32_t o4 = e2m1x4_to_e4m3x4(v.z & 0xFFFFu, lut), o5 = e2m1x4_to_e4m3x4(v.z >> 16, lut);
+            const uint32_t o6 = e2m1x4_to_e4m3x4(v.w & 0xFFFFu, lut), o7 = e2m1x4_to_e4m3x4(v.w >> 16, lut);
             const int pp = 2 * bk;
-            *reinterpret_cast<uint4*>(dst + ((pp ^ (di & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
-            *reinterpret_cast<uint4*>(dst + (((pp + 1) ^ (di & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+            *reinterpret_cast<uint4*>(dst + ((pp ^ (di & 7)) << 4)) = make_uint4(o0, o1, o2, o3);
+            *reinterpret_cast<uint4*>(dst + (((pp + 1) ^ (di & 7)) << 4)) = make_uint4(o4, o5, o6, o7);
           }
+          if (++slot == C::kRing) slot = 0;
         }
       } else {
+#pragma unroll
         for (int c = 0; c < C::kSPT; ++c) {
-          uint4* dst = reinterpret_cast<uint4*>(ring + ((g * C::kSPT + c) % C::kRing) * C::kSlotBytes + di * 128);
+          uint4* dst = reinterpret_cast<uint4*>(ring + slot * C::kSlotBytes + di * 128);
 #pragma unroll
           for (int q = 0; q < 8; ++q) dst[q] = make_uint4(0u, 0u, 0u, 0u);
+          if (++slot == C::kRing) slot = 0;
         }
       }
       if (has_half) mbar_arrive(smem_u32(&sh->raw_empty[my_r % kRawStages]));
@@ -652,6 +665,101 @@ __device__ void run_mma_pv(const DecodeParams& p, SharedState* sh, const Descs& 
 }
 
 // ---------------------------------------------------------------- softmax / epilogue (128 threads)
+// Pieces (partial results) of sequence b and their first workspace slot.
+__device__ __forceinline__ int seq_pieces(const DecodeParams& p, int b, long long total, int* slot0) {
+  if (p.num_splits >= 1) {
+    *slot0 = b * p.num_splits;
+    return p.num_splits;
+  }
+  const int Ge = balanced_ctas(total, p.num_ctas);
+  const int cf = cta_of_token(p.kv_indptr[b], total, Ge);
+  const int cl = cta_of_token(static_cast<long long>(p.kv_indptr[b + 1]) - 1, total, Ge);
+  *slot0 = b + cf;
+  return cl - cf + 1;
+}
+
+// Log-sum-exp merge of all pieces of sequence b (run by the CTA that wrote the last piece):
+// m = max_s lse_s, w_s = 2^(lse_s - m), out = sum w_s o_s / sum w_s (bf16, RNE).  Pieces
+// with lse = -inf carry no weight (their partial output was never written); a row with no
+// weight at all is written as 0.  One warp per head: lane l owns dims 4l + 128j (j < 4);
+// weights are broadcast by shuffle and the loads of four pieces are issued together.
+// Partials of other CTAs are read through L2 (ld.global.cg).
+__device__ void merge_pieces(const DecodeParams& p, int b, int slot0, int pieces, int ts, int nt) {
+  const int warp = ts >> 5, lane = ts & 31, nw = nt >> 5;
+  for (int h = warp; h < kHeads; h += nw) {
+    float m = kNegInf;
+    for (int s = lane; s < pieces; s += 32) m = fmaxf(m, __ldcg(p.part_lse + (slot0 + s) * kHeads + h));
+    m = warp_max(m);
+    float4 acc[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+    float ws = 0.f;
+    if (m != kNegInf) {
+      for (int s0 = 0; s0 < pieces; s0 += 32) {
+        const int cnt = min(32, pieces - s0);
+        const float l = lane < cnt ? __ldcg(p.part_lse + (slot0 + s0 + lane) * kHeads + h) : kNegInf;
+        const float myw = (l == kNegInf) ? 0.f : ex2(l - m);
+        float t = myw;
+        t += __shfl_xor_sync(0xffffffffu, t, 16);
+        t += __shfl_xor_sync(0xffffffffu, t, 8);
+        t += __shfl_xor_sync(0xffffffffu, t, 4);
+        t += __shfl_xor_sync(0xffffffffu, t, 2);
+        t += __shfl_xor_sync(0xffffffffu, t, 1);
+        ws += t;
+#pragma unroll 4
+        for (int k = 0; k < cnt; ++k) {
+          const float w = __shfl_sync(0xffffffffu, myw, k);
+          const float4* src =
+              reinterpret_cast<const float4*>(p.part_o + (static_cast<size_t>(slot0 + s0 + k) * kHeads + h) * kDimV);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const float4 v = __ldcg(src + lane + 32 * j);
+            if (w != 0.f) {  // a weightless piece's partial was never written: never read it into the sum
+              acc[j].x = fmaf(w, v.x, acc[j].x);
+              acc[j].y = fmaf(w, v.y, acc[j].y);
+              acc[j].z = fmaf(w, v.z, acc[j].z);
+              acc[j].w = fmaf(w, v.w, acc[j].w);
+            }
+          }
+        }
+      }
+    }
+    const float inv = ws > 0.f ? 1.0f / ws : 0.f;
+    uint2* dst = reinterpret_cast<uint2*>(p.out + (static_cast<size_t>(b) * kHeads + h) * kDimV);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t lo = static_cast<uint32_t>(f_to_bf16_bits(acc[j].x * inv)) |
+                          (static_cast<uint32_t>(f_to_bf16_bits(acc[j].y * inv)) << 16);
+      const uint32_t hi = static_cast<uint32_t>(f_to_bf16_bits(acc[j].z * inv)) |
+                          (static_cast<uint32_t>(f_to_bf16_bits(acc[j].w * inv)) << 16);
+      dst[lane + 32 * j] = make_uint2(lo, hi);
+    }
+  }
+}
+
+// After this CTA wrote its piece of sequence s.b: count the piece; the CTA whose piece
+// completes the count merges all pieces and re-arms the counter for the next call.
+// Reached by all `nt` softmax threads.
+__device__ void finish_piece(const DecodeParams& p, SharedState* sh, const Seg& s, int ts, int nt) {
+  __threadfence();
+  bar_sync(1, nt);
+  if (ts == 0) {
+    int slot0 = 0;
+    const int pieces = seq_pieces(p, s.b, sh->seg_total, &slot0);
+    const int old = atomicAdd(p.seq_count + s.b, 1);
+    const bool last = (old == pieces - 1);
+    if (last) p.seq_count[s.b] = 0;
+    sh->merge_slot0 = slot0;
+    sh->merge_pieces = last ? pieces : 0;
+  }
+  bar_sync(1, nt);
+  const int pieces = sh->merge_pieces;
+  if (pieces > 0) {
+    __threadfence();
+    merge_pieces(p, s.b, sh->merge_slot0, pieces, ts, nt);
+  }
+}
+
 template <int KV>
 __device__ void write_empty_result(const DecodeParams& p, const Seg& s, int ts) {
   if (s.direct) {
@@ -689,11 +797,20 @@ __device__ void run_softmax(const DecodeParams& p, SharedState* sh, uint8_t* qs,
   it.init(p, blockIdx.x, sh->seg_total, sh->seg_b0);
   Seg cur, nxt;
   bool has_cur = it.next(p, cur);
-  if (has_cur && cur.n_hi > cur.n_lo && ts < 128) {
-    if constexpr (KV == 0) stage_q_bf16(p, cur.b, qs, ts); else stage_q_fp8(p, cur.b, qs, sh->qscale, ts);
-    fence_proxy_async_smem();
-    mbar_arrive(smem_u32(&sh->q_ready));
-  }
+  // Stage q of the first non-empty segment (the iterator may first yield empty ones).
+  auto stage_next_nonempty = [&](const SegIter& from, const Seg* first) {
+    Seg sn;
+    bool found = false;
+    if (first != nullptr && first->n_hi > first->n_lo) { sn = *first; found = true; }
+    SegIter look = from;
+    while (!found && look.next(p, sn)) found = sn.n_hi > sn.n_lo;
+    if (found && ts < 128) {
+      if constexpr (KV == 0) stage_q_bf16(p, sn.b, qs, ts); else stage_q_fp8(p, sn.b, qs, sh->qscale, ts);
+      fence_proxy_async_smem();
+      mbar_arrive(smem_u32(&sh->q_ready));
+    }
+  };
+  if (has_cur) stage_next_nonempty(it, &cur);
   bar_sync(1, NT);  // qscale visible to all softmax threads
   uint32_t g = 0;
   bool ok = true;
@@ -701,6 +818,7 @@ __device__ void run_softmax(const DecodeParams& p, SharedState* sh, uint8_t* qs,
     const int n = cur.n_hi - cur.n_lo;
     if (n <= 0) {
       write_empty_result<KV>(p, cur, ts);
+      if (!cur.direct) finish_piece(p, sh, cur, ts, NT);
       has_cur = it.next(p, cur);
       continue;
     }
@@ -861,11 +979,7 @@ __device__ void run_softmax(const DecodeParams& p, SharedState* sh, uint8_t* qs,
         // All QK MMAs of this segment are complete (s_full of its last tile was observed):
         // the q buffer can take the next segment's queries.
         has_nxt = it.next(p, nxt);
-        if (has_nxt && nxt.n_hi > nxt.n_lo && ts < 128) {
-          if constexpr (KV == 0) stage_q_bf16(p, nxt.b, qs, ts); else stage_q_fp8(p, nxt.b, qs, sh->qscale, ts);
-          fence_proxy_async_smem();
-          mbar_arrive(smem_u32(&sh->q_ready));
-        }
+        if (has_nxt) stage_next_nonempty(it, &nxt);
       }
     }
     if (!ok) break;
@@ -914,6 +1028,7 @@ __device__ void run_softmax(const DecodeParams& p, SharedState* sh, uint8_t* qs,
     }
     tc_fence_before();
     mbar_arrive(smem_u32(&sh->o_free));
+    if (!cur.direct) finish_piece(p, sh, cur, ts, NT);
     cur = nxt;
     has_cur = has_nxt;
   }
@@ -966,7 +1081,8 @@ __global__ void __launch_bounds__(Cfg<KV>::kThreads, 1) mla_split_kernel(const _
     const long long total = p.kv_indptr[p.batch];
     const int Ge = balanced_ctas(total, p.num_ctas);
     int b0 = p.batch;
-    if (total > 0 && static_cast<int>(blockIdx.x) < Ge) b0 = warp_first_seq(p.kv_indptr, p.batch, cta_lo(blockIdx.x, total, Ge));
+    // first b with kv_indptr[b+1] >= lo: empty sequences sitting at lo are this CTA's too
+    if (static_cast<int>(blockIdx.x) < Ge) b0 = warp_first_seq(p.kv_indptr, p.batch, cta_lo(blockIdx.x, total, Ge) - 1);
     if (lane == 0) { sh->seg_total = total; sh->seg_b0 = b0; }
   }
   tc_fence_before();
@@ -996,45 +1112,6 @@ __global__ void __launch_bounds__(Cfg<KV>::kThreads, 1) mla_split_kernel(const _
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
-}
-
-// ---------------------------------------------------------------- combine
-// Per (b, h): m = max_s lse_s, w_s = 2^(lse_s - m), out = sum w_s o_s / sum w_s (bf16, RNE).
-// Splits with lse = -inf carry no weight; a row with no weight at all is written as 0.
-__global__ void __launch_bounds__(128) mla_combine_kernel(const CombineParams p) {
-  const int b = blockIdx.x >> 4, h = blockIdx.x & 15, t = threadIdx.x;
-  uint2* dst = reinterpret_cast<uint2*>(p.out + (static_cast<size_t>(b) * kHeads + h) * kDimV) + t;
-  int s0, s1;
-  if (p.num_splits >= 1) {
-    s0 = b * p.num_splits;
-    s1 = s0 + p.num_splits;
-  } else {
-    const int r0 = p.kv_indptr[b], r1 = p.kv_indptr[b + 1];
-    if (r1 <= r0) { *dst = make_uint2(0u, 0u); return; }
-    const long long total = p.kv_indptr[p.batch];
-    const int Ge = balanced_ctas(total, p.num_ctas);
-    const int cf = cta_of_token(r0, total, Ge), cl = cta_of_token(static_cast<long long>(r1) - 1, total, Ge);
-    if (cf == cl) return;  // one CTA held the whole sequence and wrote it directly
-    s0 = b + cf;
-    s1 = b + cl + 1;
-  }
-  float m = kNegInf;
-  for (int s = s0; s < s1; ++s) m = fmaxf(m, __ldg(p.part_lse + s * kHeads + h));
-  if (m == kNegInf) { *dst = make_uint2(0u, 0u); return; }
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float ws = 0.f;
-  for (int s = s0; s < s1; ++s) {
-    const float l = __ldg(p.part_lse + s * kHeads + h);
-    if (l == kNegInf) continue;
-    const float w = ex2(l - m);
-    ws += w;
-    const float4 v = __ldg(reinterpret_cast<const float4*>(p.part_o + (static_cast<size_t>(s) * kHeads + h) * kDimV) + t);
-    acc.x += w * v.x; acc.y += w * v.y; acc.z += w * v.z; acc.w += w * v.w;
-  }
-  const float inv = 1.0f / ws;
-  const uint32_t lo = static_cast<uint32_t>(f_to_bf16_bits(acc.x * inv)) | (static_cast<uint32_t>(f_to_bf16_bits(acc.y * inv)) << 16);
-  const uint32_t hi = static_cast<uint32_t>(f_to_bf16_bits(acc.z * inv)) | (static_cast<uint32_t>(f_to_bf16_bits(acc.w * inv)) << 16);
-  *dst = make_uint2(lo, hi);
 }
 
 template <int KV>
@@ -1069,9 +1146,5 @@ cudaError_t launch_split(int kv_dtype, const DecodeParams& p, int grid, cudaStre
   return cudaErrorNotSupported;
 }
 
-cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream) {
-  mla_combine_kernel<<<p.batch * kHeads, 128, 0, stream>>>(p);
-  return cudaGetLastError();
-}
 
 }  // namespace mla

@@ -146,3 +146,34 @@ def test_mxfp4_wide_block_exponent_spread(pkg):
     ref, _ = oracle.decode(inp.q, inp.kv, inp.kv_scale, inp.kv_indptr, synth.KV_MXFP4)
     for ns in (1, 0):
         _check(_run(pkg, inp, ns), ref, f"mxfp4 spread ns {ns}")
+
+
+@pytest.mark.parametrize("kv_dtype", DTYPES)
+@pytest.mark.parametrize("lens", [[0, 0, 700, 0, 1200, 0, 0], [0, 0, 0], [5, 0], [0, 3000, 0, 2500, 0]])
+def test_empty_sequences_anywhere_in_balanced_mode(pkg, kv_dtype, lens):
+    inp = synth.make_inputs(len(lens), lens, kv_dtype, seed=61 + len(lens))
+    ref, _ = oracle.decode(inp.q, inp.kv, inp.kv_scale, inp.kv_indptr, kv_dtype)
+    # one unused trailing row keeps the cache pointer non-null when every sequence is empty
+    pad = lambda t: torch.cat([t, torch.zeros_like(t[:1]) if t.shape[0] else torch.zeros((1,) + t.shape[1:], dtype=t.dtype)])
+    kv = pad(inp.kv) if inp.kv.shape[0] else torch.zeros((1,) + tuple(inp.kv.shape[1:]), dtype=inp.kv.dtype)
+    sc = inp.kv_scale
+    if kv_dtype == synth.KV_MXFP4:
+        sc = pad(sc) if sc.shape[0] else torch.full((1, 18), 127, dtype=torch.uint8)
+    inp = synth.DecodeInputs(inp.q, None, kv, sc, inp.kv_indptr, kv_dtype, inp.lens)
+    g = inp.to("cuda")
+    out = torch.full((len(lens), 16, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+    pkg.decode(g.q, g.kv, g.kv_scale, g.kv_indptr, kv_dtype, num_splits=0, out=out)
+    torch.cuda.synchronize()
+    assert pkg.device_status(clear=True) == pkg.MLA_OK
+    _check(out, ref, f"empty-anywhere {lens}")
+
+
+@pytest.mark.parametrize("ns", [0, 5])
+def test_repeated_calls_give_identical_results(pkg, ns):
+    # The merge step re-arms its per-sequence counters at the end of every call.
+    inp = synth.make_inputs(6, [4000, 1, 2900, 0, 800, 6100], synth.KV_FP8, seed=71).to("cuda")
+    outs = [pkg.decode(inp.q, inp.kv, inp.kv_scale, inp.kv_indptr, inp.kv_dtype, num_splits=ns) for _ in range(4)]
+    torch.cuda.synchronize()
+    assert pkg.device_status(clear=True) == pkg.MLA_OK
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
