@@ -483,28 +483,30 @@ __device__ void run_dequant(const DecodeParams& p, SharedState* sh, uint8_t* rin
 #pragma unroll
         for (int j = 0; j < 9; ++j) sc[j] = __ldg(sp + j);
       }
-      for (int c = 0; c < C::kSPT && ok; ++c) {
-        const uint32_t idx = g * C::kSPT + c;
-        ok = wait_bar(smem_u32(&sh->empty[idx % C::kRing]), ((idx / C::kRing) & 1) ^ 1, abortf, p.status,
-                      p.wait_limit_ns);
-      }
       const bool has_half = half * kRawRows < w.cnt;
       const uint32_t my_r = ridx + half;
-      if (ok && has_half)
+      if (has_half)
         ok = wait_bar(smem_u32(&sh->raw_full[my_r % kRawStages]), (my_r / kRawStages) & 1, abortf, p.status,
                       p.wait_limit_ns);
       if (!ok) break;
       int emax = 127;
-      uint32_t slot = (g * C::kSPT) % C::kRing;     // ring slot of chunk 0 of this tile
       if (live) {
         emax = 0;
 #pragma unroll
         for (int j = 0; j < 9; ++j) emax = max(emax, max(static_cast<int>(sc[j] & 0xFF), static_cast<int>(sc[j] >> 8)));
-        const uint4* src = reinterpret_cast<const uint4*>(raw + (my_r % kRawStages) * kRawBytes + (di & 63) * kMxPacked);
-        // Fully unrolled over the 18 blocks so that the block scales stay in registers.
+      }
+      const uint4* src = reinterpret_cast<const uint4*>(raw + (my_r % kRawStages) * kRawBytes + (di & 63) * kMxPacked);
+      uint32_t slot = (g * C::kSPT) % C::kRing;     // ring slot of chunk 0 of this tile
+      const uint32_t phase = ((g * C::kSPT) / C::kRing) & 1;
+      // Chunk by chunk: each chunk is published (full barrier) as soon as it is written, so
+      // the QK MMAs of this tile can start on chunks whose slots were already free.
+      // Fully unrolled over the 18 blocks so that the block scales stay in registers.
 #pragma unroll
-        for (int c = 0; c < C::kSPT; ++c) {
-          uint8_t* dst = ring + slot * C::kSlotBytes + di * 128;
+      for (int c = 0; c < C::kSPT; ++c) {
+        const uint32_t ph = phase ^ static_cast<uint32_t>(((g * C::kSPT) % C::kRing + c) >= C::kRing);
+        if (!(ok = wait_bar(smem_u32(&sh->empty[slot]), ph ^ 1, abortf, p.status, p.wait_limit_ns))) break;
+        uint8_t* dst = ring + slot * C::kSlotBytes + di * 128;
+        if (live) {
 #pragma unroll
           for (int bk = 0; bk < (c < 4 ? 4 : 2); ++bk) {
             const int j = 4 * c + bk;                       // block (32 elements, 16 packed bytes)
@@ -519,21 +521,19 @@ __device__ void run_dequant(const DecodeParams& p, SharedState* sh, uint8_t* rin
             *reinterpret_cast<uint4*>(dst + ((pp ^ (di & 7)) << 4)) = make_uint4(o0, o1, o2, o3);
             *reinterpret_cast<uint4*>(dst + (((pp + 1) ^ (di & 7)) << 4)) = make_uint4(o4, o5, o6, o7);
           }
-          if (++slot == C::kRing) slot = 0;
-        }
-      } else {
+        } else {
 #pragma unroll
-        for (int c = 0; c < C::kSPT; ++c) {
-          uint4* dst = reinterpret_cast<uint4*>(ring + slot * C::kSlotBytes + di * 128);
-#pragma unroll
-          for (int q = 0; q < 8; ++q) dst[q] = make_uint4(0u, 0u, 0u, 0u);
-          if (++slot == C::kRing) slot = 0;
+          for (int q = 0; q < 8; ++q) reinterpret_cast<uint4*>(dst)[q] = make_uint4(0u, 0u, 0u, 0u);
         }
+        if (c == C::kSPT - 1) {
+          if (has_half) mbar_arrive(smem_u32(&sh->raw_empty[my_r % kRawStages]));  // raw row fully read
+          sh->etok[g & 3][di] = emax;
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(smem_u32(&sh->full[slot]));
+        if (++slot == C::kRing) slot = 0;
       }
-      if (has_half) mbar_arrive(smem_u32(&sh->raw_empty[my_r % kRawStages]));
-      sh->etok[g & 3][di] = emax;
-      fence_proxy_async_smem();
-      for (int c = 0; c < C::kSPT; ++c) mbar_arrive(smem_u32(&sh->full[(g * C::kSPT + c) % C::kRing]));
+      if (!ok) break;
       mbar_arrive(smem_u32(&sh->etok_full[g & 3]));
       ridx += (w.cnt > kRawRows) ? 2u : 1u;
       ++g;
