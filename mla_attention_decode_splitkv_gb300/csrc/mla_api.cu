@@ -30,7 +30,6 @@ Workspace g_ws[kMaxDevices];
 int g_sm_count[kMaxDevices];
 int g_cc[kMaxDevices];
 unsigned long long g_wait_limit_ns = 2000000000ull;
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 thread_local const char* t_last_cuda_error = "";
 
 // Optional timing of each call's split kernel (events recorded on the call's stream).
@@ -112,28 +111,38 @@ long long slots_needed(int batch, int num_splits, int num_sms) {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
+}  // namespace
+
+namespace mla {
+
 int encode_kv_map(CUtensorMap* map, const void* kv, int kv_dtype) {
-  if (g_encode == nullptr) {
-    cudaDriverEntryPointQueryResult q;
-    void* fn = nullptr;
-    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
-    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr) return MLA_ERR_UNSUPPORTED;
-    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  static std::mutex mu;
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    if (encode == nullptr) {
+      cudaDriverEntryPointQueryResult q;
+      void* fn = nullptr;
+      cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+      if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || fn == nullptr) return MLA_ERR_UNSUPPORTED;
+      encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
   }
-  // Rows: an upper bound; the kernel never addresses a row at or past kv_indptr[batch].
   const cuuint64_t rows = 1ull << 30;
-  const bool bf = kv_dtype == MLA_KV_BF16;
-  cuuint64_t gdim[2] = {static_cast<cuuint64_t>(mla::kDim), rows};
-  cuuint64_t gstride[1] = {static_cast<cuuint64_t>(mla::kDim) * (bf ? 2 : 1)};
-  cuuint32_t box[2] = {bf ? 64u : 128u, static_cast<cuuint32_t>(mla::kBN)};
+  const bool bf = kv_dtype == MLA_KV_BF16, mx = kv_dtype == MLA_KV_MXFP4;
+  const cuuint64_t width = mx ? kMxPacked : kDim;                       // elements per row
+  cuuint64_t gdim[2] = {width, rows};
+  cuuint64_t gstride[1] = {width * (bf ? 2 : 1)};                       // bytes per row
+  cuuint32_t box[2] = {bf ? 64u : (mx ? 64u : 128u), static_cast<cuuint32_t>(kBN)};
   cuuint32_t estride[2] = {1, 1};
-  CUresult r = g_encode(map, bf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
-                        const_cast<void*>(kv), gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = encode(map, bf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+                      const_cast<void*>(kv), gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                      mx ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_CUDA;
 }
 
-}  // namespace
+}  // namespace mla
 
 extern "C" {
 
@@ -249,10 +258,8 @@ int mla_decode(const void* q, const void* kv, const void* kv_scale, const int32_
   }
 
   mla::DecodeParams p;
-  if (kv_dtype != MLA_KV_MXFP4) {  // MXFP4 rows are fetched with plain bulk copies
-    rc = encode_kv_map(&p.tmap, kv, kv_dtype);
-    if (rc) return rc;
-  }
+  rc = mla::encode_kv_map(&p.tmap, kv, kv_dtype);
+  if (rc) return rc;
   p.q = static_cast<const uint16_t*>(q);
   p.kv = static_cast<const uint8_t*>(kv);
   p.kv_scale = kv_scale;

@@ -20,7 +20,7 @@ constexpr int kBalancedMinTokens = 256;  // fewest tokens a persistent CTA is gi
 constexpr int kStatusTimeout = 1;
 
 struct DecodeParams {
-  CUtensorMap tmap;                // KV rows as a 2D tensor (bf16 / fp8 caches)
+  CUtensorMap tmap;                // KV rows as a 2D tensor (see encode_kv_map)
   const uint16_t* q;               // bf16 bits [batch][16][576]
   const uint8_t* kv;               // raw cache base
   const void* kv_scale;            // fp8: const float*; mxfp4: const uint8_t* [T][18]
@@ -37,6 +37,14 @@ struct DecodeParams {
   unsigned long long wait_limit_ns;
 };
 
+
+// Tensor map of the cache rows for the kernel's TMA loads.  bf16: [rows x 576] bf16,
+// 64-element boxes, 128-byte swizzle; fp8: [rows x 576] bytes, 128-byte boxes, 128-byte
+// swizzle; MXFP4: the packed nibbles [rows x 288] bytes, 64-byte boxes, 64-byte swizzle.
+// All boxes are 128 rows.  The row count is an upper bound: the kernel never addresses a
+// row at or past kv_indptr[batch] (its 128-row windows end at the last row of a sequence;
+// rows before row 0 are zero-filled by the TMA).  Returns an MLA_* status.
+int encode_kv_map(CUtensorMap* map, const void* kv, int kv_dtype);
 
 // Per-kv-dtype launch geometry (host side).
 int split_threads(int kv_dtype);

@@ -16,8 +16,6 @@
 // call therefore does one-time set-up work and should happen before any stream capture.
 // All calls share the one array and it keeps the previous call's contents, so calls that
 // overlap on the GPU (different streams, no ordering between them) race on it.
-#include <cudaTypedefs.h>
-
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -42,31 +40,6 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratch
 
 std::mutex g_mu;
 void* g_addr[kMaxDevices];
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-
-// KV rows as a 2D tensor for the TMA loads (bf16: 64-element boxes, fp8: 128-byte boxes;
-// 128 rows; 128-byte swizzle).  The row count is an upper bound: the kernel never
-// addresses a row at or past kv_indptr[batch].
-int encode_map(CUtensorMap* map, const void* kv, int kv_dtype) {
-  if (g_encode == nullptr) {
-    cudaDriverEntryPointQueryResult qr;
-    void* fn = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &qr) != cudaSuccess ||
-        qr != cudaDriverEntryPointSuccess || fn == nullptr)
-      return MLA_ERR_UNSUPPORTED;
-    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-  }
-  const bool bf = kv_dtype == MLA_KV_BF16;
-  cuuint64_t gdim[2] = {static_cast<cuuint64_t>(mla::kDim), 1ull << 30};
-  cuuint64_t gstride[1] = {static_cast<cuuint64_t>(mla::kDim) * (bf ? 2 : 1)};
-  cuuint32_t box[2] = {bf ? 64u : 128u, static_cast<cuuint32_t>(mla::kBN)};
-  cuuint32_t estride[2] = {1, 1};
-  CUresult r = g_encode(map, bf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
-                        const_cast<void*>(kv), gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_CUDA;
-}
-
 }  // namespace
 
 extern "C" int mla_decode_noalloc(const void* q, const void* kv, const void* kv_scale, const int32_t* kv_indptr,
@@ -117,10 +90,8 @@ extern "C" int mla_decode_noalloc(const void* q, const void* kv, const void* kv_
   if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess) { cudaGetLastError(); return MLA_ERR_CUDA; }
 
   mla::DecodeParams p;
-  if (kv_dtype != MLA_KV_MXFP4) {
-    const int rc = encode_map(&p.tmap, kv, kv_dtype);
-    if (rc) return rc;
-  }
+  const int rc = mla::encode_kv_map(&p.tmap, kv, kv_dtype);
+  if (rc) return rc;
   p.q = static_cast<const uint16_t*>(q);
   p.kv = static_cast<const uint8_t*>(kv);
   p.kv_scale = kv_scale;

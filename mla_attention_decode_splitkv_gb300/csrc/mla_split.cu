@@ -49,7 +49,8 @@ template <>
 struct Cfg<0> {                    // bf16 cache
   static constexpr int kSlotBytes = 32768;   // two [128 x 64 bf16] SW128 boxes
   static constexpr int kRing = 6;
-  static constexpr int kSPT = 5;             // slots per tile: 4 x 128 value dims + rope
+  static constexpr int kSPT = 5;             // chunks per tile: 4 x 128 value dims + rope
+  static constexpr int kRingPT = 5;          // ring slots per tile (the rope chunk rides in the ring)
   static constexpr int kN = 16;
   static constexpr int kQBytes = 9 * 2048;   // 9 chunks of [16 rows x 128 B]
   static constexpr int kTmemCols = 128;
@@ -57,6 +58,7 @@ struct Cfg<0> {                    // bf16 cache
   static constexpr int kOCols = 16;
   static constexpr float kTau = 8.0f;
   static constexpr int kSoftWarps = 8;
+  static constexpr int kDeqWarps = 0;
   static constexpr int kThreads = 384;       // producer, QK issuer, 2 PV issuers, 8 softmax warps
 };
 template <>
@@ -64,6 +66,7 @@ struct Cfg<1> {                    // fp8 e4m3 cache
   static constexpr int kSlotBytes = 16384;   // one [128 x 128 B] SW128 box
   static constexpr int kRing = 12;
   static constexpr int kSPT = 5;
+  static constexpr int kRingPT = 5;
   static constexpr int kN = 32;              // 16 hi heads + 16 lo heads
   static constexpr int kQBytes = 5 * 4096;   // 5 chunks of [32 rows x 128 B]
   static constexpr int kTmemCols = 256;
@@ -71,29 +74,40 @@ struct Cfg<1> {                    // fp8 e4m3 cache
   static constexpr int kOCols = 32;
   static constexpr float kTau = 4.0f;        // P <= 16 -> 16 P <= 256 fits e4m3
   static constexpr int kSoftWarps = 8;
+  static constexpr int kDeqWarps = 0;
   static constexpr int kThreads = 384;       // producer, QK issuer, 2 PV issuers, 8 softmax warps
 };
 
 template <>
 struct Cfg<2> {                    // MXFP4 cache: dequantised to an e4m3 carrier in SMEM
   static constexpr int kSlotBytes = 16384;
-  static constexpr int kRing = 8;
+  static constexpr int kRing = 8;            // value chunks of exactly two tiles
   static constexpr int kSPT = 5;
+  static constexpr int kRingPT = 4;          // the rope chunk has its own [128 x 64 B] SW64 buffer
   static constexpr int kN = 32;
   static constexpr int kQBytes = 5 * 4096;
   static constexpr int kTmemCols = 256;
   static constexpr int kSCols = 32;
   static constexpr int kOCols = 32;
   static constexpr float kTau = 4.0f;
-  static constexpr int kSoftWarps = 4;
-  static constexpr int kThreads = 384;       // producer, QK, 2 PV, 4 softmax warps, 4 dequant warps
+  static constexpr int kSoftWarps = 8;
+  static constexpr int kDeqWarps = 4;
+  static constexpr int kThreads = 512;       // producer, QK, 2 PV, 8 softmax warps, 4 dequant warps
+  // Registers per thread after the role split (launch: 128 each): the issuer and dequant
+  // warpgroups give registers up to the softmax warpgroups.
+  // 32 * (4 * 72 + 8 * 168 + 4 * 104) = 65536 = 512 * 128.
+  static constexpr int kRegsIssue = 72;
+  static constexpr int kRegsSoft = 168;
+  static constexpr int kRegsDeq = 104;
+  static constexpr int kRegsNeeded = 32 * (4 * kRegsIssue + kSoftWarps * kRegsSoft + kDeqWarps * kRegsDeq);
 };
+static_assert(Cfg<2>::kRegsNeeded <= 65536, "MXFP4 register split exceeds the register file");
 
 constexpr int kPBytes = 4096;      // one P^T buffer: [128 tokens x 32 B] SW32
-constexpr int kRawRows = 64;       // MXFP4 raw staging: half a tile of packed rows
-constexpr int kRawStages = 3;
-constexpr int kRawBytes = kRawRows * kMxPacked;   // 18432
+constexpr int kSlabBytes = 8192;   // MXFP4 staging: 64 packed bytes (4 blocks) of each of 128 rows, SW64
+constexpr int kSlabs = 7;          // slab ring: a tile is 5 slabs (4 value chunks + rope)
 constexpr int kLutCount = 14;      // e2m1 -> e4m3 tables for block shifts 0..-12, then zero
+constexpr int kRopeBytes = 8192;   // MXFP4 rope carrier: [128 rows x 64 B] SW64
 
 struct SharedState {
   uint64_t full[16];
@@ -108,9 +122,11 @@ struct SharedState {
   alignas(16) float red[2][4][16];  // read as float4
   alignas(16) float lsum[4][16];
   alignas(16) float qscale[16];
-  uint64_t raw_full[kRawStages];   // MXFP4 only
-  uint64_t raw_empty[kRawStages];
+  uint64_t slab_full[kSlabs];      // MXFP4 only
+  uint64_t slab_empty[kSlabs];
   uint64_t etok_full[4];
+  uint64_t rope_full;              // MXFP4 rope carrier written / consumed by QK
+  uint64_t rope_empty;
   int etok[4][128];                // per-row max block exponent of the last 4 tiles
   uint2 lut[kLutCount];            // 8 e4m3 bytes per block shift
   long long seg_total;              // kv_indptr[batch] (balanced mode)
@@ -126,13 +142,20 @@ static_assert(offsetof(SharedState, lut) % 8 == 0, "uint2 reads of SharedState::
 
 template <int KV>
 __host__ __device__ constexpr size_t raw_bytes() {
-  return KV == 2 ? (size_t)kRawStages * kRawBytes : 0;
+  return KV == 2 ? (size_t)kSlabs * kSlabBytes : 0;
+}
+template <int KV>
+__host__ __device__ constexpr size_t rope_bytes() {
+  return KV == 2 ? (size_t)kRopeBytes : 0;
 }
 template <int KV>
 __host__ __device__ constexpr size_t smem_bytes() {
-  return 1024 + (size_t)Cfg<KV>::kRing * Cfg<KV>::kSlotBytes + Cfg<KV>::kQBytes + 2 * kPBytes + raw_bytes<KV>() +
-         sizeof(SharedState);
+  return 1024 + (size_t)Cfg<KV>::kRing * Cfg<KV>::kSlotBytes + rope_bytes<KV>() + Cfg<KV>::kQBytes + 2 * kPBytes +
+         raw_bytes<KV>() + sizeof(SharedState);
 }
+static_assert(smem_bytes<2>() <= 232448, "MXFP4 shared memory exceeds 227 KB");
+static_assert(smem_bytes<1>() <= 232448, "fp8 shared memory exceeds 227 KB");
+static_assert(smem_bytes<0>() <= 232448, "bf16 shared memory exceeds 227 KB");
 
 // ---------------------------------------------------------------- work decomposition
 struct Seg {
@@ -266,7 +289,7 @@ template <int KV>
 __device__ __forceinline__ Window tile_window(const Seg& s, int t) {
   int row_start = s.row0 + s.n_lo + t * kBN;
   int row_hi = s.row0 + s.n_hi;
-  int y0 = KV == 2 ? row_start : min(row_start, row_hi - kBN);
+  int y0 = min(row_start, row_hi - kBN);
   Window w;
   w.y0 = y0;
   w.shift = row_start - y0;
@@ -288,6 +311,14 @@ __device__ __forceinline__ float2 unpack_e4m3x2(uint32_t v) {
   __half2_raw r = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(v & 0xFFFFu), __NV_E4M3);
   __half2 h = *reinterpret_cast<__half2*>(&r);
   return __half22float2(h);
+}
+
+// One arrival per warp on an mbarrier whose count is in warps: the lanes' earlier shared
+// memory writes (and their proxy / tcgen05 fences) are ordered before lane 0's arrive by
+// the warp barrier.  Called by all 32 lanes.
+__device__ __forceinline__ void warp_arrive(uint32_t bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
 }
 
 // ---------------------------------------------------------------- q staging
@@ -352,14 +383,16 @@ __device__ void stage_q_fp8(const DecodeParams& p, int b, uint8_t* qs, float* qs
 }
 
 // ---------------------------------------------------------------- producer (1 thread)
-// MXFP4: packed rows of each tile in two 64-row halves, copied with exact-size bulk copies
-// (rows [row_start, row_start + cnt) only, so nothing outside the sequence is read).
-__device__ void run_producer_mx(const DecodeParams& p, SharedState* sh, uint8_t* raw) {
+// MXFP4: each tile is fetched as five column slabs of the packed rows (2D TMA, 64-byte
+// boxes, 64-byte swizzle): bytes [64c, 64c + 64) of the window's 128 rows for the value
+// chunks c = 0..3 and bytes [256, 288) for the rope chunk (the box's columns past 288 are
+// zero-filled).  The dequantisation frees each slab as soon as it has read it.
+__device__ void run_producer_mx(const DecodeParams& p, SharedState* sh, uint8_t* slabs) {
   volatile int* abortf = &sh->abort;
   SegIter it;
   it.init(p, blockIdx.x, sh->seg_total, sh->seg_b0);
   Seg s;
-  uint32_t ridx = 0;
+  uint32_t idx = 0, slot = 0, phase = 0;
   bool ok = true;
   while (ok && it.next(p, s)) {
     const int n = s.n_hi - s.n_lo;
@@ -367,28 +400,23 @@ __device__ void run_producer_mx(const DecodeParams& p, SharedState* sh, uint8_t*
     const int ntiles = (n + kBN - 1) / kBN;
     for (int t = 0; t < ntiles && ok; ++t) {
       const Window w = tile_window<2>(s, t);
-      for (int half = 0; half * kRawRows < w.cnt; ++half) {
-        const uint32_t st = ridx % kRawStages;
-        if (!wait_bar(smem_u32(&sh->raw_empty[st]), ((ridx / kRawStages) & 1) ^ 1, abortf, p.status,
-                      p.wait_limit_ns)) {
+      for (int c = 0; c < 5; ++c) {
+        if (!wait_bar(smem_u32(&sh->slab_empty[slot]), phase ^ 1, abortf, p.status, p.wait_limit_ns)) {
           ok = false;
           break;
         }
-        const int rows = min(kRawRows, w.cnt - half * kRawRows);
-        const uint32_t bytes = static_cast<uint32_t>(rows) * kMxPacked;
-        const uint32_t fb = smem_u32(&sh->raw_full[st]);
-        mbar_arrive_expect_tx(fb, bytes);
-        bulk_load(smem_u32(raw + st * kRawBytes), p.kv + static_cast<size_t>(w.y0 + half * kRawRows) * kMxPacked,
-                  bytes, fb);
-        ++ridx;
+        const uint32_t fb = smem_u32(&sh->slab_full[slot]);
+        mbar_arrive_expect_tx(fb, kSlabBytes);
+        tma_load_2d(smem_u32(slabs + slot * kSlabBytes), &p.tmap, 64 * c, w.y0, fb);
+        ++idx;
+        if (++slot == kSlabs) { slot = 0; phase ^= 1; }
       }
     }
   }
-  if (!ok) {
-    const uint32_t first = ridx > (uint32_t)kRawStages ? ridx - kRawStages : 0u;
-    for (uint32_t j = first; j < ridx; ++j)
-      wait_bar(smem_u32(&sh->raw_full[j % kRawStages]), (j / kRawStages) & 1, abortf, p.status, p.wait_limit_ns,
-               false);
+  if (!ok) {  // drain copies already issued so that none lands after the CTA exits
+    const uint32_t first = idx > (uint32_t)kSlabs ? idx - kSlabs : 0u;
+    for (uint32_t j = first; j < idx; ++j)
+      wait_bar(smem_u32(&sh->slab_full[j % kSlabs]), (j / kSlabs) & 1, abortf, p.status, p.wait_limit_ns, false);
   }
 }
 
@@ -444,18 +472,36 @@ __device__ void run_producer(const DecodeParams& p, SharedState* sh, uint8_t* ri
 // e2m1 * 2^(E_j - e_i) with e_i = max_j E_j, looked up per nibble in an 8-entry table for
 // the shift E_j - e_i (exact for shifts >= -8, e4m3-rounded below, zero below -12).
 // The row factor 2^(e_i - 127) is applied by the softmax to the logits and to P.
-// Layout: the same K-major SW128 chunks the TMA writes for fp8 caches.
-__device__ __forceinline__ uint32_t e2m1x4_to_e4m3x4(uint32_t nib16, uint2 lut) {
-  const uint32_t mag = __byte_perm(lut.x, lut.y, nib16 & 0x7777u);
-  const uint32_t sgn = __byte_perm(0x8000u, 0u, (nib16 >> 3) & 0x1111u);
-  return mag | sgn;
+// Layout: the same K-major SW128 chunks the TMA writes for fp8 caches (value chunks) and
+// a [128 x 64 B] SW64 buffer for the rope chunk.
+
+// Eight e2m1 nibbles (one packed word, element k in bits 4k..4k+3) -> eight e4m3 bytes:
+// magnitudes through the shift table (byte permute on the 3-bit codes), signs placed by a
+// second byte permute.
+__device__ __forceinline__ void e2m1x8_to_e4m3x8(uint32_t w, uint2 lut, uint32_t& lo, uint32_t& hi) {
+  const uint32_t m = w & 0x77777777u;
+  const uint32_t sg = (w >> 3) & 0x11111111u;
+  lo = __byte_perm(lut.x, lut.y, m) | __byte_perm(0x8000u, 0u, sg);
+  hi = __byte_perm(lut.x, lut.y, m >> 16) | __byte_perm(0x8000u, 0u, sg >> 16);
+}
+// One 32-element block (16 packed bytes) -> 32 carrier bytes (two 16-byte pieces).
+__device__ __forceinline__ void deq_block(const uint4 v, const uint2 lut, uint4& lo, uint4& hi) {
+  e2m1x8_to_e4m3x8(v.x, lut, lo.x, lo.y);
+  e2m1x8_to_e4m3x8(v.y, lut, lo.z, lo.w);
+  e2m1x8_to_e4m3x8(v.z, lut, hi.x, hi.y);
+  e2m1x8_to_e4m3x8(v.w, lut, hi.z, hi.w);
 }
 
-__device__ void run_dequant(const DecodeParams& p, SharedState* sh, uint8_t* ring, uint8_t* raw) {
+// Tile g, chunk c: the packed bytes come from slab 5g + c of the slab ring (freed right
+// after they are read); value chunk c (128 dims) goes to ring slot 4 * (g & 1) + c (the
+// ring holds the value chunks of exactly two tiles, so dequantising tile g + 2 only waits
+// for the PV MMAs of tile g); the rope chunk goes to its own SW64 buffer.  Each chunk is
+// published (full barrier) as soon as it is written.  Window rows before cached row 0
+// hold zeros (TMA fill) and get no scale: they decode to zeros.
+__device__ void run_dequant(const DecodeParams& p, SharedState* sh, uint8_t* ring, uint8_t* rope, uint8_t* slabs) {
   using C = Cfg<2>;
   volatile int* abortf = &sh->abort;
-  const int di = threadIdx.x - 256;        // carrier row of the tile
-  const int half = di >> 6;
+  const int di = threadIdx.x - 32 * (4 + C::kSoftWarps);   // carrier row of the tile
   const uint8_t* scales = static_cast<const uint8_t*>(p.kv_scale);
   if (di < kLutCount * 8) {
     const int k = di >> 3, c = di & 7;
@@ -464,78 +510,94 @@ __device__ void run_dequant(const DecodeParams& p, SharedState* sh, uint8_t* rin
         : static_cast<uint32_t>(__nv_cvt_float_to_fp8(ldexpf(mag, -k), __NV_SATFINITE, __NV_E4M3));
     reinterpret_cast<uint8_t*>(&sh->lut[0])[k * 8 + c] = static_cast<uint8_t>(code);
   }
-  bar_sync(2, 128);
+  bar_sync(2, C::kDeqWarps * 32);
+  const int ssw = (di >> 1) & 3;           // SW64 piece swizzle of this row in a slab
   SegIter it;
   it.init(p, blockIdx.x, sh->seg_total, sh->seg_b0);
   Seg s;
-  uint32_t g = 0, ridx = 0;
+  uint32_t g = 0;
   bool ok = true;
   while (ok && it.next(p, s)) {
     const int n = s.n_hi - s.n_lo;
     if (n <= 0) continue;
     const int ntiles = (n + kBN - 1) / kBN;
+    uint32_t scn[9];   // block scales of the segment's next tile, loaded one tile ahead
     for (int t = 0; t < ntiles; ++t) {
       const Window w = tile_window<2>(s, t);
-      const bool live = di < w.cnt;
-      uint32_t sc[9];
-      if (live) {
-        const uint16_t* sp = reinterpret_cast<const uint16_t*>(scales + static_cast<size_t>(w.y0 + di) * kMxScales);
-#pragma unroll
-        for (int j = 0; j < 9; ++j) sc[j] = __ldg(sp + j);
-      }
-      const bool has_half = half * kRawRows < w.cnt;
-      const uint32_t my_r = ridx + half;
-      if (has_half)
-        ok = wait_bar(smem_u32(&sh->raw_full[my_r % kRawStages]), (my_r / kRawStages) & 1, abortf, p.status,
-                      p.wait_limit_ns);
-      if (!ok) break;
+      // e_i = max_j E_j and the shift-table index min(e_i - E_j, 13) of each block, packed
+      // as 4-bit fields (block j in bits 4 (j % 8) of kpk[j / 8]).
       int emax = 127;
-      if (live) {
+      uint32_t kpk[3] = {0u, 0u, 0u};
+      if (w.y0 + di >= 0) {
+        uint32_t sc[9];
+        if (t > 0) {
+#pragma unroll
+          for (int j = 0; j < 9; ++j) sc[j] = scn[j];
+        } else {
+          const uint16_t* sp = reinterpret_cast<const uint16_t*>(scales + static_cast<size_t>(w.y0 + di) * kMxScales);
+#pragma unroll
+          for (int j = 0; j < 9; ++j) sc[j] = __ldg(sp + j);
+        }
         emax = 0;
 #pragma unroll
         for (int j = 0; j < 9; ++j) emax = max(emax, max(static_cast<int>(sc[j] & 0xFF), static_cast<int>(sc[j] >> 8)));
+#pragma unroll
+        for (int j = 0; j < 18; ++j) {
+          const int e = static_cast<int>((sc[j >> 1] >> (8 * (j & 1))) & 0xFF);
+          kpk[j >> 3] |= static_cast<uint32_t>(min(emax - e, kLutCount - 1)) << (4 * (j & 7));
+        }
       }
-      const uint4* src = reinterpret_cast<const uint4*>(raw + (my_r % kRawStages) * kRawBytes + (di & 63) * kMxPacked);
-      uint32_t slot = (g * C::kSPT) % C::kRing;     // ring slot of chunk 0 of this tile
-      const uint32_t phase = ((g * C::kSPT) / C::kRing) & 1;
-      // Chunk by chunk: each chunk is published (full barrier) as soon as it is written, so
-      // the QK MMAs of this tile can start on chunks whose slots were already free.
-      // Fully unrolled over the 18 blocks so that the block scales stay in registers.
+      if (t + 1 < ntiles) {
+        const Window wn = tile_window<2>(s, t + 1);
+        if (wn.y0 + di >= 0) {
+          const uint16_t* sp = reinterpret_cast<const uint16_t*>(scales + static_cast<size_t>(wn.y0 + di) * kMxScales);
+#pragma unroll
+          for (int j = 0; j < 9; ++j) scn[j] = __ldg(sp + j);
+        }
+      }
+      const uint32_t vslot0 = (g & 1) * C::kRingPT, vphase = (g >> 1) & 1;
+      // Fully unrolled over the 18 blocks so that the block indices are constants.
 #pragma unroll
       for (int c = 0; c < C::kSPT; ++c) {
-        const uint32_t ph = phase ^ static_cast<uint32_t>(((g * C::kSPT) % C::kRing + c) >= C::kRing);
-        if (!(ok = wait_bar(smem_u32(&sh->empty[slot]), ph ^ 1, abortf, p.status, p.wait_limit_ns))) break;
-        uint8_t* dst = ring + slot * C::kSlotBytes + di * 128;
-        if (live) {
+        const bool rc = (c == C::kSPT - 1);
+        const uint32_t si = (g * C::kSPT + c) % kSlabs, sph = ((g * C::kSPT + c) / kSlabs) & 1;
+        ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&sh->slab_full[si]), sph, abortf, p.status, p.wait_limit_ns));
+        if (!ok) break;
+        const uint8_t* srow = slabs + si * kSlabBytes + di * 64;
+        uint4 v[4];
 #pragma unroll
-          for (int bk = 0; bk < (c < 4 ? 4 : 2); ++bk) {
-            const int j = 4 * c + bk;                       // block (32 elements, 16 packed bytes)
-            const int e = static_cast<int>((sc[j >> 1] >> (8 * (j & 1))) & 0xFF);
-            const uint2 lut = sh->lut[min(emax - e, kLutCount - 1)];
-            const uint4 v = src[j];
-            const uint32_t o0 = e2m1x4_to_e4m3x4(v.x & 0xFFFFu, lut), o1 = e2m1x4_to_e4m3x4(v.x >> 16, lut);
-            const uint32_t o2 = e2m1x4_to_e4m3x4(v.y & 0xFFFFu, lut), o3 = e2m1x4_to_e4m3x4(v.y >> 16, lut);
-            const uint32_t o4 = e2m1x4_to_e4m3x4(v.z & 0xFFFFu, lut), o5 = e2m1x4_to_e4m3x4(v.z >> 16, lut);
-            const uint32_t o6 = e2m1x4_to_e4m3x4(v.w & 0xFFFFu, lut), o7 = e2m1x4_to_e4m3x4(v.w >> 16, lut);
-            const int pp = 2 * bk;
-            *reinterpret_cast<uint4*>(dst + ((pp ^ (di & 7)) << 4)) = make_uint4(o0, o1, o2, o3);
-            *reinterpret_cast<uint4*>(dst + (((pp + 1) ^ (di & 7)) << 4)) = make_uint4(o4, o5, o6, o7);
+        for (int q = 0; q < (rc ? 2 : 4); ++q) v[q] = *reinterpret_cast<const uint4*>(srow + ((q ^ ssw) << 4));
+        warp_arrive(smem_u32(&sh->slab_empty[si]));     // the slab's bytes are in registers
+        const uint32_t eb = rc ? smem_u32(&sh->rope_empty) : smem_u32(&sh->empty[vslot0 + c]);
+        ok = __all_sync(0xffffffffu, wait_bar(eb, (rc ? (g & 1) : vphase) ^ 1, abortf, p.status, p.wait_limit_ns));
+        if (!ok) break;
+        if (!rc) {
+          uint8_t* dst = ring + (vslot0 + c) * C::kSlotBytes + di * 128;     // [128 x 128 B] SW128
+#pragma unroll
+          for (int bk = 0; bk < 4; ++bk) {
+            const int j = 4 * c + bk;
+            uint4 lo, hi;
+            deq_block(v[bk], sh->lut[(kpk[j >> 3] >> (4 * (j & 7))) & 15u], lo, hi);
+            *reinterpret_cast<uint4*>(dst + (((2 * bk) ^ (di & 7)) << 4)) = lo;
+            *reinterpret_cast<uint4*>(dst + (((2 * bk + 1) ^ (di & 7)) << 4)) = hi;
           }
         } else {
+          uint8_t* dst = rope + di * 64;                                      // [128 x 64 B] SW64
 #pragma unroll
-          for (int q = 0; q < 8; ++q) reinterpret_cast<uint4*>(dst)[q] = make_uint4(0u, 0u, 0u, 0u);
-        }
-        if (c == C::kSPT - 1) {
-          if (has_half) mbar_arrive(smem_u32(&sh->raw_empty[my_r % kRawStages]));  // raw row fully read
+          for (int bk = 0; bk < 2; ++bk) {
+            const int j = 16 + bk;
+            uint4 lo, hi;
+            deq_block(v[bk], sh->lut[(kpk[j >> 3] >> (4 * (j & 7))) & 15u], lo, hi);
+            *reinterpret_cast<uint4*>(dst + (((2 * bk) ^ ssw) << 4)) = lo;
+            *reinterpret_cast<uint4*>(dst + (((2 * bk + 1) ^ ssw) << 4)) = hi;
+          }
           sh->etok[g & 3][di] = emax;
         }
         fence_proxy_async_smem();
-        mbar_arrive(smem_u32(&sh->full[slot]));
-        if (++slot == C::kRing) slot = 0;
+        warp_arrive(rc ? smem_u32(&sh->rope_full) : smem_u32(&sh->full[vslot0 + c]));
       }
       if (!ok) break;
-      mbar_arrive(smem_u32(&sh->etok_full[g & 3]));
-      ridx += (w.cnt > kRawRows) ? 2u : 1u;
+      warp_arrive(smem_u32(&sh->etok_full[g & 3]));
       ++g;
     }
   }
@@ -550,13 +612,15 @@ __device__ void run_dequant(const DecodeParams& p, SharedState* sh, uint8_t* rin
 struct Descs {
   uint64_t ring_k;   // K-major SW128 descriptor of ring slot 0 (sbo = 1024)
   uint64_t ring_mn;  // MN-major SW128 descriptor of ring slot 0 (lbo = 16 KB, sbo = 1024)
+  uint64_t rope;     // K-major SW64 descriptor of the MXFP4 rope carrier (sbo = 512)
   uint64_t q;        // K-major SW128 descriptor of the q chunks
   uint64_t p;        // MN-major SW32 descriptor of P buffer 0 (sbo = 256)
 };
-__device__ __forceinline__ Descs make_descs(uint8_t* ring, uint8_t* qs, uint8_t* ps) {
+__device__ __forceinline__ Descs make_descs(uint8_t* ring, uint8_t* rope, uint8_t* qs, uint8_t* ps) {
   Descs d;
   d.ring_k = smem_desc(smem_u32(ring), 16, 1024, kSwizzle128B);
   d.ring_mn = smem_desc(smem_u32(ring), 16384, 1024, kSwizzle128B);
+  d.rope = smem_desc(smem_u32(rope), 16, 512, kSwizzle64B);
   d.q = smem_desc(smem_u32(qs), 16, 1024, kSwizzle128B);
   d.p = smem_desc(smem_u32(ps), 0, 256, kSwizzle32B);
   return d;
@@ -587,9 +651,11 @@ __device__ void run_mma_qk(const DecodeParams& p, SharedState* sh, const Descs& 
       const uint32_t d = tmem + (g & 1) * C::kSCols;
 #pragma unroll
       for (int c = 0; c < C::kSPT; ++c) {
-        if (!(ok = wait_bar(smem_u32(&sh->full[slot]), phase, abortf, p.status, p.wait_limit_ns))) break;
+        const bool rope_sep = (C::kRingPT < C::kSPT) && c == C::kSPT - 1;   // rope outside the ring
+        const uint32_t fb = rope_sep ? smem_u32(&sh->rope_full) : smem_u32(&sh->full[slot]);
+        if (!(ok = wait_bar(fb, rope_sep ? (g & 1) : phase, abortf, p.status, p.wait_limit_ns))) break;
         tc_fence_after();
-        const uint64_t a = ds.ring_k + dofs(slot * C::kSlotBytes);
+        const uint64_t a = rope_sep ? ds.rope : ds.ring_k + dofs(slot * C::kSlotBytes);
         if constexpr (KV == 0) {
           const uint64_t b = ds.q + dofs(2 * c * 2048);
 #pragma unroll
@@ -603,8 +669,9 @@ __device__ void run_mma_qk(const DecodeParams& p, SharedState* sh, const Descs& 
 #pragma unroll
           for (int k = 0; k < (c < 4 ? 4 : 2); ++k) mma_f8(d, a + dofs(32 * k), b + dofs(32 * k), idq, (c | k) != 0);
         }
-        if (c == C::kSPT - 1) mma_commit(smem_u32(&sh->empty[slot]));  // rope slot: QK only
-        if (++slot == C::kRing) { slot = 0; phase ^= 1; }
+        if (c == C::kSPT - 1)   // the rope chunk is read by QK only
+          mma_commit(rope_sep ? smem_u32(&sh->rope_empty) : smem_u32(&sh->empty[slot]));
+        if (!rope_sep && ++slot == C::kRing) { slot = 0; phase ^= 1; }
       }
       if (ok) mma_commit(smem_u32(&sh->s_full[g & 1]));
     }
@@ -655,7 +722,7 @@ __device__ void run_mma_pv(const DecodeParams& p, SharedState* sh, const Descs& 
         mma_commit(smem_u32(&sh->empty[slot]));
       }
       mma_commit(smem_u32(&sh->pv_done[g & 1]));   // completes once both PV issuers have committed
-      slot0 += C::kSPT;
+      slot0 += C::kRingPT;
       if (slot0 >= C::kRing) slot0 -= C::kRing;
     }
     ++kseg;
@@ -807,7 +874,7 @@ __device__ void run_softmax(const DecodeParams& p, SharedState* sh, uint8_t* qs,
     if (found && ts < 128) {
       if constexpr (KV == 0) stage_q_bf16(p, sn.b, qs, ts); else stage_q_fp8(p, sn.b, qs, sh->qscale, ts);
       fence_proxy_async_smem();
-      mbar_arrive(smem_u32(&sh->q_ready));
+      warp_arrive(smem_u32(&sh->q_ready));
     }
   };
   if (has_cur) stage_next_nonempty(it, &cur);
@@ -841,7 +908,7 @@ __device__ void run_softmax(const DecodeParams& p, SharedState* sh, uint8_t* qs,
         tmem_wait_ld();
       }
       tc_fence_before();
-      mbar_arrive(smem_u32(&sh->s_free[g & 1]));
+      warp_arrive(smem_u32(&sh->s_free[g & 1]));
       const bool valid = okw && row >= w.shift && row < w.shift + w.cnt;
       // MXFP4 rows carry a power-of-two factor 2^eadd (eadd = e_row - 127): logits are
       // scaled by it, P is weighted by it (w = x + eadd) and the softmax sum is not.
@@ -973,7 +1040,7 @@ __device__ void run_softmax(const DecodeParams& p, SharedState* sh, uint8_t* qs,
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(smem_u32(&sh->p_full[g & 1]));
+      warp_arrive(smem_u32(&sh->p_full[g & 1]));
       ++g;
       if (t == ntiles - 1) {
         // All QK MMAs of this segment are complete (s_full of its last tile was observed):
@@ -1027,7 +1094,7 @@ __device__ void run_softmax(const DecodeParams& p, SharedState* sh, uint8_t* qs,
       }
     }
     tc_fence_before();
-    mbar_arrive(smem_u32(&sh->o_free));
+    warp_arrive(smem_u32(&sh->o_free));
     if (!cur.direct) finish_piece(p, sh, cur, ts, NT);
     cur = nxt;
     has_cur = has_nxt;
@@ -1041,33 +1108,36 @@ __global__ void __launch_bounds__(Cfg<KV>::kThreads, 1) mla_split_kernel(const _
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = base;
-  uint8_t* qs = ring + C::kRing * C::kSlotBytes;
+  uint8_t* rope = ring + C::kRing * C::kSlotBytes;
+  uint8_t* qs = rope + rope_bytes<KV>();
   uint8_t* ps = qs + C::kQBytes;
-  uint8_t* raw = ps + 2 * kPBytes;
-  SharedState* sh = reinterpret_cast<SharedState*>(raw + raw_bytes<KV>());
+  uint8_t* slabs = ps + 2 * kPBytes;                 // MXFP4 packed-row staging
+  SharedState* sh = reinterpret_cast<SharedState*>(slabs + raw_bytes<KV>());
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kRing; ++i) {
-      mbar_init(smem_u32(&sh->full[i]), KV == 2 ? 128 : 1);   // MXFP4: every dequant thread arrives
+      mbar_init(smem_u32(&sh->full[i]), KV == 2 ? C::kDeqWarps : 1);   // MXFP4: one arrival per dequant warp
       mbar_init(smem_u32(&sh->empty[i]), 1);
     }
     if (KV == 2) {
-      for (int i = 0; i < kRawStages; ++i) {
-        mbar_init(smem_u32(&sh->raw_full[i]), 1);
-        mbar_init(smem_u32(&sh->raw_empty[i]), kRawRows);
+      for (int i = 0; i < kSlabs; ++i) {
+        mbar_init(smem_u32(&sh->slab_full[i]), 1);
+        mbar_init(smem_u32(&sh->slab_empty[i]), C::kDeqWarps);   // one arrival per dequant warp
       }
-      for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&sh->etok_full[i]), 128);
+      for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&sh->etok_full[i]), C::kDeqWarps);
+      mbar_init(smem_u32(&sh->rope_full), C::kDeqWarps);
+      mbar_init(smem_u32(&sh->rope_empty), 1);
     }
-    constexpr uint32_t kSoftThreads = C::kSoftWarps * 32;
-    mbar_init(smem_u32(&sh->q_ready), 128);
+    // softmax-side barriers count warps (one arrival per warp)
+    mbar_init(smem_u32(&sh->q_ready), 4);       // the first four softmax warps stage q
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&sh->s_full[i]), 1);
-      mbar_init(smem_u32(&sh->s_free[i]), kSoftThreads);
-      mbar_init(smem_u32(&sh->p_full[i]), kSoftThreads);
+      mbar_init(smem_u32(&sh->s_free[i]), C::kSoftWarps);
+      mbar_init(smem_u32(&sh->p_full[i]), C::kSoftWarps);
       mbar_init(smem_u32(&sh->pv_done[i]), 2);   // one commit from each PV issuer
     }
-    mbar_init(smem_u32(&sh->o_free), kSoftThreads);
+    mbar_init(smem_u32(&sh->o_free), C::kSoftWarps);
     for (int i = 0; i < 3; ++i) mbar_init(smem_u32(&sh->mma_done[i]), 1);
     sh->abort = 0;
     fence_barrier_init();
@@ -1089,22 +1159,29 @@ __global__ void __launch_bounds__(Cfg<KV>::kThreads, 1) mla_split_kernel(const _
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sh->tmem_base;
-
-  if (warp == 0) {
-    if (lane == 0) {
-      if constexpr (KV == 2) run_producer_mx(p, sh, raw); else run_producer<KV>(p, sh, ring);
+  // Role dispatch by warpgroup: issuers (warps 0-3) | softmax | dequant (MXFP4).  Each
+  // register-budget change sits at the top of its warpgroup's branch, so that the role's
+  // code is compiled for that budget.
+  if (warp < 4) {
+    if constexpr (KV == 2) regs_dec<C::kRegsIssue>();
+    if (warp == 0) {
+      if (lane == 0) {
+        if constexpr (KV == 2) run_producer_mx(p, sh, slabs); else run_producer<KV>(p, sh, ring);
+      }
+    } else if (warp == 1) {
+      if (lane == 0) run_mma_qk<KV>(p, sh, make_descs(ring, rope, qs, ps), tmem);
+    } else {
+      if (lane == 0) run_mma_pv<KV>(p, sh, make_descs(ring, rope, qs, ps), tmem, warp - 2);
     }
     __syncwarp();
-  } else if (warp == 1) {
-    if (lane == 0) run_mma_qk<KV>(p, sh, make_descs(ring, qs, ps), tmem);
-    __syncwarp();
-  } else if (warp == 2 || warp == 3) {
-    if (lane == 0) run_mma_pv<KV>(p, sh, make_descs(ring, qs, ps), tmem, warp - 2);
-    __syncwarp();
   } else if (warp < 4 + C::kSoftWarps) {
+    if constexpr (KV == 2) regs_inc<C::kRegsSoft>();
     run_softmax<KV>(p, sh, qs, ps, tmem);
   } else {
-    if constexpr (KV == 2) run_dequant(p, sh, ring, raw);
+    if constexpr (KV == 2) {
+      regs_dec<C::kRegsDeq>();
+      run_dequant(p, sh, ring, rope, slabs);
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -1124,6 +1201,14 @@ cudaError_t launch_split_t(const DecodeParams& p, int grid, cudaStream_t stream)
     e = cudaFuncSetAttribute(mla_split_kernel<KV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem_bytes<KV>()));
     if (e != cudaSuccess) return e;
+    if constexpr (KV == 2) {
+      // The register split's increases only complete if the CTA launched with at least the
+      // registers the split hands out: refuse to launch otherwise.
+      cudaFuncAttributes fa;
+      e = cudaFuncGetAttributes(&fa, mla_split_kernel<KV>);
+      if (e != cudaSuccess) return e;
+      if (fa.numRegs * Cfg<KV>::kThreads < Cfg<KV>::kRegsNeeded) return cudaErrorInvalidConfiguration;
+    }
     configured_device = dev;
   }
   mla_split_kernel<KV><<<grid, Cfg<KV>::kThreads, smem_bytes<KV>(), stream>>>(p);

@@ -37,6 +37,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// Like mbar_try_wait, but the thread may be suspended (not polling) for up to `hint_ns`
+// while the phase is incomplete; it resumes when the phase completes or the hint expires.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
 // Non-blocking test of phase `parity`.
 __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   uint32_t ok;
@@ -62,15 +73,15 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
                                          uint64_t limit_ns, bool check_abort = true) {
   if (mbar_try_wait(bar, parity)) return true;
   uint64_t t0 = globaltimer();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 15) == 0) {
-      if (check_abort && *abort) return false;
-      if (globaltimer() - t0 > limit_ns) {
-        *abort = 1;
-        atomicOr(status, 1);
-        return false;
-      }
+  for (;;) {
+    // Sleep on the barrier instead of polling it: spinning warps would take issue slots
+    // and shared-memory bandwidth from the warps doing the work.
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+    if (check_abort && *abort) return false;
+    if (globaltimer() - t0 > limit_ns) {
+      *abort = 1;
+      atomicOr(status, 1);
+      return false;
     }
   }
 }
@@ -214,6 +225,17 @@ __device__ __forceinline__ bool bar_and(uint32_t id, uint32_t count, bool pred) 
 }
 __device__ __forceinline__ void bar_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+// Per-warpgroup register budget (all four warps of a warpgroup execute the same one).
+// An increase waits until decreases elsewhere in the CTA have freed enough registers, so
+// the budgets of all warpgroups must add up to at most the registers the CTA launched with.
+template <uint32_t N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 }  // namespace ptx
