@@ -90,15 +90,18 @@ int mla_decode(const void* q, const void* kv, const void* kv_scale, const int32_
                void* out, int batch, int num_splits, int kv_dtype, void* stream);
 
 /*
- * mla_decode_pick_splits -- host-only split-count heuristic for the uniform-split mode.
- * Chooses ns in [1, min(ceil(kv_len_hint/128), 64)] maximising
- *     wave_util(batch*ns CTAs over num_sms SMs, one CTA per SM) * L / (L + c*ns),
- * where c (in tokens) is the cost of one extra split: writing and re-reading its fp32
- * partial output (16 x 512 x 4 B x 2) plus a fixed pipeline fill, divided by the bytes of
- * one cached row of kv_dtype.  (Shape of the analytic model of submission 700955,
- * `_estimate_custom_splits`; constants derived here from the byte counts, no table.)
- * Returns ns >= 1, or MLA_ERR_INVALID_ARG for batch <= 0, kv_len_hint < 0, num_sms <= 0
- * or an unknown kv_dtype.
+ * mla_decode_pick_splits -- host-only choice of num_splits for mla_decode.
+ *     ns = min(floor(num_sms / batch), ceil(kv_len_hint / 256));  returns ns if ns >= 2,
+ *     else 0 (the balanced persistent mode).
+ * That is: one wave of uniform splits (each CTA works on one contiguous piece of one
+ * sequence, every piece at least two 128-row tiles) when the batch leaves at least two
+ * SMs per sequence; otherwise one CTA per SM over the concatenated cached rows, which
+ * also suits ragged batches.  (Measured on GB300: a CTA that crosses from one sequence
+ * into the next pays a pipeline drain, so a one-wave uniform split beats the balanced
+ * mode for short uniform batches; the pages' analytic split model, submission 700955
+ * `_estimate_custom_splits`, targets another GPU and is not used.)
+ * Returns ns = 0 or ns >= 2, or MLA_ERR_INVALID_ARG for batch <= 0, kv_len_hint < 0,
+ * num_sms <= 0 or an unknown kv_dtype.
  */
 int mla_decode_pick_splits(int batch, int kv_len_hint, int num_sms, int kv_dtype);
 

@@ -126,6 +126,11 @@ def pick_splits(batch: int, kv_len_hint: int, num_sms: int, kv_dtype: int) -> in
     return rc
 
 
+def resolve_splits(num_splits, batch: int, kv_len_hint: int, num_sms: int, kv_dtype: int) -> int:
+    """num_splits for mla_decode: the given value, or the library's choice when None."""
+    return int(num_splits) if num_splits is not None else pick_splits(batch, kv_len_hint, num_sms, kv_dtype)
+
+
 def workspace_slots(batch: int, num_splits: int, num_sms: int) -> int:
     rc = load().mla_decode_workspace_slots(int(batch), int(num_splits), int(num_sms))
     if rc < 0:

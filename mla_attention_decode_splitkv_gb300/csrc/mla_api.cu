@@ -164,26 +164,12 @@ void mla_decode_set_wait_limit_ns(unsigned long long ns) { g_wait_limit_ns = ns 
 
 int mla_decode_pick_splits(int batch, int kv_len_hint, int num_sms, int kv_dtype) {
   if (batch <= 0 || kv_len_hint < 0 || num_sms <= 0 || kv_dtype < 0 || kv_dtype > 2) return MLA_ERR_INVALID_ARG;
-  const double row_bytes = kv_dtype == MLA_KV_BF16 ? 1152.0 : (kv_dtype == MLA_KV_FP8_E4M3 ? 576.0 : 306.0);
-  // One extra split costs its fp32 partial output written and read back, plus a fixed
-  // pipeline fill (about one 128-row tile that is fetched before any math can start).
-  const double split_bytes = 2.0 * mla::kHeads * mla::kDimV * 4.0 + mla::kBN * row_bytes;
-  const double c = split_bytes / row_bytes;             // in tokens
-  const double L = kv_len_hint > 0 ? kv_len_hint : 1.0;
-  int max_ns = static_cast<int>((L + mla::kBN - 1) / mla::kBN);
-  if (max_ns > 64) max_ns = 64;
-  if (max_ns < 1) max_ns = 1;
-  int best = 1;
-  double best_score = -1.0;
-  for (int ns = 1; ns <= max_ns; ++ns) {
-    const double ctas = static_cast<double>(batch) * ns;
-    const double waves = std::ceil(ctas / num_sms);
-    const double util = ctas / (waves * num_sms);
-    const double eff = L / (L + c * (ns - 1));
-    const double score = util * eff;
-    if (score > best_score * (1.0 + 1e-9)) { best_score = score; best = ns; }
-  }
-  return best;
+  // One wave of uniform splits (every CTA one segment, no segment switches inside a CTA)
+  // when the batch leaves at least two SMs per sequence; each piece keeps >= 2 tiles.
+  const long long per_seq = num_sms / batch;
+  const long long max_pieces = (static_cast<long long>(kv_len_hint) + 2 * mla::kBN - 1) / (2 * mla::kBN);
+  const long long ns = per_seq < max_pieces ? per_seq : max_pieces;
+  return ns >= 2 ? static_cast<int>(ns) : 0;   // else: balanced persistent mode
 }
 
 int mla_decode_workspace_slots(int batch, int num_splits, int num_sms) {

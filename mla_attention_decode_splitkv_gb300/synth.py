@@ -45,17 +45,17 @@ class ConfigSpec:
     batch: int
     kv_len: Optional[int]          # None -> ragged
     kv_dtype: int
-    num_splits: int                # 0 -> library heuristic
+    num_splits: Optional[int]      # None -> mla_decode_pick_splits (0 = balanced mode)
     seed: int
 
 
 # The five workloads (index = position in the list); seeds are 1234 + index.
 CONFIGS: List[ConfigSpec] = [
     ConfigSpec("bf16_b4_l1024_ns1", 4, 1024, KV_BF16, 1, 1234),
-    ConfigSpec("fp8_b32_l1024", 32, 1024, KV_FP8, 0, 1235),
-    ConfigSpec("fp8_b64_l8192_splitkv", 64, 8192, KV_FP8, 0, 1236),
-    ConfigSpec("mxfp4_b256_l8192", 256, 8192, KV_MXFP4, 0, 1237),
-    ConfigSpec("fp8_ragged_b128_l1to8192", 128, None, KV_FP8, 0, 1238),
+    ConfigSpec("fp8_b32_l1024", 32, 1024, KV_FP8, None, 1235),
+    ConfigSpec("fp8_b64_l8192_splitkv", 64, 8192, KV_FP8, None, 1236),
+    ConfigSpec("mxfp4_b256_l8192", 256, 8192, KV_MXFP4, None, 1237),
+    ConfigSpec("fp8_ragged_b128_l1to8192", 128, None, KV_FP8, None, 1238),
 ]
 
 

@@ -115,7 +115,9 @@ def test_workload_configs_sampled_rows(pkg, cfg):
     sampled batch rows (first, last, and a few seeded ones)."""
     spec = synth.CONFIGS[cfg]
     inp = synth.make_config(cfg, device="cuda", keep_src=False)
-    out = pkg.decode(inp.q, inp.kv, inp.kv_scale, inp.kv_indptr, inp.kv_dtype, num_splits=spec.num_splits)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    ns = pkg.resolve_splits(spec.num_splits, inp.batch, inp.rows // inp.batch, sms, inp.kv_dtype)
+    out = pkg.decode(inp.q, inp.kv, inp.kv_scale, inp.kv_indptr, inp.kv_dtype, num_splits=ns)
     torch.cuda.synchronize()
     assert pkg.device_status(clear=True) == pkg.MLA_OK
     B = inp.batch

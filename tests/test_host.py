@@ -81,25 +81,18 @@ def test_valid_call_without_a_gpu_fails_cleanly(lib):
     assert rc in (-2, -3)  # MLA_ERR_UNSUPPORTED or MLA_ERR_CUDA, never a crash
 
 
-def _model(batch, L, sms, row_bytes, ns):
-    c = (2 * 16 * 512 * 4 + 128 * row_bytes) / row_bytes
-    ctas = batch * ns
-    util = ctas / (math.ceil(ctas / sms) * sms)
-    return util * L / (L + c * (ns - 1))
-
-
-@pytest.mark.parametrize("dtype,row_bytes", [(0, 1152), (1, 576), (2, 306)])
-def test_pick_splits_maximises_the_documented_model(lib, dtype, row_bytes):
-    for batch in (1, 4, 32, 64, 128, 151, 152, 153, 256, 1000):
-        for L in (1, 100, 1024, 4000, 8192, 65536):
+@pytest.mark.parametrize("dtype", [0, 1, 2])
+def test_pick_splits_follows_the_documented_rule(lib, dtype):
+    for batch in (1, 4, 32, 64, 75, 76, 77, 128, 151, 152, 153, 256, 1000):
+        for L in (0, 1, 100, 256, 257, 1024, 4000, 8192, 65536):
             for sms in (148, 152):
-                ns = lib.mla_decode_pick_splits(batch, L, sms, dtype)
-                hi = max(1, min(64, math.ceil(L / 128)))
-                assert 1 <= ns <= hi
-                best = max(_model(batch, L, sms, row_bytes, k) for k in range(1, hi + 1))
-                assert _model(batch, L, sms, row_bytes, ns) >= best * (1 - 1e-9)
-    assert lib.mla_decode_pick_splits(1000, 8192, 152, dtype) == 1 or dtype == 0
-    assert lib.mla_decode_pick_splits(1, 65536, 152, dtype) > 8
+                ns = min(sms // batch, -(-L // 256))
+                want = ns if ns >= 2 else 0
+                assert lib.mla_decode_pick_splits(batch, L, sms, dtype) == want, (batch, L, sms)
+    # the workloads: batch 64 x 8192 -> 2 splits, 32 x 1024 -> 4, 256 x 8192 -> balanced
+    assert lib.mla_decode_pick_splits(64, 8192, 152, 1) == 2
+    assert lib.mla_decode_pick_splits(32, 1024, 152, 1) == 4
+    assert lib.mla_decode_pick_splits(256, 8192, 152, 2) == 0
 
 
 def test_pick_splits_rejects_bad_arguments(lib):
