@@ -12,8 +12,9 @@
  * Method: split-KV flash decoding (submission 727205 `mla_s1` + `mla_rd`, submission
  * 700955 `mla_attn_v71` + `reduce_lse_v71`, submission 599694 `_flash_fp8_split_s1/_s2`):
  * each sequence's rows are cut into splits, each split produces an online-softmax
- * partial result (normalised output + log-sum-exp), and a combine step merges the
- * partials by log-sum-exp weights.
+ * partial result (normalised output + log-sum-exp), and the partials are merged by
+ * log-sum-exp weights.  Here the merge runs inside the same kernel: the CTA that writes
+ * a sequence's last partial merges all of them, so one call is one kernel launch.
  *
  * All pointers are DEVICE pointers unless stated otherwise.  The caller owns every
  * buffer it passes; the library never frees or retains them past the call.  Calls are
@@ -70,11 +71,11 @@ typedef enum {
  *  batch      >= 1.
  *  num_splits >= 1: cut every sequence into that many splits (BN = 128-token-rounded
  *             chunks, submission 727205 `mla_s1` split rule; splits past the end are
- *             empty; num_splits = 1 writes out directly with no combine step).
+ *             empty; num_splits = 1 writes out directly with no merge).
  *             <= 0: the library balances the total token count of the batch evenly over
  *             the GPU's SMs (one persistent CTA per SM, contiguous token ranges that may
  *             span several sequences) and merges the pieces of each sequence.
- *             At most 4096 splits.
+ *             At most 4096 splits.  mla_decode_pick_splits returns a good value.
  *  kv_dtype   an mla_kv_dtype value.
  *  stream     cudaStream_t or NULL.
  * Empty sequences (kv_indptr[b] == kv_indptr[b+1]) produce zeros.
@@ -117,7 +118,9 @@ int mla_decode_release_workspace(void);
 
 /* Reads and (if clear != 0) resets the current device's kernel status word.  Synchronises
  * the device.  Returns MLA_OK, or MLA_ERR_TIMEOUT if a pipeline wait in a kernel gave up
- * since the last clear. */
+ * since the last clear.  After a timeout the output of that call is undefined and the
+ * workspace's piece counters may be left non-zero: call mla_decode_release_workspace
+ * before the next call that splits sequences. */
 int mla_decode_device_status(int clear);
 
 /* Sets the time after which a kernel's pipeline wait gives up, sets the status word and
@@ -138,7 +141,8 @@ int mla_decode_profile_end(double* split_ms, double* call_ms, int* calls);
  * afford cudaMalloc / cudaFree, the latter synchronising the whole device).  The pages
  * have no counterpart: this is a deployment variant of mla_decode.
  *
- * Scratch (split partial results and the kernel status word) lives in a fixed array
+ * Scratch (split partial results, the per-sequence piece counters that select the
+ * merging CTA, and the kernel status word) lives in a fixed array
  * inside the library's device code instead of a cudaMalloc'd workspace: every GPU that
  * loads the library holds it (about MLA_NOALLOC_MAX_SLOTS x 32.8 KB, 16.8 MB) until the
  * process exits.  The call allocates nothing: no cudaMalloc, no cudaFree, no allocating
@@ -154,7 +158,10 @@ int mla_decode_profile_end(double* split_ms, double* call_ms, int* calls);
  *    GPU (different streams with no ordering between them) race on the array: serialise
  *    them on one stream or order them with events.
  *  - A pipeline timeout inside these kernels is recorded only in the array's status word,
- *    which mla_decode_device_status does not read.
+ *    which mla_decode_device_status does not read.  After a timeout the piece counters
+ *    may be left non-zero; the results of later calls that split sequences are then
+ *    undefined until the process restarts (mla_decode: release and re-reserve the
+ *    workspace, which re-zeroes its counters).
  * Errors as mla_decode, plus MLA_ERR_NO_MEMORY when the scratch is too small.
  */
 #define MLA_NOALLOC_MAX_SLOTS 512
