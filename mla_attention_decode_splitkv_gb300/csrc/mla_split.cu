@@ -751,8 +751,65 @@ __device__ __forceinline__ int seq_pieces(const DecodeParams& p, int b, long lon
 // weight at all is written as 0.  One warp per head: lane l owns dims 4l + 128j (j < 4);
 // weights are broadcast by shuffle and the loads of four pieces are issued together.
 // Partials of other CTAs are read through L2 (ld.global.cg).
+__device__ __forceinline__ uint2 pack_bf16x4(float4 v, float inv) {
+  return make_uint2(static_cast<uint32_t>(f_to_bf16_bits(v.x * inv)) | (static_cast<uint32_t>(f_to_bf16_bits(v.y * inv)) << 16),
+                    static_cast<uint32_t>(f_to_bf16_bits(v.z * inv)) | (static_cast<uint32_t>(f_to_bf16_bits(v.w * inv)) << 16));
+}
+__device__ __forceinline__ float warp_sum(float t) {
+  t += __shfl_xor_sync(0xffffffffu, t, 16);
+  t += __shfl_xor_sync(0xffffffffu, t, 8);
+  t += __shfl_xor_sync(0xffffffffu, t, 4);
+  t += __shfl_xor_sync(0xffffffffu, t, 2);
+  t += __shfl_xor_sync(0xffffffffu, t, 1);
+  return t;
+}
+
 __device__ void merge_pieces(const DecodeParams& p, int b, int slot0, int pieces, int ts, int nt) {
   const int warp = ts >> 5, lane = ts & 31, nw = nt >> 5;
+  if (2 * nw == kHeads && pieces <= 32) {
+    // Two heads per warp, merged together: one round of log-sum-exp loads (lane s holds
+    // piece s), then the partial outputs of two pieces x two heads in flight at a time.
+    const int ha = warp, hb = warp + nw;
+    const float la = lane < pieces ? __ldcg(p.part_lse + (slot0 + lane) * kHeads + ha) : kNegInf;
+    const float lb = lane < pieces ? __ldcg(p.part_lse + (slot0 + lane) * kHeads + hb) : kNegInf;
+    const float ma = warp_max(la), mb = warp_max(lb);
+    const float wa = (la == kNegInf) ? 0.f : ex2(la - ma);
+    const float wb = (lb == kNegInf) ? 0.f : ex2(lb - mb);
+    const float sa = warp_sum(wa), sb = warp_sum(wb);
+    float4 acca[4], accb[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      acca[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+      accb[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll 2
+    for (int k = 0; k < pieces; ++k) {
+      const float ua = __shfl_sync(0xffffffffu, wa, k), ub = __shfl_sync(0xffffffffu, wb, k);
+      const float4* srca = reinterpret_cast<const float4*>(p.part_o + (static_cast<size_t>(slot0 + k) * kHeads + ha) * kDimV);
+      const float4* srcb = reinterpret_cast<const float4*>(p.part_o + (static_cast<size_t>(slot0 + k) * kHeads + hb) * kDimV);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float4 va = __ldcg(srca + lane + 32 * j), vb = __ldcg(srcb + lane + 32 * j);
+        if (ua != 0.f) {  // a weightless piece's partial was never written: never read it into the sum
+          acca[j].x = fmaf(ua, va.x, acca[j].x); acca[j].y = fmaf(ua, va.y, acca[j].y);
+          acca[j].z = fmaf(ua, va.z, acca[j].z); acca[j].w = fmaf(ua, va.w, acca[j].w);
+        }
+        if (ub != 0.f) {
+          accb[j].x = fmaf(ub, vb.x, accb[j].x); accb[j].y = fmaf(ub, vb.y, accb[j].y);
+          accb[j].z = fmaf(ub, vb.z, accb[j].z); accb[j].w = fmaf(ub, vb.w, accb[j].w);
+        }
+      }
+    }
+    const float ia = sa > 0.f ? 1.0f / sa : 0.f, ib = sb > 0.f ? 1.0f / sb : 0.f;
+    uint2* da = reinterpret_cast<uint2*>(p.out + (static_cast<size_t>(b) * kHeads + ha) * kDimV);
+    uint2* db = reinterpret_cast<uint2*>(p.out + (static_cast<size_t>(b) * kHeads + hb) * kDimV);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      da[lane + 32 * j] = pack_bf16x4(acca[j], ia);
+      db[lane + 32 * j] = pack_bf16x4(accb[j], ib);
+    }
+    return;
+  }
   for (int h = warp; h < kHeads; h += nw) {
     float m = kNegInf;
     for (int s = lane; s < pieces; s += 32) m = fmaxf(m, __ldcg(p.part_lse + (slot0 + s) * kHeads + h));
