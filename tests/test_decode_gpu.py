@@ -179,3 +179,21 @@ def test_repeated_calls_give_identical_results(pkg, ns):
     assert pkg.device_status(clear=True) == pkg.MLA_OK
     for o in outs[1:]:
         assert torch.equal(o, outs[0])
+
+
+@pytest.mark.parametrize("kv_dtype", [synth.KV_FP8, synth.KV_BF16])
+def test_maximum_split_count(pkg, kv_dtype):
+    # 4096 splits (the limit) of a 600-token sequence: 5 pieces hold rows, 4091 are empty
+    # (log-sum-exp -inf); the merge walks all 4096 in chunks of 32.  A second sequence of
+    # one token rides along.
+    lens = [600, 1]
+    inp = synth.make_inputs(len(lens), lens, kv_dtype, seed=4096)
+    ref, _ = oracle.decode(inp.q, inp.kv, inp.kv_scale, inp.kv_indptr, kv_dtype)
+    _check(_run(pkg, inp, 4096), ref, f"4096 splits dtype {kv_dtype}")
+
+
+def test_split_count_above_the_limit_is_rejected(pkg):
+    inp = synth.make_inputs(1, [10], synth.KV_FP8, seed=1).to("cuda")
+    out = torch.empty((1, 16, 512), dtype=torch.bfloat16, device="cuda")
+    rc = pkg.mla_decode(inp.q, inp.kv, inp.kv_scale, inp.kv_indptr, out, 1, 4097, inp.kv_dtype)
+    assert rc == pkg.MLA_ERR_INVALID_ARG
