@@ -46,9 +46,7 @@ struct DecodeParams {
 // rows before row 0 are zero-filled by the TMA).  Returns an MLA_* status.
 int encode_kv_map(CUtensorMap* map, const void* kv, int kv_dtype);
 
-// Per-kv-dtype launch geometry (host side).
-int split_threads(int kv_dtype);
-size_t split_smem_bytes(int kv_dtype);
+// Launches the split kernel for kv_dtype (geometry per dtype is internal to mla_split.cu).
 cudaError_t launch_split(int kv_dtype, const DecodeParams& p, int grid, cudaStream_t stream);
 
 }  // namespace mla

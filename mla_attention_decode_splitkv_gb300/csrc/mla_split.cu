@@ -1,10 +1,12 @@
-// mla_split.cu -- split-KV flash-decode kernel (tcgen05 / TMA, sm_103a) and the
-// log-sum-exp combine kernel for single-token MLA decode.
+// mla_split.cu -- the split-KV flash-decode kernel (tcgen05 / TMA, sm_103a) for
+// single-token MLA decode, with the log-sum-exp merge of the splits fused in.
 //
 // Method (amd-mixed-mla submissions 727205 `mla_s1`/`mla_rd`, 700955 `mla_attn_v71`/
 // `reduce_lse_v71`, 599694 `_flash_fp8_split_s1`/`_s2`): every (sequence, split) pair
 // runs an online softmax over its cached rows and emits a normalised partial output plus
-// its log-sum-exp; a combine step merges the partials.  The GB300 design:
+// its log-sum-exp; the partials are merged by log-sum-exp weights.  Here the CTA that
+// writes a sequence's last partial merges them (per-sequence counters), so one call is one
+// launch.  The GB300 design:
 //
 //  * "swap-AB" tensor-core formulation, so the 16 heads sit on the MMA's N side:
 //        S^T[128 tok x 16 h]   = K_tile[128 x 576] . Q^T          (UMMA M = 128 tokens)
@@ -16,10 +18,13 @@
 //    N = 32 and the contraction error stays at the bf16 level.  The per-tensor kv_scale
 //    is folded into the logit multiplier and the final output.
 //  * bf16 caches use kind::f16 with bf16 q and P (N = 16).
-//  * KV rows stream HBM -> SMEM with 2D TMA (128B swizzle) through an mbarrier ring that
-//    one producer warp fills; one warp issues all MMAs; four warps run the online
-//    softmax (one token per thread, lanes of TMEM), the rare lazy O rescale in TMEM and
-//    the epilogue.
+//  * MXFP4 caches are dequantised in shared memory by four extra warps into an e4m3
+//    "carrier" (per-block shift tables, per-row power-of-two factor applied by the softmax)
+//    and then take the fp8 path.
+//  * KV rows stream HBM -> SMEM with 2D TMA through an mbarrier ring that one producer
+//    warp fills; one warp issues the QK^T MMAs and two warps the PV MMAs; eight warps run
+//    the online softmax (one token per thread = one TMEM lane, eight heads each), the rare
+//    lazy O rescale in TMEM, the epilogue and the merge.
 //  * Online softmax in the log2 domain with a lazy reference maximum: O is rescaled only
 //    when a tile's maximum exceeds the reference by more than kTau (log2 units).
 //
@@ -131,7 +136,7 @@ struct SharedState {
   uint2 lut[kLutCount];            // 8 e4m3 bytes per block shift
   long long seg_total;              // kv_indptr[batch] (balanced mode)
   int seg_b0;                      // first sequence of this CTA (balanced mode)
-  int merge_slot0;                 // fused combine: first slot and piece count to merge
+  int merge_slot0;                 // fused merge: first slot and piece count to merge
   int merge_pieces;
   uint32_t tmem_base;
   int abort;
@@ -1273,13 +1278,6 @@ cudaError_t launch_split_t(const DecodeParams& p, int grid, cudaStream_t stream)
 }
 
 }  // namespace
-
-int split_threads(int kv_dtype) {
-  return kv_dtype == 0 ? Cfg<0>::kThreads : (kv_dtype == 1 ? Cfg<1>::kThreads : Cfg<2>::kThreads);
-}
-size_t split_smem_bytes(int kv_dtype) {
-  return kv_dtype == 0 ? smem_bytes<0>() : (kv_dtype == 1 ? smem_bytes<1>() : smem_bytes<2>());
-}
 
 cudaError_t launch_split(int kv_dtype, const DecodeParams& p, int grid, cudaStream_t stream) {
   if (kv_dtype == 0) return launch_split_t<0>(p, grid, stream);

@@ -1,4 +1,4 @@
-// ptx.cuh -- thin inline-PTX wrappers for sm_103a: mbarrier, TMA (bulk + tensor),
+// ptx.cuh -- thin inline-PTX wrappers for sm_103a: mbarrier, TMA (tensor tiles),
 // tcgen05 (TMEM alloc, MMA, commit, ld/st), UMMA shared-memory / instruction
 // descriptors.  Every wait in this file is bounded (see wait_bar).
 #pragma once
@@ -48,16 +48,6 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
       : "memory");
   return ok != 0;
 }
-// Non-blocking test of phase `parity`.
-__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
 __device__ __forceinline__ void fence_barrier_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
@@ -92,12 +82,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int3
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar)
       : "memory");
-}
-// Non-tensor bulk copy global -> shared; dst, src 16-byte aligned, bytes multiple of 16.
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
-               : "memory");
 }
 
 // ---------------------------------------------------------------- tcgen05
