@@ -562,27 +562,33 @@ __device__ void run_dequant(const DecodeParams& p, SharedState* sh, uint8_t* rin
       }
       const uint32_t vslot0 = (g & 1) * C::kRingPT, vphase = (g >> 1) & 1;
       // Fully unrolled over the 18 blocks so that the block indices are constants.
-#pragma unroll
+      // Rolled over the five chunks (the loop body holds one value chunk and the rope chunk),
+      // so that the dequantisation code stays small next to the softmax and issue loops
+      // sharing the SM's instruction cache.  Shift-table indices of blocks 0-15 come from
+      // one 64-bit register by a run-time shift.
+      const uint64_t kv64 = static_cast<uint64_t>(kpk[0]) | (static_cast<uint64_t>(kpk[1]) << 32);
+#pragma unroll 1
       for (int c = 0; c < C::kSPT; ++c) {
         const bool rc = (c == C::kSPT - 1);
-        const uint32_t si = (g * C::kSPT + c) % kSlabs, sph = ((g * C::kSPT + c) / kSlabs) & 1;
+        const uint32_t lin = g * C::kSPT + c;
+        const uint32_t si = lin % kSlabs, sph = (lin / kSlabs) & 1;
         ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&sh->slab_full[si]), sph, abortf, p.status, p.wait_limit_ns));
         if (!ok) break;
         const uint8_t* srow = slabs + si * kSlabBytes + di * 64;
         uint4 v[4];
 #pragma unroll
-        for (int q = 0; q < (rc ? 2 : 4); ++q) v[q] = *reinterpret_cast<const uint4*>(srow + ((q ^ ssw) << 4));
+        for (int q = 0; q < 4; ++q) v[q] = *reinterpret_cast<const uint4*>(srow + ((q ^ ssw) << 4));
         warp_arrive(smem_u32(&sh->slab_empty[si]));     // the slab's bytes are in registers
         const uint32_t eb = rc ? smem_u32(&sh->rope_empty) : smem_u32(&sh->empty[vslot0 + c]);
         ok = __all_sync(0xffffffffu, wait_bar(eb, (rc ? (g & 1) : vphase) ^ 1, abortf, p.status, p.wait_limit_ns));
         if (!ok) break;
         if (!rc) {
           uint8_t* dst = ring + (vslot0 + c) * C::kSlotBytes + di * 128;     // [128 x 128 B] SW128
+          const uint32_t kc = static_cast<uint32_t>(kv64 >> (16 * c));        // blocks 4c .. 4c+3
 #pragma unroll
           for (int bk = 0; bk < 4; ++bk) {
-            const int j = 4 * c + bk;
             uint4 lo, hi;
-            deq_block(v[bk], sh->lut[(kpk[j >> 3] >> (4 * (j & 7))) & 15u], lo, hi);
+            deq_block(v[bk], sh->lut[(kc >> (4 * bk)) & 15u], lo, hi);
             *reinterpret_cast<uint4*>(dst + (((2 * bk) ^ (di & 7)) << 4)) = lo;
             *reinterpret_cast<uint4*>(dst + (((2 * bk + 1) ^ (di & 7)) << 4)) = hi;
           }
@@ -590,9 +596,8 @@ __device__ void run_dequant(const DecodeParams& p, SharedState* sh, uint8_t* rin
           uint8_t* dst = rope + di * 64;                                      // [128 x 64 B] SW64
 #pragma unroll
           for (int bk = 0; bk < 2; ++bk) {
-            const int j = 16 + bk;
             uint4 lo, hi;
-            deq_block(v[bk], sh->lut[(kpk[j >> 3] >> (4 * (j & 7))) & 15u], lo, hi);
+            deq_block(v[bk], sh->lut[(kpk[2] >> (4 * bk)) & 15u], lo, hi);
             *reinterpret_cast<uint4*>(dst + (((2 * bk) ^ ssw) << 4)) = lo;
             *reinterpret_cast<uint4*>(dst + (((2 * bk + 1) ^ ssw) << 4)) = hi;
           }
