@@ -304,6 +304,11 @@ __device__ __forceinline__ Window tile_window(const Seg& s, int t) {
 
 __device__ __forceinline__ float bf16_bits_to_f(uint32_t b) { return __uint_as_float(b << 16); }
 
+// 2^n exactly, for -149 <= n <= 127, from the exponent bits (subnormal below 2^-126).
+__device__ __forceinline__ float pow2i(int n) {
+  return n >= -126 ? __uint_as_float(static_cast<uint32_t>(n + 127) << 23) : __uint_as_float(1u << (n + 149));
+}
+
 __device__ __forceinline__ uint16_t f_to_bf16_bits(float f) {
   __nv_bfloat16 h = __float2bfloat16_rn(f);
   return *reinterpret_cast<uint16_t*>(&h);
@@ -361,9 +366,9 @@ __device__ void stage_q_fp8(const DecodeParams& p, int b, uint8_t* qs, float* qs
   amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
   int e = 0;
   frexpf(amax, &e);
-  const int a = amax > 0.f ? 8 - e : 0;
-  const float sc = ldexpf(1.0f, a);
-  if (t8 == 0) qscale[h] = ldexpf(1.0f, -a);
+  const int a = amax > 0.f ? min(max(8 - e, -126), 126) : 0;
+  const float sc = pow2i(a);
+  if (t8 == 0) qscale[h] = pow2i(-a);
 #pragma unroll
   for (int i = 0; i < 9; ++i) {
     const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
@@ -985,7 +990,7 @@ __device__ void run_softmax(const DecodeParams& p, SharedState* sh, uint8_t* qs,
         okw = okw && oke;
         const int e = sh->etok[g & 3][row];
         eadd = static_cast<float>(e - 127);
-        rowf = ldexpf(1.0f, e - 127);
+        rowf = pow2i(e - 127);
       }
       float x[H];
 #pragma unroll
@@ -1076,7 +1081,7 @@ __device__ void run_softmax(const DecodeParams& p, SharedState* sh, uint8_t* qs,
           *reinterpret_cast<uint4*>(prow + (((h0 / 8 + c) ^ sw) << 4)) =
               make_uint4(wv[4 * c], wv[4 * c + 1], wv[4 * c + 2], wv[4 * c + 3]);
       } else {
-        const float einv = ldexpf(0.0625f, -static_cast<int>(eadd));   // 2^-eadd / 16
+        const float einv = pow2i(-static_cast<int>(eadd) - 4);   // 2^-eadd / 16
         uint32_t hw[H / 4], lw[H / 4];
 #pragma unroll
         for (int j = 0; j < H / 4; ++j) {
