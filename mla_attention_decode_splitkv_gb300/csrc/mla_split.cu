@@ -485,14 +485,22 @@ __device__ void run_producer(const DecodeParams& p, SharedState* sh, uint8_t* ri
 // Layout: the same K-major SW128 chunks the TMA writes for fp8 caches (value chunks) and
 // a [128 x 64 B] SW64 buffer for the rope chunk.
 
+// Byte permute with sign replication (PTX prmt default mode: a selector nibble with its
+// top bit set yields the selected byte's top bit copied into all eight bits).
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
 // Eight e2m1 nibbles (one packed word, element k in bits 4k..4k+3) -> eight e4m3 bytes:
-// magnitudes through the shift table (byte permute on the 3-bit codes), signs placed by a
-// second byte permute.
+// magnitudes through the shift table (byte permute on the 3-bit codes); each element's
+// sign bit (bit 3 of its nibble) is the top bit of a byte of w (odd elements) or of w << 4
+// (even elements), so one sign-replicating permute per four elements yields its sign mask.
 __device__ __forceinline__ void e2m1x8_to_e4m3x8(uint32_t w, uint2 lut, uint32_t& lo, uint32_t& hi) {
   const uint32_t m = w & 0x77777777u;
-  const uint32_t sg = (w >> 3) & 0x11111111u;
-  lo = __byte_perm(lut.x, lut.y, m) | __byte_perm(0x8000u, 0u, sg);
-  hi = __byte_perm(lut.x, lut.y, m >> 16) | __byte_perm(0x8000u, 0u, sg >> 16);
+  const uint32_t w4 = w << 4;
+  lo = prmt(lut.x, lut.y, m) | (prmt(w4, w, 0xD9C8u) & 0x80808080u);
+  hi = prmt(lut.x, lut.y, m >> 16) | (prmt(w4, w, 0xFBEAu) & 0x80808080u);
 }
 // One 32-element block (16 packed bytes) -> 32 carrier bytes (two 16-byte pieces).
 __device__ __forceinline__ void deq_block(const uint4 v, const uint2 lut, uint4& lo, uint4& hi) {
