@@ -100,10 +100,10 @@ struct Cfg<2> {                    // MXFP4 cache: dequantised to an e4m3 carrie
   static constexpr int kThreads = 512;       // producer, QK, 2 PV, 8 softmax warps, 4 dequant warps
   // Registers per thread after the role split (launch: 128 each): the issuer and dequant
   // warpgroups give registers up to the softmax warpgroups.
-  // 32 * (4 * 72 + 8 * 168 + 4 * 104) = 65536 = 512 * 128.
-  static constexpr int kRegsIssue = 72;
+  // 32 * (4 * 80 + 8 * 168 + 4 * 96) = 65536 = 512 * 128.
+  static constexpr int kRegsIssue = 80;
   static constexpr int kRegsSoft = 168;
-  static constexpr int kRegsDeq = 104;
+  static constexpr int kRegsDeq = 96;
   static constexpr int kRegsNeeded = 32 * (4 * kRegsIssue + kSoftWarps * kRegsSoft + kDeqWarps * kRegsDeq);
 };
 static_assert(Cfg<2>::kRegsNeeded <= 65536, "MXFP4 register split exceeds the register file");
