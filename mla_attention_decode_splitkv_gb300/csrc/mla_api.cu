@@ -115,7 +115,7 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 namespace mla {
 
-int encode_kv_map(CUtensorMap* map, const void* kv, int kv_dtype) {
+static int encode_map(CUtensorMap* map, const void* kv, int kv_dtype, bool rope) {
   static std::mutex mu;
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   {
@@ -133,14 +133,17 @@ int encode_kv_map(CUtensorMap* map, const void* kv, int kv_dtype) {
   const cuuint64_t width = mx ? kMxPacked : kDim;                       // elements per row
   cuuint64_t gdim[2] = {width, rows};
   cuuint64_t gstride[1] = {width * (bf ? 2 : 1)};                       // bytes per row
-  cuuint32_t box[2] = {bf ? 64u : (mx ? 64u : 128u), static_cast<cuuint32_t>(kBN)};
+  cuuint32_t box[2] = {(bf || mx || rope) ? 64u : 128u, static_cast<cuuint32_t>(kBN)};
   cuuint32_t estride[2] = {1, 1};
   CUresult r = encode(map, bf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
                       const_cast<void*>(kv), gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                      mx ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      (mx || rope) ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_CUDA;
 }
+
+int encode_kv_map(CUtensorMap* map, const void* kv, int kv_dtype) { return encode_map(map, kv, kv_dtype, false); }
+int encode_rope_map(CUtensorMap* map, const void* kv) { return encode_map(map, kv, MLA_KV_FP8_E4M3, true); }
 
 }  // namespace mla
 
@@ -246,6 +249,10 @@ int mla_decode(const void* q, const void* kv, const void* kv_scale, const int32_
   mla::DecodeParams p;
   rc = mla::encode_kv_map(&p.tmap, kv, kv_dtype);
   if (rc) return rc;
+  if (kv_dtype == MLA_KV_FP8_E4M3) {
+    rc = mla::encode_rope_map(&p.tmap_rope, kv);
+    if (rc) return rc;
+  }
   p.q = static_cast<const uint16_t*>(q);
   p.kv = static_cast<const uint8_t*>(kv);
   p.kv_scale = kv_scale;

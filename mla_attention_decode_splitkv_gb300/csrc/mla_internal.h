@@ -21,6 +21,7 @@ constexpr int kStatusTimeout = 1;
 
 struct DecodeParams {
   CUtensorMap tmap;                // KV rows as a 2D tensor (see encode_kv_map)
+  CUtensorMap tmap_rope;           // fp8: the rope bytes [512, 576) of each row, 64-byte boxes
   const uint16_t* q;               // bf16 bits [batch][16][576]
   const uint8_t* kv;               // raw cache base
   const void* kv_scale;            // fp8: const float*; mxfp4: const uint8_t* [T][18]
@@ -45,6 +46,8 @@ struct DecodeParams {
 // row at or past kv_indptr[batch] (its 128-row windows end at the last row of a sequence;
 // rows before row 0 are zero-filled by the TMA).  Returns an MLA_* status.
 int encode_kv_map(CUtensorMap* map, const void* kv, int kv_dtype);
+// fp8 caches: the same rows with 64-byte boxes and 64-byte swizzle (the rope chunk).
+int encode_rope_map(CUtensorMap* map, const void* kv);
 
 // Launches the split kernel for kv_dtype (geometry per dtype is internal to mla_split.cu).
 cudaError_t launch_split(int kv_dtype, const DecodeParams& p, int grid, cudaStream_t stream);

@@ -90,8 +90,9 @@ extern "C" int mla_decode_noalloc(const void* q, const void* kv, const void* kv_
   if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess) { cudaGetLastError(); return MLA_ERR_CUDA; }
 
   mla::DecodeParams p;
-  const int rc = mla::encode_kv_map(&p.tmap, kv, kv_dtype);
+  int rc = mla::encode_kv_map(&p.tmap, kv, kv_dtype);
   if (rc) return rc;
+  if (kv_dtype == MLA_KV_FP8_E4M3 && (rc = mla::encode_rope_map(&p.tmap_rope, kv)) != 0) return rc;
   p.q = static_cast<const uint16_t*>(q);
   p.kv = static_cast<const uint8_t*>(kv);
   p.kv_scale = kv_scale;

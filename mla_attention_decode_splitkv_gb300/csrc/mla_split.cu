@@ -56,6 +56,7 @@ struct Cfg<0> {                    // bf16 cache
   static constexpr int kRing = 6;
   static constexpr int kSPT = 5;             // chunks per tile: 4 x 128 value dims + rope
   static constexpr int kRingPT = 5;          // ring slots per tile (the rope chunk rides in the ring)
+  static constexpr int kRopeSlots = 0;
   static constexpr int kN = 16;
   static constexpr int kQBytes = 9 * 2048;   // 9 chunks of [16 rows x 128 B]
   static constexpr int kTmemCols = 128;
@@ -69,11 +70,12 @@ struct Cfg<0> {                    // bf16 cache
 template <>
 struct Cfg<1> {                    // fp8 e4m3 cache
   static constexpr int kSlotBytes = 16384;   // one [128 x 128 B] SW128 box
-  static constexpr int kRing = 12;
+  static constexpr int kRing = 11;           // value chunks only (2.75 tiles)
   static constexpr int kSPT = 5;
-  static constexpr int kRingPT = 5;
+  static constexpr int kRingPT = 4;
+  static constexpr int kRopeSlots = 2;       // rope chunks: [128 x 64 B] SW64 slots of their own
   static constexpr int kN = 32;              // 16 hi heads + 16 lo heads
-  static constexpr int kQBytes = 5 * 4096;   // 5 chunks of [32 rows x 128 B]
+  static constexpr int kQBytes = 4 * 4096 + 2048;   // 4 chunks of [32 rows x 128 B] SW128 + rope [32 x 64 B] SW64
   static constexpr int kTmemCols = 256;
   static constexpr int kSCols = 32;
   static constexpr int kOCols = 32;
@@ -89,8 +91,9 @@ struct Cfg<2> {                    // MXFP4 cache: dequantised to an e4m3 carrie
   static constexpr int kRing = 8;            // value chunks of exactly two tiles
   static constexpr int kSPT = 5;
   static constexpr int kRingPT = 4;          // the rope chunk has its own [128 x 64 B] SW64 buffer
+  static constexpr int kRopeSlots = 1;
   static constexpr int kN = 32;
-  static constexpr int kQBytes = 5 * 4096;
+  static constexpr int kQBytes = 4 * 4096 + 2048;
   static constexpr int kTmemCols = 256;
   static constexpr int kSCols = 32;
   static constexpr int kOCols = 32;
@@ -112,7 +115,7 @@ constexpr int kPBytes = 4096;      // one P^T buffer: [128 tokens x 32 B] SW32
 constexpr int kSlabBytes = 8192;   // MXFP4 staging: 64 packed bytes (4 blocks) of each of 128 rows, SW64
 constexpr int kSlabs = 7;          // slab ring: a tile is 5 slabs (4 value chunks + rope)
 constexpr int kLutCount = 14;      // e2m1 -> e4m3 tables for block shifts 0..-12, then zero
-constexpr int kRopeBytes = 8192;   // MXFP4 rope carrier: [128 rows x 64 B] SW64
+constexpr int kRopeBytes = 8192;   // one rope slot: [128 rows x 64 B] SW64 (fp8 cache bytes / MXFP4 carrier)
 
 struct SharedState {
   uint64_t full[16];
@@ -130,8 +133,8 @@ struct SharedState {
   uint64_t slab_full[kSlabs];      // MXFP4 only
   uint64_t slab_empty[kSlabs];
   uint64_t etok_full[4];
-  uint64_t rope_full;              // MXFP4 rope carrier written / consumed by QK
-  uint64_t rope_empty;
+  uint64_t rope_full[2];           // rope slots (fp8: TMA, MXFP4: dequant) / consumed by QK
+  uint64_t rope_empty[2];
   int etok[4][128];                // per-row max block exponent of the last 4 tiles
   uint2 lut[kLutCount];            // 8 e4m3 bytes per block shift
   long long seg_total;              // kv_indptr[batch] (balanced mode)
@@ -151,7 +154,7 @@ __host__ __device__ constexpr size_t raw_bytes() {
 }
 template <int KV>
 __host__ __device__ constexpr size_t rope_bytes() {
-  return KV == 2 ? (size_t)kRopeBytes : 0;
+  return (size_t)Cfg<KV>::kRopeSlots * kRopeBytes;
 }
 template <int KV>
 __host__ __device__ constexpr size_t smem_bytes() {
@@ -386,9 +389,17 @@ __device__ void stage_q_fp8(const DecodeParams& p, int b, uint8_t* qs, float* qs
     }
     const int f0 = 72 * t8 + 8 * i;
     const int c = f0 >> 7, jb = f0 & 127, piece = jb >> 4, half = (jb >> 3) & 1;
-    const int off = ((piece ^ (h & 7)) << 4) + half * 8;
-    *reinterpret_cast<uint2*>(qs + c * 4096 + h * 128 + off) = make_uint2(hi[0], hi[1]);
-    *reinterpret_cast<uint2*>(qs + c * 4096 + (16 + h) * 128 + off) = make_uint2(lo[0], lo[1]);
+    if (c < 4) {   // value dims: [32 rows x 128 B] SW128 chunks
+      const int off = ((piece ^ (h & 7)) << 4) + half * 8;
+      *reinterpret_cast<uint2*>(qs + c * 4096 + h * 128 + off) = make_uint2(hi[0], hi[1]);
+      *reinterpret_cast<uint2*>(qs + c * 4096 + (16 + h) * 128 + off) = make_uint2(lo[0], lo[1]);
+    } else {       // rope dims: [32 rows x 64 B] SW64
+      const int rh = h, rl = 16 + h;
+      *reinterpret_cast<uint2*>(qs + 4 * 4096 + rh * 64 + ((piece ^ ((rh >> 1) & 3)) << 4) + half * 8) =
+          make_uint2(hi[0], hi[1]);
+      *reinterpret_cast<uint2*>(qs + 4 * 4096 + rl * 64 + ((piece ^ ((rl >> 1) & 3)) << 4) + half * 8) =
+          make_uint2(lo[0], lo[1]);
+    }
   }
 }
 
@@ -431,13 +442,13 @@ __device__ void run_producer_mx(const DecodeParams& p, SharedState* sh, uint8_t*
 }
 
 template <int KV>
-__device__ void run_producer(const DecodeParams& p, SharedState* sh, uint8_t* ring) {
+__device__ void run_producer(const DecodeParams& p, SharedState* sh, uint8_t* ring, uint8_t* rope) {
   using C = Cfg<KV>;
   volatile int* abortf = &sh->abort;
   SegIter it;
   it.init(p, blockIdx.x, sh->seg_total, sh->seg_b0);
   Seg s;
-  uint32_t idx = 0, slot = 0, phase = 0;
+  uint32_t idx = 0, slot = 0, phase = 0, ridx = 0;
   bool ok = true;
   while (ok && it.next(p, s)) {
     const int n = s.n_hi - s.n_lo;
@@ -445,7 +456,7 @@ __device__ void run_producer(const DecodeParams& p, SharedState* sh, uint8_t* ri
     const int ntiles = (n + kBN - 1) / kBN;
     for (int t = 0; t < ntiles && ok; ++t) {
       const Window w = tile_window<KV>(s, t);
-      for (int c = 0; c < C::kSPT; ++c) {
+      for (int c = 0; c < C::kRingPT; ++c) {
         if (!wait_bar(smem_u32(&sh->empty[slot]), phase ^ 1, abortf, p.status, p.wait_limit_ns)) {
           ok = false;
           break;
@@ -468,12 +479,31 @@ __device__ void run_producer(const DecodeParams& p, SharedState* sh, uint8_t* ri
         ++idx;
         if (++slot == C::kRing) { slot = 0; phase ^= 1; }
       }
+      if constexpr (C::kRopeSlots > 0) {   // fp8: the rope chunk (64 B of each row) into its own slots
+        if (!ok) break;
+        const uint32_t rs = ridx % C::kRopeSlots;
+        if (!wait_bar(smem_u32(&sh->rope_empty[rs]), ((ridx / C::kRopeSlots) & 1) ^ 1, abortf, p.status,
+                      p.wait_limit_ns)) {
+          ok = false;
+          break;
+        }
+        const uint32_t fb = smem_u32(&sh->rope_full[rs]);
+        mbar_arrive_expect_tx(fb, kRopeBytes);
+        tma_load_2d(smem_u32(rope + rs * kRopeBytes), &p.tmap_rope, kDimV, w.y0, fb);
+        ++ridx;
+      }
     }
   }
   if (!ok) {  // drain copies already issued so that none lands after the CTA exits
     const uint32_t first = idx > (uint32_t)C::kRing ? idx - C::kRing : 0u;
     for (uint32_t j = first; j < idx; ++j)
       wait_bar(smem_u32(&sh->full[j % C::kRing]), (j / C::kRing) & 1, abortf, p.status, p.wait_limit_ns, false);
+    if constexpr (C::kRopeSlots > 0) {
+      const uint32_t rfirst = ridx > (uint32_t)C::kRopeSlots ? ridx - C::kRopeSlots : 0u;
+      for (uint32_t j = rfirst; j < ridx; ++j)
+        wait_bar(smem_u32(&sh->rope_full[j % C::kRopeSlots]), (j / C::kRopeSlots) & 1, abortf, p.status,
+                 p.wait_limit_ns, false);
+    }
   }
 }
 
@@ -592,7 +622,7 @@ __device__ void run_dequant(const DecodeParams& p, SharedState* sh, uint8_t* rin
 #pragma unroll
         for (int q = 0; q < 4; ++q) v[q] = *reinterpret_cast<const uint4*>(srow + ((q ^ ssw) << 4));
         warp_arrive(smem_u32(&sh->slab_empty[si]));     // the slab's bytes are in registers
-        const uint32_t eb = rc ? smem_u32(&sh->rope_empty) : smem_u32(&sh->empty[vslot0 + c]);
+        const uint32_t eb = rc ? smem_u32(&sh->rope_empty[0]) : smem_u32(&sh->empty[vslot0 + c]);
         ok = __all_sync(0xffffffffu, wait_bar(eb, (rc ? (g & 1) : vphase) ^ 1, abortf, p.status, p.wait_limit_ns));
         if (!ok) break;
         if (!rc) {
@@ -617,7 +647,7 @@ __device__ void run_dequant(const DecodeParams& p, SharedState* sh, uint8_t* rin
           sh->etok[g & 3][di] = emax;
         }
         fence_proxy_async_smem();
-        warp_arrive(rc ? smem_u32(&sh->rope_full) : smem_u32(&sh->full[vslot0 + c]));
+        warp_arrive(rc ? smem_u32(&sh->rope_full[0]) : smem_u32(&sh->full[vslot0 + c]));
       }
       if (!ok) break;
       warp_arrive(smem_u32(&sh->etok_full[g & 3]));
@@ -637,6 +667,7 @@ struct Descs {
   uint64_t ring_mn;  // MN-major SW128 descriptor of ring slot 0 (lbo = 16 KB, sbo = 1024)
   uint64_t rope;     // K-major SW64 descriptor of the MXFP4 rope carrier (sbo = 512)
   uint64_t q;        // K-major SW128 descriptor of the q chunks
+  uint64_t q_rope;   // K-major SW64 descriptor of the q rope chunk (fp8 / MXFP4)
   uint64_t p;        // MN-major SW32 descriptor of P buffer 0 (sbo = 256)
 };
 __device__ __forceinline__ Descs make_descs(uint8_t* ring, uint8_t* rope, uint8_t* qs, uint8_t* ps) {
@@ -645,6 +676,7 @@ __device__ __forceinline__ Descs make_descs(uint8_t* ring, uint8_t* rope, uint8_
   d.ring_mn = smem_desc(smem_u32(ring), 16384, 1024, kSwizzle128B);
   d.rope = smem_desc(smem_u32(rope), 16, 512, kSwizzle64B);
   d.q = smem_desc(smem_u32(qs), 16, 1024, kSwizzle128B);
+  d.q_rope = smem_desc(smem_u32(qs + 4 * 4096), 16, 512, kSwizzle64B);
   d.p = smem_desc(smem_u32(ps), 0, 256, kSwizzle32B);
   return d;
 }
@@ -675,10 +707,12 @@ __device__ void run_mma_qk(const DecodeParams& p, SharedState* sh, const Descs& 
 #pragma unroll
       for (int c = 0; c < C::kSPT; ++c) {
         const bool rope_sep = (C::kRingPT < C::kSPT) && c == C::kSPT - 1;   // rope outside the ring
-        const uint32_t fb = rope_sep ? smem_u32(&sh->rope_full) : smem_u32(&sh->full[slot]);
-        if (!(ok = wait_bar(fb, rope_sep ? (g & 1) : phase, abortf, p.status, p.wait_limit_ns))) break;
+        const uint32_t rs = C::kRopeSlots > 0 ? g % (C::kRopeSlots > 0 ? C::kRopeSlots : 1) : 0;
+        const uint32_t rph = C::kRopeSlots > 0 ? (g / (C::kRopeSlots > 0 ? C::kRopeSlots : 1)) & 1 : 0;
+        const uint32_t fb = rope_sep ? smem_u32(&sh->rope_full[rs]) : smem_u32(&sh->full[slot]);
+        if (!(ok = wait_bar(fb, rope_sep ? rph : phase, abortf, p.status, p.wait_limit_ns))) break;
         tc_fence_after();
-        const uint64_t a = rope_sep ? ds.rope : ds.ring_k + dofs(slot * C::kSlotBytes);
+        const uint64_t a = rope_sep ? ds.rope + dofs(rs * kRopeBytes) : ds.ring_k + dofs(slot * C::kSlotBytes);
         if constexpr (KV == 0) {
           const uint64_t b = ds.q + dofs(2 * c * 2048);
 #pragma unroll
@@ -688,12 +722,12 @@ __device__ void run_mma_qk(const DecodeParams& p, SharedState* sh, const Descs& 
             for (int k = 0; k < 4; ++k) mma_f16(d, a + dofs(16384 + 32 * k), b + dofs(2048 + 32 * k), idq, 1u);
           }
         } else {
-          const uint64_t b = ds.q + dofs(c * 4096);
+          const uint64_t b = c < 4 ? ds.q + dofs(c * 4096) : ds.q_rope;
 #pragma unroll
           for (int k = 0; k < (c < 4 ? 4 : 2); ++k) mma_f8(d, a + dofs(32 * k), b + dofs(32 * k), idq, (c | k) != 0);
         }
         if (c == C::kSPT - 1)   // the rope chunk is read by QK only
-          mma_commit(rope_sep ? smem_u32(&sh->rope_empty) : smem_u32(&sh->empty[slot]));
+          mma_commit(rope_sep ? smem_u32(&sh->rope_empty[rs]) : smem_u32(&sh->empty[slot]));
         if (!rope_sep && ++slot == C::kRing) { slot = 0; phase ^= 1; }
       }
       if (ok) mma_commit(smem_u32(&sh->s_full[g & 1]));
@@ -1206,11 +1240,14 @@ __global__ void __launch_bounds__(Cfg<KV>::kThreads, 1) mla_split_kernel(const _
         mbar_init(smem_u32(&sh->slab_empty[i]), C::kDeqWarps);   // one arrival per dequant warp
       }
       for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&sh->etok_full[i]), C::kDeqWarps);
-      mbar_init(smem_u32(&sh->rope_full), C::kDeqWarps);
-      mbar_init(smem_u32(&sh->rope_empty), 1);
+
     }
     // softmax-side barriers count warps (one arrival per warp)
     mbar_init(smem_u32(&sh->q_ready), 4);       // the first four softmax warps stage q
+    for (int i = 0; i < C::kRopeSlots; ++i) {
+      mbar_init(smem_u32(&sh->rope_full[i]), KV == 2 ? C::kDeqWarps : 1);   // MXFP4: per dequant warp; fp8: TMA
+      mbar_init(smem_u32(&sh->rope_empty[i]), 1);                          // QK commit
+    }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&sh->s_full[i]), 1);
       mbar_init(smem_u32(&sh->s_free[i]), C::kSoftWarps);
@@ -1246,7 +1283,7 @@ __global__ void __launch_bounds__(Cfg<KV>::kThreads, 1) mla_split_kernel(const _
     if constexpr (KV == 2) regs_dec<C::kRegsIssue>();
     if (warp == 0) {
       if (lane == 0) {
-        if constexpr (KV == 2) run_producer_mx(p, sh, slabs); else run_producer<KV>(p, sh, ring);
+        if constexpr (KV == 2) run_producer_mx(p, sh, slabs); else run_producer<KV>(p, sh, ring, rope);
       }
     } else if (warp == 1) {
       if (lane == 0) run_mma_qk<KV>(p, sh, make_descs(ring, rope, qs, ps), tmem);
