@@ -47,9 +47,28 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--cpu-seconds", type=float, default=60.0,
+                    help="--impl reference: total oracle time over all warm-up and timed steps")
     ap.add_argument("--quick", action="store_true",
                     help="timed steps only (no clock soak, e2e or CPU baseline); for profiler runs")
     return ap.parse_args()
+
+
+def max_over_ranks(values, ws, device=None):
+    """Element-wise maximum of `values` over all ranks (a job takes as long as its slowest
+    rank).  Identity for a single process."""
+    if ws <= 1:
+        return [float(v) for v in values]
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_gbs(kv_bytes_per_rank, ws, ms):
+    """Whole-job KV GB/s: every rank decodes its own replica of the workload in `ms`."""
+    return kv_bytes_per_rank * ws / (ms * 1e-3) / 1e9
 
 
 def dist_env():
@@ -197,7 +216,7 @@ def run_reference(args, ws, rank):
     spec = synth.CONFIGS[args.config]
     inp = synth.make_config(args.config, device="cpu", keep_src=False) if spec.batch * (spec.kv_len or 4096) <= 600000 \
         else synth.make_config(args.config, device="cuda" if torch.cuda.is_available() else "cpu", keep_src=False)
-    per_step_budget = max(0.5, 60.0 / max(1, args.steps + args.warmup))
+    per_step_budget = max(0.05, args.cpu_seconds / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
         oracle_sample_rate(inp, per_step_budget / 4, max_rows=1)
     rates, secs, nrows = [], 0.0, 0
@@ -354,14 +373,11 @@ def main():
     assert torch.equal(out_h, out.cpu())
 
     # ---- aggregate over ranks (max time)
-    if ws > 1:
-        t = torch.tensor([ms, split_ms, e2e_ms], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms, split_ms, e2e_ms = t.tolist()
+    ms, split_ms, e2e_ms = max_over_ranks([ms, split_ms, e2e_ms], ws, dev)
     if rank != 0:
         return
     kv_bytes = inp.kv_bytes()
-    value = kv_bytes * ws / (ms * 1e-3) / 1e9
+    value = job_gbs(kv_bytes, ws, ms)
     peak, peak_kind = peaks()
     achieved = kv_bytes / (split_ms * 1e-3) / 1e9
     launches_per_call = 1          # the split kernel; the merge runs inside it
@@ -376,7 +392,7 @@ def main():
                      "peak_kind": f"{peak_kind} (burst copy)", "kernel": "mla_split_kernel",
                      "split_kernel_us": split_ms * 1e3, "algorithmic_bytes_per_launch": kv_bytes,
                      "traffic": ncu_traffic(spec.name)},
-        "e2e": {"value": kv_bytes * ws / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_step": e2e_ms,
+        "e2e": {"value": job_gbs(kv_bytes, ws, e2e_ms), "unit": "GB/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps * launches_per_call,
         "clocks": clocks,
