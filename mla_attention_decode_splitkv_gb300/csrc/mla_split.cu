@@ -563,7 +563,7 @@ __device__ void run_dequant(const DecodeParams& p, SharedState* sh, uint8_t* rin
   SegIter it;
   it.init(p, blockIdx.x, sh->seg_total, sh->seg_b0);
   Seg s;
-  uint32_t g = 0;
+  uint32_t g = 0, slab_i = 0, slab_ph = 0;
   bool ok = true;
   while (ok && it.next(p, s)) {
     const int n = s.n_hi - s.n_lo;
@@ -603,18 +603,25 @@ __device__ void run_dequant(const DecodeParams& p, SharedState* sh, uint8_t* rin
           for (int j = 0; j < 9; ++j) scn[j] = __ldg(sp + j);
         }
       }
-      const uint32_t vslot0 = (g & 1) * C::kRingPT, vphase = (g >> 1) & 1;
+      const uint32_t vslot0 = (g & 1) * C::kRingPT;
       // Fully unrolled over the 18 blocks so that the block indices are constants.
       // Rolled over the five chunks (the loop body holds one value chunk and the rope chunk),
       // so that the dequantisation code stays small next to the softmax and issue loops
       // sharing the SM's instruction cache.  Shift-table indices of blocks 0-15 come from
       // one 64-bit register by a run-time shift.
       const uint64_t kv64 = static_cast<uint64_t>(kpk[0]) | (static_cast<uint64_t>(kpk[1]) << 32);
+      // The value slots of tile g were last read by tile g - 2: one wait on its PV completion
+      // covers all four (QK of g - 2 completed before its softmax, hence before its PV).
+      if (g >= 2) {
+        ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&sh->pv_done[g & 1]), ((g >> 1) & 1) ^ 1, abortf, p.status,
+                                              p.wait_limit_ns));
+        if (!ok) break;
+      }
 #pragma unroll 1
       for (int c = 0; c < C::kSPT; ++c) {
         const bool rc = (c == C::kSPT - 1);
-        const uint32_t lin = g * C::kSPT + c;
-        const uint32_t si = lin % kSlabs, sph = (lin / kSlabs) & 1;
+        const uint32_t si = slab_i, sph = slab_ph;
+        if (++slab_i == kSlabs) { slab_i = 0; slab_ph ^= 1u; }
         ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&sh->slab_full[si]), sph, abortf, p.status, p.wait_limit_ns));
         if (!ok) break;
         const uint8_t* srow = slabs + si * kSlabBytes + di * 64;
@@ -622,9 +629,11 @@ __device__ void run_dequant(const DecodeParams& p, SharedState* sh, uint8_t* rin
 #pragma unroll
         for (int q = 0; q < 4; ++q) v[q] = *reinterpret_cast<const uint4*>(srow + ((q ^ ssw) << 4));
         warp_arrive(smem_u32(&sh->slab_empty[si]));     // the slab's bytes are in registers
-        const uint32_t eb = rc ? smem_u32(&sh->rope_empty[0]) : smem_u32(&sh->empty[vslot0 + c]);
-        ok = __all_sync(0xffffffffu, wait_bar(eb, (rc ? (g & 1) : vphase) ^ 1, abortf, p.status, p.wait_limit_ns));
-        if (!ok) break;
+        if (rc) {   // the rope buffer was last read by the QK MMAs of tile g - 1
+          ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&sh->rope_empty[0]), (g & 1) ^ 1, abortf, p.status,
+                                                p.wait_limit_ns));
+          if (!ok) break;
+        }
         if (!rc) {
           uint8_t* dst = ring + (vslot0 + c) * C::kSlotBytes + di * 128;     // [128 x 128 B] SW128
           const uint32_t kc = static_cast<uint32_t>(kv64 >> (16 * c));        // blocks 4c .. 4c+3
