@@ -830,8 +830,63 @@ __device__ __forceinline__ float warp_sum(float t) {
   return t;
 }
 
+// kTwoPiece compiles the two-piece path (left out of the MXFP4 kernel, whose softmax warps
+// share the instruction cache with the dequantisation loop).
+template <bool kTwoPiece>
 __device__ void merge_pieces(const DecodeParams& p, int b, int slot0, int pieces, int ts, int nt) {
   const int warp = ts >> 5, lane = ts & 31, nw = nt >> 5;
+  if (kTwoPiece && 2 * nw == kHeads && pieces == 2) {
+    // Two pieces, two heads per warp: the partial outputs are loaded together with the
+    // log-sum-exps (one round trip to L2; a weightless piece's unwritten partial is loaded
+    // but never used).
+    const int ha = warp, hb = warp + nw;
+    float4 va[2][4], vb[2][4];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const float4* srca = reinterpret_cast<const float4*>(p.part_o + (static_cast<size_t>(slot0 + k) * kHeads + ha) * kDimV);
+      const float4* srcb = reinterpret_cast<const float4*>(p.part_o + (static_cast<size_t>(slot0 + k) * kHeads + hb) * kDimV);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        va[k][j] = __ldcg(srca + lane + 32 * j);
+        vb[k][j] = __ldcg(srcb + lane + 32 * j);
+      }
+    }
+    float la[2], lb[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      la[k] = __ldcg(p.part_lse + (slot0 + k) * kHeads + ha);
+      lb[k] = __ldcg(p.part_lse + (slot0 + k) * kHeads + hb);
+    }
+    const float ma = fmaxf(la[0], la[1]), mb = fmaxf(lb[0], lb[1]);
+    float ua[2], ub[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      ua[k] = la[k] == kNegInf ? 0.f : ex2(la[k] - ma);
+      ub[k] = lb[k] == kNegInf ? 0.f : ex2(lb[k] - mb);
+    }
+    const float sa = ua[0] + ua[1], sb = ub[0] + ub[1];
+    const float ia = sa > 0.f ? 1.0f / sa : 0.f, ib = sb > 0.f ? 1.0f / sb : 0.f;
+    uint2* da = reinterpret_cast<uint2*>(p.out + (static_cast<size_t>(b) * kHeads + ha) * kDimV);
+    uint2* db = reinterpret_cast<uint2*>(p.out + (static_cast<size_t>(b) * kHeads + hb) * kDimV);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float4 oa = make_float4(0.f, 0.f, 0.f, 0.f), ob = oa;
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        if (ua[k] != 0.f) {
+          oa.x = fmaf(ua[k], va[k][j].x, oa.x); oa.y = fmaf(ua[k], va[k][j].y, oa.y);
+          oa.z = fmaf(ua[k], va[k][j].z, oa.z); oa.w = fmaf(ua[k], va[k][j].w, oa.w);
+        }
+        if (ub[k] != 0.f) {
+          ob.x = fmaf(ub[k], vb[k][j].x, ob.x); ob.y = fmaf(ub[k], vb[k][j].y, ob.y);
+          ob.z = fmaf(ub[k], vb[k][j].z, ob.z); ob.w = fmaf(ub[k], vb[k][j].w, ob.w);
+        }
+      }
+      da[lane + 32 * j] = pack_bf16x4(oa, ia);
+      db[lane + 32 * j] = pack_bf16x4(ob, ib);
+    }
+    return;
+  }
   if (2 * nw == kHeads && pieces <= 32) {
     // Two heads per warp, merged together: one round of log-sum-exp loads (lane s holds
     // piece s), then the partial outputs of two pieces x two heads in flight at a time.
@@ -930,6 +985,7 @@ __device__ void merge_pieces(const DecodeParams& p, int b, int slot0, int pieces
 // After this CTA wrote its piece of sequence s.b: count the piece; the CTA whose piece
 // completes the count merges all pieces and re-arms the counter for the next call.
 // Reached by all `nt` softmax threads.
+template <int KV>
 __device__ void finish_piece(const DecodeParams& p, SharedState* sh, const Seg& s, int ts, int nt) {
   __threadfence();
   bar_sync(1, nt);
@@ -946,7 +1002,7 @@ __device__ void finish_piece(const DecodeParams& p, SharedState* sh, const Seg& 
   const int pieces = sh->merge_pieces;
   if (pieces > 0) {
     __threadfence();
-    merge_pieces(p, s.b, sh->merge_slot0, pieces, ts, nt);
+    merge_pieces<KV != 2>(p, s.b, sh->merge_slot0, pieces, ts, nt);
   }
 }
 
@@ -1008,7 +1064,7 @@ __device__ void run_softmax(const DecodeParams& p, SharedState* sh, uint8_t* qs,
     const int n = cur.n_hi - cur.n_lo;
     if (n <= 0) {
       write_empty_result<KV>(p, cur, ts);
-      if (!cur.direct) finish_piece(p, sh, cur, ts, NT);
+      if (!cur.direct) finish_piece<KV>(p, sh, cur, ts, NT);
       has_cur = it.next(p, cur);
       continue;
     }
@@ -1218,7 +1274,7 @@ __device__ void run_softmax(const DecodeParams& p, SharedState* sh, uint8_t* qs,
     }
     tc_fence_before();
     warp_arrive(smem_u32(&sh->o_free));
-    if (!cur.direct) finish_piece(p, sh, cur, ts, NT);
+    if (!cur.direct) finish_piece<KV>(p, sh, cur, ts, NT);
     cur = nxt;
     has_cur = has_nxt;
   }
