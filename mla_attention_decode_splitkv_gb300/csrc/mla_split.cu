@@ -994,16 +994,16 @@ __device__ void finish_piece(const DecodeParams& p, SharedState* sh, const Seg& 
     const int pieces = seq_pieces(p, s.b, sh->seg_total, &slot0);
     const int old = atomicAdd(p.seq_count + s.b, 1);
     const bool last = (old == pieces - 1);
-    if (last) p.seq_count[s.b] = 0;
+    if (last) {
+      p.seq_count[s.b] = 0;
+      fence_acq_rel_gpu();   // the other pieces' partials (released by their fence + count)
+    }
     sh->merge_slot0 = slot0;
     sh->merge_pieces = last ? pieces : 0;
   }
   bar_sync(1, nt);
   const int pieces = sh->merge_pieces;
-  if (pieces > 0) {
-    __threadfence();
-    merge_pieces<KV != 2>(p, s.b, sh->merge_slot0, pieces, ts, nt);
-  }
+  if (pieces > 0) merge_pieces<KV != 2>(p, s.b, sh->merge_slot0, pieces, ts, nt);
 }
 
 template <int KV>
