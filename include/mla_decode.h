@@ -124,8 +124,15 @@ int mla_decode_release_workspace(void);
 int mla_decode_device_status(int clear);
 
 /* Sets the time after which a kernel's pipeline wait gives up, sets the status word and
- * lets the kernel return (default 2e9 ns).  For tests of the failure path. */
+ * lets the kernel return (default 2e9 ns).  For tests of the failure path.  The waits a CTA
+ * makes for its own copies and MMAs in flight before it exits keep a fixed 2 s limit. */
 void mla_decode_set_wait_limit_ns(unsigned long long ns);
+
+/* Test hook (failure path without a fault): while on != 0, every mla_decode call's QK
+ * issuer first waits on a barrier that nothing completes, so that the wait runs past the
+ * limit, the device status reads MLA_ERR_TIMEOUT and the kernel returns.  Never set outside
+ * tests; mla_decode_noalloc ignores it. */
+void mla_decode_set_test_stall(int on);
 
 /* Timing hooks.  Between begin and end, every mla_decode call records CUDA events on its
  * stream around its split kernel and around the whole call.  end() waits for those events

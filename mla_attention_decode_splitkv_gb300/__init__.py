@@ -7,6 +7,6 @@ in-tree by ``build.build()``); ``decode`` / ``mla_decode`` here only marshal arg
 from ._lib import (MLA_ERR_CUDA, MLA_ERR_INVALID_ARG, MLA_ERR_NO_MEMORY, MLA_ERR_TIMEOUT,  # noqa: F401
                    MLA_ERR_UNSUPPORTED, MLA_OK, MLAError, decode, device_status, load, mla_decode,
                    pick_splits, profile_begin, profile_end, release_workspace, reserve_workspace, resolve_splits,
-                   set_wait_limit_ns, workspace_slots)
+                   set_test_stall, set_wait_limit_ns, workspace_slots)
 
 KV_BF16, KV_FP8, KV_MXFP4 = 0, 1, 2

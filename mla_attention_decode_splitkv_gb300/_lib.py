@@ -27,6 +27,7 @@ EXPORTED = (
     "mla_decode_release_workspace",
     "mla_decode_device_status",
     "mla_decode_set_wait_limit_ns",
+    "mla_decode_set_test_stall",
     "mla_decode_profile_begin",
     "mla_decode_profile_end",
     "mla_decode_noalloc",
@@ -72,6 +73,8 @@ def load(path: str = LIB_PATH):
         lib.mla_decode_device_status.argtypes = [c_int]
         lib.mla_decode_set_wait_limit_ns.restype = None
         lib.mla_decode_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
+        lib.mla_decode_set_test_stall.restype = None
+        lib.mla_decode_set_test_stall.argtypes = [c_int]
         lib.mla_decode_profile_begin.restype = c_int
         lib.mla_decode_profile_begin.argtypes = []
         lib.mla_decode_profile_end.restype = c_int
@@ -156,6 +159,11 @@ def device_status(clear: bool = True) -> int:
 
 def set_wait_limit_ns(ns: int) -> None:
     load().mla_decode_set_wait_limit_ns(int(ns))
+
+
+def set_test_stall(on: bool) -> None:
+    """Test hook: make every mla_decode call's pipeline wait run past its limit."""
+    load().mla_decode_set_test_stall(1 if on else 0)
 
 
 def profile_begin() -> None:

@@ -30,6 +30,7 @@ Workspace g_ws[kMaxDevices];
 int g_sm_count[kMaxDevices];
 int g_cc[kMaxDevices];
 unsigned long long g_wait_limit_ns = 2000000000ull;
+int g_test_stall = 0;
 thread_local const char* t_last_cuda_error = "";
 
 // Optional timing of each call's split kernel (events recorded on the call's stream).
@@ -165,6 +166,8 @@ const char* mla_last_cuda_error(void) { return t_last_cuda_error; }
 
 void mla_decode_set_wait_limit_ns(unsigned long long ns) { g_wait_limit_ns = ns ? ns : 1ull; }
 
+void mla_decode_set_test_stall(int on) { g_test_stall = on ? 1 : 0; }
+
 int mla_decode_pick_splits(int batch, int kv_len_hint, int num_sms, int kv_dtype) {
   if (batch <= 0 || kv_len_hint < 0 || num_sms <= 0 || kv_dtype < 0 || kv_dtype > 2) return MLA_ERR_INVALID_ARG;
   // One wave of uniform splits (every CTA one segment, no segment switches inside a CTA)
@@ -267,6 +270,7 @@ int mla_decode(const void* q, const void* kv, const void* kv_scale, const int32_
   p.num_ctas = static_cast<int>(grid_ll);
   p.logit_scale_log2 = static_cast<float>((1.0 / std::sqrt(static_cast<double>(mla::kDim))) * 1.4426950408889634);
   p.wait_limit_ns = g_wait_limit_ns;
+  p.test_stall = g_test_stall;
 
   ProfRecord rec{nullptr, nullptr, nullptr};
   bool prof = false;

@@ -36,6 +36,7 @@ struct DecodeParams {
   int num_ctas;                    // grid size (balanced mode: persistent CTAs)
   float logit_scale_log2;          // sm_scale * log2(e)
   unsigned long long wait_limit_ns;
+  int test_stall;                  // test hook: the QK issuer waits on a barrier that never completes
 };
 
 

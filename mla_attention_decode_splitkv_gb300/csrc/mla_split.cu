@@ -46,6 +46,10 @@ using namespace ptx;
 namespace {
 
 constexpr float kNegInf = -__builtin_huge_valf();
+// Waits for a CTA's own copies and MMAs in flight (before it exits, also after a give-up)
+// keep this limit whatever the pipeline wait limit is, so that no CTA ends with an async
+// write to its shared memory or an MMA still reading it.
+constexpr unsigned long long kDrainLimitNs = 2000000000ull;
 
 // ---------------------------------------------------------------- per-dtype geometry
 template <int KV>
@@ -127,6 +131,7 @@ struct SharedState {
   uint64_t pv_done[2];
   uint64_t o_free;
   uint64_t mma_done[3];
+  uint64_t never;                  // test hook: a barrier nothing arrives on
   alignas(16) float red[2][4][16];  // read as float4
   alignas(16) float lsum[4][16];
   alignas(16) float qscale[16];
@@ -437,7 +442,7 @@ __device__ void run_producer_mx(const DecodeParams& p, SharedState* sh, uint8_t*
   if (!ok) {  // drain copies already issued so that none lands after the CTA exits
     const uint32_t first = idx > (uint32_t)kSlabs ? idx - kSlabs : 0u;
     for (uint32_t j = first; j < idx; ++j)
-      wait_bar(smem_u32(&sh->slab_full[j % kSlabs]), (j / kSlabs) & 1, abortf, p.status, p.wait_limit_ns, false);
+      wait_bar(smem_u32(&sh->slab_full[j % kSlabs]), (j / kSlabs) & 1, abortf, p.status, kDrainLimitNs, false);
   }
 }
 
@@ -497,12 +502,12 @@ __device__ void run_producer(const DecodeParams& p, SharedState* sh, uint8_t* ri
   if (!ok) {  // drain copies already issued so that none lands after the CTA exits
     const uint32_t first = idx > (uint32_t)C::kRing ? idx - C::kRing : 0u;
     for (uint32_t j = first; j < idx; ++j)
-      wait_bar(smem_u32(&sh->full[j % C::kRing]), (j / C::kRing) & 1, abortf, p.status, p.wait_limit_ns, false);
+      wait_bar(smem_u32(&sh->full[j % C::kRing]), (j / C::kRing) & 1, abortf, p.status, kDrainLimitNs, false);
     if constexpr (C::kRopeSlots > 0) {
       const uint32_t rfirst = ridx > (uint32_t)C::kRopeSlots ? ridx - C::kRopeSlots : 0u;
       for (uint32_t j = rfirst; j < ridx; ++j)
         wait_bar(smem_u32(&sh->rope_full[j % C::kRopeSlots]), (j / C::kRopeSlots) & 1, abortf, p.status,
-                 p.wait_limit_ns, false);
+                 kDrainLimitNs, false);
     }
   }
 }
@@ -702,7 +707,8 @@ __device__ void run_mma_qk(const DecodeParams& p, SharedState* sh, const Descs& 
   Seg s;
   uint32_t g = 0, slot = 0, phase = 0;
   int kseg = 0;
-  bool ok = true;
+  // Test hook: a wait that can only end by running past the limit (status word, abort).
+  bool ok = !p.test_stall || wait_bar(smem_u32(&sh->never), 0, abortf, p.status, p.wait_limit_ns);
   while (ok && it.next(p, s)) {
     const int n = s.n_hi - s.n_lo;
     if (n <= 0) continue;
@@ -744,7 +750,7 @@ __device__ void run_mma_qk(const DecodeParams& p, SharedState* sh, const Descs& 
     ++kseg;
   }
   mma_commit(smem_u32(&sh->mma_done[0]));
-  wait_bar(smem_u32(&sh->mma_done[0]), 0, abortf, p.status, p.wait_limit_ns, false);
+  wait_bar(smem_u32(&sh->mma_done[0]), 0, abortf, p.status, kDrainLimitNs, false);
 }
 
 // PV issuer `part` (0 or 1) issues the two 128-dim blocks 2*part, 2*part+1 of every tile.
@@ -794,7 +800,7 @@ __device__ void run_mma_pv(const DecodeParams& p, SharedState* sh, const Descs& 
     ++kseg;
   }
   mma_commit(smem_u32(&sh->mma_done[1 + part]));
-  wait_bar(smem_u32(&sh->mma_done[1 + part]), 0, abortf, p.status, p.wait_limit_ns, false);
+  wait_bar(smem_u32(&sh->mma_done[1 + part]), 0, abortf, p.status, kDrainLimitNs, false);
 }
 
 // ---------------------------------------------------------------- softmax / epilogue (128 threads)
@@ -1321,6 +1327,7 @@ __global__ void __launch_bounds__(Cfg<KV>::kThreads, 1) mla_split_kernel(const _
     }
     mbar_init(smem_u32(&sh->o_free), C::kSoftWarps);
     for (int i = 0; i < 3; ++i) mbar_init(smem_u32(&sh->mma_done[i]), 1);
+    mbar_init(smem_u32(&sh->never), 1);
     sh->abort = 0;
     fence_barrier_init();
     fence_proxy_async_smem();

@@ -197,3 +197,28 @@ def test_split_count_above_the_limit_is_rejected(pkg):
     out = torch.empty((1, 16, 512), dtype=torch.bfloat16, device="cuda")
     rc = pkg.mla_decode(inp.q, inp.kv, inp.kv_scale, inp.kv_indptr, out, 1, 4097, inp.kv_dtype)
     assert rc == pkg.MLA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kv_dtype", DTYPES)
+def test_wait_timeout_is_reported_and_the_next_call_recovers(pkg, kv_dtype):
+    """Failure path without a GPU fault: the QK issuer waits on a barrier that nothing
+    completes, the wait runs past a short limit, the kernel sets the status word and
+    returns (its copies and MMAs in flight drained), and the host reads MLA_ERR_TIMEOUT.
+    After the workspace is released the next call is correct again."""
+    inp = synth.make_inputs(3, [1, 300, 1000], kv_dtype, seed=71)
+    g = inp.to("cuda")
+    before = _run(pkg, inp, 2)
+    pkg.reserve_workspace(pkg.workspace_slots(len(inp.lens), 2, torch.cuda.get_device_properties(0).multi_processor_count))
+    pkg.set_wait_limit_ns(200_000)
+    pkg.set_test_stall(True)
+    try:
+        pkg.decode(g.q, g.kv, g.kv_scale, g.kv_indptr, inp.kv_dtype, num_splits=2)
+        torch.cuda.synchronize()
+        status = pkg.device_status(clear=True)
+    finally:
+        pkg.set_test_stall(False)
+        pkg.set_wait_limit_ns(2_000_000_000)
+    assert status == pkg.MLA_ERR_TIMEOUT
+    pkg.release_workspace()                     # the piece counters may be left mid-count
+    after = _run(pkg, inp, 2)
+    assert torch.equal(before, after)
