@@ -1256,7 +1256,7 @@ __device__ void run_softmax(const DecodeParams& p, SharedState* sh, uint8_t* qs,
 #pragma unroll
     for (int h = 0; h < H; ++h) {
       const float l = sh->lsum[0][h0 + h] + sh->lsum[1][h0 + h] + sh->lsum[2][h0 + h] + sh->lsum[3][h0 + h];
-      inv[h] = (KV == 0 ? 1.0f : kv_scale * 0.0625f) / l;
+      inv[h] = __fdividef(KV == 0 ? 1.0f : kv_scale * 0.0625f, l);
       if (!cur.direct && quarter == 0 && lane == 0) p.part_lse[cur.slot * kHeads + h0 + h] = mref[h] + lg2(l);
     }
 #pragma unroll 1
