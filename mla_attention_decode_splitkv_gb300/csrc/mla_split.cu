@@ -633,7 +633,6 @@ __device__ void run_dequant(const DecodeParams& p, SharedState* sh, uint8_t* rin
         uint4 v[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) v[q] = *reinterpret_cast<const uint4*>(srow + ((q ^ ssw) << 4));
-        warp_arrive(smem_u32(&sh->slab_empty[si]));     // the slab's bytes are in registers
         if (rc) {   // the rope buffer was last read by the QK MMAs of tile g - 1
           ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&sh->rope_empty[0]), (g & 1) ^ 1, abortf, p.status,
                                                 p.wait_limit_ns));
@@ -660,6 +659,12 @@ __device__ void run_dequant(const DecodeParams& p, SharedState* sh, uint8_t* rin
           }
           sh->etok[g & 3][di] = emax;
         }
+        // The slab is released only after this chunk's carrier stores.  Released right after
+        // its loads (the loads being complete, or not), about one call in fifteen of the
+        // balanced mode with one- or two-tile segments had a few MX blocks of one value chunk
+        // wrong; with the release here none in 1,500 calls.  A proxy fence after the PV wait,
+        // per-thread publish arrivals and a data-dependent early release did not remove it.
+        warp_arrive(smem_u32(&sh->slab_empty[si]));
         fence_proxy_async_smem();
         warp_arrive(rc ? smem_u32(&sh->rope_full[0]) : smem_u32(&sh->full[vslot0 + c]));
       }

@@ -222,3 +222,19 @@ def test_wait_timeout_is_reported_and_the_next_call_recovers(pkg, kv_dtype):
     pkg.release_workspace()                     # the piece counters may be left mid-count
     after = _run(pkg, inp, 2)
     assert torch.equal(before, after)
+
+
+@pytest.mark.parametrize("lens", [[1, 129, 1000, 2048], [64, 65, 127, 383]])
+def test_mxfp4_short_segments_repeated(pkg, lens):
+    """Repeated balanced-mode MXFP4 calls whose CTAs switch sequences every one or two tiles.
+    Guards the release of a packed-row slab: it must not be handed back to the TMA before
+    the dequantising warps' shared loads of it have completed (when it was, about one call
+    in fifteen had a few MX blocks of one value chunk decoded from the next slab fill)."""
+    inp = synth.make_inputs(len(lens), lens, synth.KV_MXFP4, seed=100 + sum(lens))
+    ref, _ = oracle.decode(inp.q, inp.kv, inp.kv_scale, inp.kv_indptr, synth.KV_MXFP4)
+    g = inp.to("cuda")
+    for rep in range(60):
+        out = pkg.decode(g.q, g.kv, g.kv_scale, g.kv_indptr, synth.KV_MXFP4, num_splits=0)
+        torch.cuda.synchronize()
+        assert pkg.device_status(clear=True) == pkg.MLA_OK
+        _check(out, ref, f"lens {lens} repetition {rep}")
