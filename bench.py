@@ -51,6 +51,9 @@ def parse():
                     help="--impl reference: total oracle time over all warm-up and timed steps")
     ap.add_argument("--quick", action="store_true",
                     help="timed steps only (no clock soak, e2e or CPU baseline); for profiler runs")
+    ap.add_argument("--page-size", type=int, default=0, choices=[0, 64, 128],
+                    help="with --quick: store the workload's cache in shuffled pages of this many rows "
+                         "and time mla_decode_paged (uniform splits)")
     return ap.parse_args()
 
 
@@ -278,6 +281,16 @@ def main():
     B = inp.batch
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     ns = pkg.resolve_splits(spec.num_splits, B, inp.rows // B, sms, spec.kv_dtype)
+    paged = None
+    if args.page_size:
+        if not args.quick:
+            raise SystemExit("--page-size is a --quick measurement")
+        paged = synth.to_paged(inp, args.page_size, seed=spec.seed + 7).to(dev)
+        kv_bytes = inp.kv_bytes()
+        inp.kv = None                    # free the contiguous copy
+        torch.cuda.empty_cache()
+        if ns < 1:                       # a paged cache takes uniform splits only
+            ns = max(1, min(sms // B, 4096))
     pkg.reserve_workspace(pkg.workspace_slots(B, ns, sms))
     out = torch.empty((B, 16, 512), dtype=torch.bfloat16, device=dev)
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
@@ -290,7 +303,11 @@ def main():
     stream = torch.cuda.current_stream(dev)
 
     def call():
-        rc = pkg.mla_decode(inp.q, inp.kv, inp.kv_scale, inp.kv_indptr, out, B, ns, spec.kv_dtype, stream)
+        if paged is not None:
+            rc = pkg.mla_decode_paged(paged.q, paged.kv, paged.kv_scale, paged.page_indptr, paged.page_indices,
+                                      paged.last_page_len, args.page_size, out, B, ns, spec.kv_dtype, stream)
+        else:
+            rc = pkg.mla_decode(inp.q, inp.kv, inp.kv_scale, inp.kv_indptr, out, B, ns, spec.kv_dtype, stream)
         if rc != pkg.MLA_OK:
             raise pkg.MLAError(rc, "mla_decode")
 
@@ -332,9 +349,10 @@ def main():
         raise RuntimeError("kernel reported a pipeline timeout during the benchmark")
     if args.quick:
         if rank == 0:
-            print(json.dumps({"workload": spec.name, "us_per_call": ms * 1e3, "split_kernel_us": split_ms * 1e3,
-                              "kv_bytes_per_call": inp.kv_bytes(),
-                              "split_gbs": inp.kv_bytes() / (split_ms * 1e-3) / 1e9}), flush=True)
+            kvb = kv_bytes if paged is not None else inp.kv_bytes()
+            print(json.dumps({"workload": spec.name, "page_size": args.page_size, "num_splits": ns,
+                              "us_per_call": ms * 1e3, "split_kernel_us": split_ms * 1e3,
+                              "kv_bytes_per_call": kvb, "split_gbs": kvb / (split_ms * 1e-3) / 1e9}), flush=True)
         return
 
     # ---- end to end: host (pinned) inputs -> device, decode, output -> host, every step

@@ -91,6 +91,34 @@ int mla_decode(const void* q, const void* kv, const void* kv_scale, const int32_
                void* out, int batch, int num_splits, int kv_dtype, void* stream);
 
 /*
+ * mla_decode_paged -- the same decode over a paged KV cache: the pages of a sequence need
+ * not be contiguous or in order.  Layout of the page table as in the library-routed a16w8
+ * path of amd-mixed-mla submission 700955 (a page-level indptr, `kv_indices`,
+ * `kv_last_page_len`, `page_size`); the operation on each sequence is exactly mla_decode's.
+ *
+ *  kv               cache rows grouped in pages of page_size rows: physical page P holds
+ *                   rows [P * page_size, (P + 1) * page_size) of the same row layout as
+ *                   mla_decode (bf16 [.][576], e4m3 [.][576] or MXFP4 [.][288]); 16-byte aligned.
+ *  kv_scale         as mla_decode; for MXFP4 indexed by the same (physical) row.
+ *  kv_page_indptr   int32 [batch+1] (device): sequence b's pages are
+ *                   kv_page_indices[kv_page_indptr[b] .. kv_page_indptr[b+1]).
+ *  kv_page_indices  int32 (device): physical page numbers, in sequence order.
+ *  kv_last_page_len int32 [batch] (device): rows used in the sequence's last page,
+ *                   1 .. page_size (ignored for a sequence with no pages, which has length 0).
+ *                   Sequence b has (npages_b - 1) * page_size + kv_last_page_len[b] tokens.
+ *  page_size        64 or 128.
+ *  num_splits       >= 1: uniform splits as mla_decode; <= 0: min(floor(SMs / batch), 4096),
+ *                   at least 1, uniform splits (there is no balanced mode for paged caches).
+ * Every page number times page_size plus page_size must be a row inside kv, and every
+ * index read must lie inside kv_page_indices; violations are undefined behaviour, as with
+ * kv_indptr.  Errors: as mla_decode, plus MLA_ERR_INVALID_ARG for a page_size other than
+ * 64 or 128 or a null page table.
+ */
+int mla_decode_paged(const void* q, const void* kv, const void* kv_scale, const int32_t* kv_page_indptr,
+                     const int32_t* kv_page_indices, const int32_t* kv_last_page_len, int page_size, void* out,
+                     int batch, int num_splits, int kv_dtype, void* stream);
+
+/*
  * mla_decode_pick_splits -- host-only choice of num_splits for mla_decode.
  *     ns = min(floor(num_sms / batch), ceil(kv_len_hint / 256));  returns ns if ns >= 2,
  *     else 0 (the balanced persistent mode).

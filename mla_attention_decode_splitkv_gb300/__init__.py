@@ -5,7 +5,8 @@ in-tree by ``build.build()``); ``decode`` / ``mla_decode`` here only marshal arg
 ``synth`` makes seeded synthetic inputs.
 """
 from ._lib import (MLA_ERR_CUDA, MLA_ERR_INVALID_ARG, MLA_ERR_NO_MEMORY, MLA_ERR_TIMEOUT,  # noqa: F401
-                   MLA_ERR_UNSUPPORTED, MLA_OK, MLAError, decode, device_status, load, mla_decode,
+                   MLA_ERR_UNSUPPORTED, MLA_OK, MLAError, decode, decode_paged, device_status, load, mla_decode,
+                   mla_decode_paged,
                    pick_splits, profile_begin, profile_end, release_workspace, reserve_workspace, resolve_splits,
                    set_test_stall, set_wait_limit_ns, workspace_slots)
 

@@ -31,6 +31,7 @@ EXPORTED = (
     "mla_decode_profile_begin",
     "mla_decode_profile_end",
     "mla_decode_noalloc",
+    "mla_decode_paged",
     "mla_status_string",
     "mla_last_cuda_error",
 )
@@ -80,6 +81,8 @@ def load(path: str = LIB_PATH):
         lib.mla_decode_profile_end.restype = c_int
         lib.mla_decode_profile_end.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double),
                                                ctypes.POINTER(c_int)]
+        lib.mla_decode_paged.restype = c_int
+        lib.mla_decode_paged.argtypes = [vp, vp, vp, vp, vp, vp, c_int, vp, c_int, c_int, c_int, vp]
         lib.mla_decode_noalloc.restype = c_int
         lib.mla_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, c_int, c_int, c_int, vp]
         lib.mla_status_string.restype = ctypes.c_char_p
@@ -119,6 +122,29 @@ def decode(q, kv, kv_scale, kv_indptr, kv_dtype: int, num_splits: int = 0, out=N
     rc = mla_decode(q, kv, kv_scale, kv_indptr, out, batch, num_splits, kv_dtype, stream)
     if rc != MLA_OK:
         raise MLAError(rc, "mla_decode")
+    return out
+
+
+def mla_decode_paged(q, kv, kv_scale, page_indptr, page_indices, last_page_len, page_size: int, out, batch: int,
+                     num_splits: int, kv_dtype: int, stream=None) -> int:
+    """Raw C-ABI call for a paged cache (device tensors); returns the mla_status code."""
+    lib = load()
+    return lib.mla_decode_paged(_ptr(q), _ptr(kv), _ptr(kv_scale), _ptr(page_indptr), _ptr(page_indices),
+                                _ptr(last_page_len), int(page_size), _ptr(out), int(batch), int(num_splits),
+                                int(kv_dtype), _stream_handle(stream))
+
+
+def decode_paged(q, kv, kv_scale, page_indptr, page_indices, last_page_len, page_size: int, kv_dtype: int,
+                 num_splits: int = 0, out=None, stream=None):
+    """out = MLA decode of q over a paged cache (all tensors on the GPU); raises MLAError."""
+    import torch
+    batch = q.shape[0]
+    if out is None:
+        out = torch.empty((batch, 16, 512), dtype=torch.bfloat16, device=q.device)
+    rc = mla_decode_paged(q, kv, kv_scale, page_indptr, page_indices, last_page_len, page_size, out, batch,
+                          num_splits, kv_dtype, stream)
+    if rc != MLA_OK:
+        raise MLAError(rc, "mla_decode_paged")
     return out
 
 

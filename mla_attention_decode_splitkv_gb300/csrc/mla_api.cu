@@ -6,6 +6,7 @@
 #include <cstdint>
 #include <cstdio>
 #include <cstdlib>
+#include <algorithm>
 #include <mutex>
 #include <vector>
 
@@ -116,7 +117,7 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 namespace mla {
 
-static int encode_map(CUtensorMap* map, const void* kv, int kv_dtype, bool rope) {
+static int encode_map(CUtensorMap* map, const void* kv, int kv_dtype, bool rope, int box_rows = kBN) {
   static std::mutex mu;
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   {
@@ -134,7 +135,7 @@ static int encode_map(CUtensorMap* map, const void* kv, int kv_dtype, bool rope)
   const cuuint64_t width = mx ? kMxPacked : kDim;                       // elements per row
   cuuint64_t gdim[2] = {width, rows};
   cuuint64_t gstride[1] = {width * (bf ? 2 : 1)};                       // bytes per row
-  cuuint32_t box[2] = {(bf || mx || rope) ? 64u : 128u, static_cast<cuuint32_t>(kBN)};
+  cuuint32_t box[2] = {(bf || mx || rope) ? 64u : 128u, static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estride[2] = {1, 1};
   CUresult r = encode(map, bf ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
                       const_cast<void*>(kv), gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -145,6 +146,12 @@ static int encode_map(CUtensorMap* map, const void* kv, int kv_dtype, bool rope)
 
 int encode_kv_map(CUtensorMap* map, const void* kv, int kv_dtype) { return encode_map(map, kv, kv_dtype, false); }
 int encode_rope_map(CUtensorMap* map, const void* kv) { return encode_map(map, kv, MLA_KV_FP8_E4M3, true); }
+int encode_kv_map_rows(CUtensorMap* map, const void* kv, int kv_dtype, int box_rows) {
+  return encode_map(map, kv, kv_dtype, false, box_rows);
+}
+int encode_rope_map_rows(CUtensorMap* map, const void* kv, int box_rows) {
+  return encode_map(map, kv, MLA_KV_FP8_E4M3, true, box_rows);
+}
 
 }  // namespace mla
 
@@ -222,9 +229,16 @@ int mla_decode_device_status(int clear) {
   return (v & mla::kStatusTimeout) ? MLA_ERR_TIMEOUT : MLA_OK;
 }
 
-int mla_decode(const void* q, const void* kv, const void* kv_scale, const int32_t* kv_indptr, void* out, int batch,
-               int num_splits, int kv_dtype, void* stream) {
+// Shared by mla_decode (page_size 0) and mla_decode_paged.
+static int decode_impl(const void* q, const void* kv, const void* kv_scale, const int32_t* kv_indptr,
+                       const int32_t* page_indices, const int32_t* last_page_len, int page_size, void* out,
+                       int batch, int num_splits, int kv_dtype, void* stream) {
   if (q == nullptr || kv == nullptr || kv_indptr == nullptr || out == nullptr) return MLA_ERR_INVALID_ARG;
+  if (page_size != 0) {
+    if (page_size != 64 && page_size != 128) return MLA_ERR_INVALID_ARG;
+    if (page_indices == nullptr || last_page_len == nullptr) return MLA_ERR_INVALID_ARG;
+    if (!aligned(page_indices, 4) || !aligned(last_page_len, 4)) return MLA_ERR_INVALID_ARG;
+  }
   if (batch <= 0 || num_splits > mla::kMaxSplits) return MLA_ERR_INVALID_ARG;
   if (kv_dtype != MLA_KV_BF16 && kv_dtype != MLA_KV_FP8_E4M3 && kv_dtype != MLA_KV_MXFP4) return MLA_ERR_INVALID_ARG;
   if (kv_dtype != MLA_KV_BF16 && kv_scale == nullptr) return MLA_ERR_INVALID_ARG;
@@ -237,7 +251,8 @@ int mla_decode(const void* q, const void* kv, const void* kv_scale, const int32_
   if (rc) return rc;
   if (cc != 103) return MLA_ERR_UNSUPPORTED;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int ns = num_splits >= 1 ? num_splits : 0;
+  int ns = num_splits >= 1 ? num_splits : 0;
+  if (page_size != 0 && ns == 0) ns = std::max(1, std::min(sms / batch, mla::kMaxSplits));   // paged: uniform only
   const long long grid_ll = ns >= 1 ? static_cast<long long>(batch) * ns : sms;
   if (grid_ll > 0x7fffffffLL) return MLA_ERR_INVALID_ARG;
 
@@ -250,12 +265,16 @@ int mla_decode(const void* q, const void* kv, const void* kv_scale, const int32_
   }
 
   mla::DecodeParams p;
-  rc = mla::encode_kv_map(&p.tmap, kv, kv_dtype);
+  const int box_rows = page_size != 0 ? page_size : mla::kBN;
+  rc = mla::encode_kv_map_rows(&p.tmap, kv, kv_dtype, box_rows);
   if (rc) return rc;
   if (kv_dtype == MLA_KV_FP8_E4M3) {
-    rc = mla::encode_rope_map(&p.tmap_rope, kv);
+    rc = mla::encode_rope_map_rows(&p.tmap_rope, kv, box_rows);
     if (rc) return rc;
   }
+  p.page_size = page_size;
+  p.page_indices = page_indices;
+  p.last_page_len = last_page_len;
   p.q = static_cast<const uint16_t*>(q);
   p.kv = static_cast<const uint8_t*>(kv);
   p.kv_scale = kv_scale;
@@ -289,13 +308,27 @@ int mla_decode(const void* q, const void* kv, const void* kv_scale, const int32_
     }
   }
   if (prof) cudaEventRecord(rec.start, st);
-  cudaError_t e = mla::launch_split(kv_dtype, p, static_cast<int>(grid_ll), st);
+  cudaError_t e = page_size != 0 ? mla::launch_split_paged(kv_dtype, p, static_cast<int>(grid_ll), st)
+                                  : mla::launch_split(kv_dtype, p, static_cast<int>(grid_ll), st);
   if (e != cudaSuccess) return note_cuda(e);
   if (prof) {
     cudaEventRecord(rec.split_end, st);
     cudaEventRecord(rec.end, st);
   }
   return MLA_OK;
+}
+
+int mla_decode(const void* q, const void* kv, const void* kv_scale, const int32_t* kv_indptr, void* out, int batch,
+               int num_splits, int kv_dtype, void* stream) {
+  return decode_impl(q, kv, kv_scale, kv_indptr, nullptr, nullptr, 0, out, batch, num_splits, kv_dtype, stream);
+}
+
+int mla_decode_paged(const void* q, const void* kv, const void* kv_scale, const int32_t* kv_page_indptr,
+                     const int32_t* kv_page_indices, const int32_t* kv_last_page_len, int page_size, void* out,
+                     int batch, int num_splits, int kv_dtype, void* stream) {
+  if (page_size == 0) return MLA_ERR_INVALID_ARG;
+  return decode_impl(q, kv, kv_scale, kv_page_indptr, kv_page_indices, kv_last_page_len, page_size, out, batch,
+                     num_splits, kv_dtype, stream);
 }
 
 int mla_decode_profile_begin(void) {

@@ -37,6 +37,10 @@ struct DecodeParams {
   float logit_scale_log2;          // sm_scale * log2(e)
   unsigned long long wait_limit_ns;
   int test_stall;                  // test hook: the QK issuer waits on a barrier that never completes
+  // Paged cache (mla_decode_paged; 0 / null otherwise): kv_indptr indexes page_indices.
+  int page_size;                   // rows per page: 64 or 128
+  const int32_t* page_indices;     // [kv_indptr[batch]] physical page of each sequence page
+  const int32_t* last_page_len;    // [batch] rows used in each sequence's last page (1..page_size)
 };
 
 
@@ -52,5 +56,10 @@ int encode_rope_map(CUtensorMap* map, const void* kv);
 
 // Launches the split kernel for kv_dtype (geometry per dtype is internal to mla_split.cu).
 cudaError_t launch_split(int kv_dtype, const DecodeParams& p, int grid, cudaStream_t stream);
+// The same for a paged cache (uniform splits; page size 64 or 128, boxes of page_size rows).
+cudaError_t launch_split_paged(int kv_dtype, const DecodeParams& p, int grid, cudaStream_t stream);
+// Tensor maps with boxes of `box_rows` rows (paged caches: box_rows = page size).
+int encode_kv_map_rows(CUtensorMap* map, const void* kv, int kv_dtype, int box_rows);
+int encode_rope_map_rows(CUtensorMap* map, const void* kv, int box_rows);
 
 }  // namespace mla

@@ -108,6 +108,9 @@ extern "C" int mla_decode_noalloc(const void* q, const void* kv, const void* kv_
   p.logit_scale_log2 = static_cast<float>((1.0 / std::sqrt(static_cast<double>(mla::kDim))) * 1.4426950408889634);
   p.wait_limit_ns = 2000000000ull;
   p.test_stall = 0;
+  p.page_size = 0;
+  p.page_indices = nullptr;
+  p.last_page_len = nullptr;
   if (mla::launch_split(kv_dtype, p, static_cast<int>(grid), st) != cudaSuccess) { cudaGetLastError(); return MLA_ERR_CUDA; }
   return MLA_OK;
 }

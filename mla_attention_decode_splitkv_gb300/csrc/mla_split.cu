@@ -173,7 +173,8 @@ static_assert(smem_bytes<0>() <= 232448, "bf16 shared memory exceeds 227 KB");
 // ---------------------------------------------------------------- work decomposition
 struct Seg {
   int b;       // batch row
-  int row0;    // kv_indptr[b]
+  int row0;    // kv_indptr[b] (paged: the sequence's first entry in the page list)
+  int n_total; // tokens in the sequence
   int n_lo;    // token range [n_lo, n_hi) within the sequence
   int n_hi;
   int slot;    // partial-result slot (when !direct)
@@ -225,6 +226,7 @@ __device__ int warp_first_seq(const int32_t* ip, int batch, long long lo) {
 //  balanced (num_splits == 0): CTA c owns tokens [c*T/G, (c+1)*T/G) of the concatenated
 //     batch (T = kv_indptr[batch]); each sequence it touches is one non-empty segment;
 //     partial slot = b + c (unique: the (b, c) pairs form a monotone staircase).
+template <bool PG>
 struct SegIter {
   long long lo, hi;
   int b, split, ns, cta;
@@ -256,12 +258,15 @@ struct SegIter {
     if (uniform) {
       int r0 = p.kv_indptr[b];
       long long L = static_cast<long long>(p.kv_indptr[b + 1]) - r0;
+      if constexpr (PG) {   // r0: the sequence's first entry in the page list
+        L = L > 0 ? (L - 1) * p.page_size + p.last_page_len[b] : 0;
+      }
       long long per = (L + ns - 1) / ns;
       long long chunk = ((per + kBN - 1) / kBN) * kBN;
       long long a = split * chunk, e = a + chunk;
       if (a > L) a = L;
       if (e > L) e = L;
-      s.b = b; s.row0 = r0; s.n_lo = (int)a; s.n_hi = (int)e;
+      s.b = b; s.row0 = r0; s.n_lo = (int)a; s.n_hi = (int)e; s.n_total = (int)L;
       s.slot = b * ns + split; s.direct = (ns == 1);
       done = true;
       return true;
@@ -276,12 +281,12 @@ struct SegIter {
       if (r1 > r0) {
         long long a = lo > r0 ? lo : r0, e = hi < r1 ? hi : r1;
         if (e > a) {
-          s.b = bb; s.row0 = r0; s.n_lo = (int)(a - r0); s.n_hi = (int)(e - r0);
+          s.b = bb; s.row0 = r0; s.n_lo = (int)(a - r0); s.n_hi = (int)(e - r0); s.n_total = r1 - r0;
           s.slot = bb + cta; s.direct = (a == r0 && e == r1);
           return true;
         }
       } else if (r0 >= lo && (r0 < hi || last_cta)) {
-        s.b = bb; s.row0 = r0; s.n_lo = 0; s.n_hi = 0; s.slot = bb + cta; s.direct = true;
+        s.b = bb; s.row0 = r0; s.n_lo = 0; s.n_hi = 0; s.n_total = 0; s.slot = bb + cta; s.direct = true;
         return true;
       }
     }
@@ -297,16 +302,35 @@ struct Window {
   int y0;     // first cached row of the window (may be negative)
   int shift;  // window row of the tile's first token
   int cnt;    // valid tokens in the tile
+  int y1;     // paged: first cached row of the window's second half (page size 64)
 };
-template <int KV>
-__device__ __forceinline__ Window tile_window(const Seg& s, int t) {
-  int row_start = s.row0 + s.n_lo + t * kBN;
-  int row_hi = s.row0 + s.n_hi;
-  int y0 = min(row_start, row_hi - kBN);
+// Contiguous cache: the window ends at the segment's last row (rows before cached row 0 are
+// the TMA's zero fill).  Paged cache (uniform splits, tiles start at multiples of 128 tokens
+// of the sequence, hence on page boundaries): window row i is token 128 t + i; its first
+// half is page (128 t) / P of the sequence, its second half (P = 64) the next page, or the
+// same page again when the sequence has no next page (rows that are masked).
+template <int KV, bool PG>
+__device__ __forceinline__ Window tile_window(const DecodeParams& p, const Seg& s, int t) {
   Window w;
-  w.y0 = y0;
-  w.shift = row_start - y0;
-  w.cnt = min(kBN, row_hi - row_start);
+  if constexpr (PG) {
+    const int start = s.n_lo + t * kBN;
+    const int P = p.page_size;
+    const int np = (s.n_total + P - 1) / P;
+    const int pg0 = start / P;
+    const int pg1 = (P == kBN || pg0 + 1 >= np) ? pg0 : pg0 + 1;
+    w.y0 = p.page_indices[s.row0 + pg0] * P;
+    w.y1 = p.page_indices[s.row0 + pg1] * P + (P == kBN ? kBN / 2 : 0);
+    w.shift = 0;
+    w.cnt = min(kBN, s.n_hi - start);
+  } else {
+    int row_start = s.row0 + s.n_lo + t * kBN;
+    int row_hi = s.row0 + s.n_hi;
+    int y0 = min(row_start, row_hi - kBN);
+    w.y0 = y0;
+    w.shift = row_start - y0;
+    w.cnt = min(kBN, row_hi - row_start);
+    w.y1 = y0 + kBN / 2;
+  }
   return w;
 }
 
@@ -413,9 +437,10 @@ __device__ void stage_q_fp8(const DecodeParams& p, int b, uint8_t* qs, float* qs
 // boxes, 64-byte swizzle): bytes [64c, 64c + 64) of the window's 128 rows for the value
 // chunks c = 0..3 and bytes [256, 288) for the rope chunk (the box's columns past 288 are
 // zero-filled).  The dequantisation frees each slab as soon as it has read it.
+template <bool PG>
 __device__ void run_producer_mx(const DecodeParams& p, SharedState* sh, uint8_t* slabs) {
   volatile int* abortf = &sh->abort;
-  SegIter it;
+  SegIter<PG> it;
   it.init(p, blockIdx.x, sh->seg_total, sh->seg_b0);
   Seg s;
   uint32_t idx = 0, slot = 0, phase = 0;
@@ -425,7 +450,7 @@ __device__ void run_producer_mx(const DecodeParams& p, SharedState* sh, uint8_t*
     if (n <= 0) continue;
     const int ntiles = (n + kBN - 1) / kBN;
     for (int t = 0; t < ntiles && ok; ++t) {
-      const Window w = tile_window<2>(s, t);
+      const Window w = tile_window<2, PG>(p, s, t);
       for (int c = 0; c < 5; ++c) {
         if (!wait_bar(smem_u32(&sh->slab_empty[slot]), phase ^ 1, abortf, p.status, p.wait_limit_ns)) {
           ok = false;
@@ -433,7 +458,12 @@ __device__ void run_producer_mx(const DecodeParams& p, SharedState* sh, uint8_t*
         }
         const uint32_t fb = smem_u32(&sh->slab_full[slot]);
         mbar_arrive_expect_tx(fb, kSlabBytes);
-        tma_load_2d(smem_u32(slabs + slot * kSlabBytes), &p.tmap, 64 * c, w.y0, fb);
+        if (PG && p.page_size < kBN) {   // two 64-row boxes: the window's two pages
+          tma_load_2d(smem_u32(slabs + slot * kSlabBytes), &p.tmap, 64 * c, w.y0, fb);
+          tma_load_2d(smem_u32(slabs + slot * kSlabBytes + kSlabBytes / 2), &p.tmap, 64 * c, w.y1, fb);
+        } else {
+          tma_load_2d(smem_u32(slabs + slot * kSlabBytes), &p.tmap, 64 * c, w.y0, fb);
+        }
         ++idx;
         if (++slot == kSlabs) { slot = 0; phase ^= 1; }
       }
@@ -446,11 +476,11 @@ __device__ void run_producer_mx(const DecodeParams& p, SharedState* sh, uint8_t*
   }
 }
 
-template <int KV>
+template <int KV, bool PG>
 __device__ void run_producer(const DecodeParams& p, SharedState* sh, uint8_t* ring, uint8_t* rope) {
   using C = Cfg<KV>;
   volatile int* abortf = &sh->abort;
-  SegIter it;
+  SegIter<PG> it;
   it.init(p, blockIdx.x, sh->seg_total, sh->seg_b0);
   Seg s;
   uint32_t idx = 0, slot = 0, phase = 0, ridx = 0;
@@ -460,7 +490,7 @@ __device__ void run_producer(const DecodeParams& p, SharedState* sh, uint8_t* ri
     if (n <= 0) continue;
     const int ntiles = (n + kBN - 1) / kBN;
     for (int t = 0; t < ntiles && ok; ++t) {
-      const Window w = tile_window<KV>(s, t);
+      const Window w = tile_window<KV, PG>(p, s, t);
       for (int c = 0; c < C::kRingPT; ++c) {
         if (!wait_bar(smem_u32(&sh->empty[slot]), phase ^ 1, abortf, p.status, p.wait_limit_ns)) {
           ok = false;
@@ -468,18 +498,29 @@ __device__ void run_producer(const DecodeParams& p, SharedState* sh, uint8_t* ri
         }
         const uint32_t dst = smem_u32(ring + slot * C::kSlotBytes);
         const uint32_t fb = smem_u32(&sh->full[slot]);
+        // A box is 128 rows (contiguous cache, 128-row pages) or 64 rows (64-row pages: the
+        // window's two pages land in the two halves of the box's SMEM footprint).
+        const bool halves = PG && p.page_size < kBN;
+        auto box = [&](uint32_t d, int x, uint32_t bytes) {
+          if (halves) {
+            tma_load_2d(d, &p.tmap, x, w.y0, fb);
+            tma_load_2d(d + bytes / 2, &p.tmap, x, w.y1, fb);
+          } else {
+            tma_load_2d(d, &p.tmap, x, w.y0, fb);
+          }
+        };
         if constexpr (KV == 0) {
           if (c < 4) {
             mbar_arrive_expect_tx(fb, 32768);
-            tma_load_2d(dst, &p.tmap, 128 * c, w.y0, fb);
-            tma_load_2d(dst + 16384, &p.tmap, 128 * c + 64, w.y0, fb);
+            box(dst, 128 * c, 16384);
+            box(dst + 16384, 128 * c + 64, 16384);
           } else {
             mbar_arrive_expect_tx(fb, 16384);
-            tma_load_2d(dst, &p.tmap, 512, w.y0, fb);
+            box(dst, 512, 16384);
           }
         } else {
           mbar_arrive_expect_tx(fb, 16384);
-          tma_load_2d(dst, &p.tmap, 128 * c, w.y0, fb);
+          box(dst, 128 * c, 16384);
         }
         ++idx;
         if (++slot == C::kRing) { slot = 0; phase ^= 1; }
@@ -494,7 +535,12 @@ __device__ void run_producer(const DecodeParams& p, SharedState* sh, uint8_t* ri
         }
         const uint32_t fb = smem_u32(&sh->rope_full[rs]);
         mbar_arrive_expect_tx(fb, kRopeBytes);
-        tma_load_2d(smem_u32(rope + rs * kRopeBytes), &p.tmap_rope, kDimV, w.y0, fb);
+        if (PG && p.page_size < kBN) {
+          tma_load_2d(smem_u32(rope + rs * kRopeBytes), &p.tmap_rope, kDimV, w.y0, fb);
+          tma_load_2d(smem_u32(rope + rs * kRopeBytes + kRopeBytes / 2), &p.tmap_rope, kDimV, w.y1, fb);
+        } else {
+          tma_load_2d(smem_u32(rope + rs * kRopeBytes), &p.tmap_rope, kDimV, w.y0, fb);
+        }
         ++ridx;
       }
     }
@@ -551,6 +597,7 @@ __device__ __forceinline__ void deq_block(const uint4 v, const uint2 lut, uint4&
 // for the PV MMAs of tile g); the rope chunk goes to its own SW64 buffer.  Each chunk is
 // published (full barrier) as soon as it is written.  Window rows before cached row 0
 // hold zeros (TMA fill) and get no scale: they decode to zeros.
+template <bool PG>
 __device__ void run_dequant(const DecodeParams& p, SharedState* sh, uint8_t* ring, uint8_t* rope, uint8_t* slabs) {
   using C = Cfg<2>;
   volatile int* abortf = &sh->abort;
@@ -565,7 +612,7 @@ __device__ void run_dequant(const DecodeParams& p, SharedState* sh, uint8_t* rin
   }
   bar_sync(2, C::kDeqWarps * 32);
   const int ssw = (di >> 1) & 3;           // SW64 piece swizzle of this row in a slab
-  SegIter it;
+  SegIter<PG> it;
   it.init(p, blockIdx.x, sh->seg_total, sh->seg_b0);
   Seg s;
   uint32_t g = 0, slab_i = 0, slab_ph = 0;
@@ -576,18 +623,20 @@ __device__ void run_dequant(const DecodeParams& p, SharedState* sh, uint8_t* rin
     const int ntiles = (n + kBN - 1) / kBN;
     uint32_t scn[9];   // block scales of the segment's next tile, loaded one tile ahead
     for (int t = 0; t < ntiles; ++t) {
-      const Window w = tile_window<2>(s, t);
+      const Window w = tile_window<2, PG>(p, s, t);
       // e_i = max_j E_j and the shift-table index min(e_i - E_j, 13) of each block, packed
       // as 4-bit fields (block j in bits 4 (j % 8) of kpk[j / 8]).
       int emax = 127;
       uint32_t kpk[3] = {0u, 0u, 0u};
-      if (w.y0 + di >= 0) {
+      // Cached row of this thread's window row (paged: its page's physical row).
+      const int yr = PG ? (di < kBN / 2 ? w.y0 + di : w.y1 + di - kBN / 2) : w.y0 + di;
+      if (yr >= 0) {
         uint32_t sc[9];
         if (t > 0) {
 #pragma unroll
           for (int j = 0; j < 9; ++j) sc[j] = scn[j];
         } else {
-          const uint16_t* sp = reinterpret_cast<const uint16_t*>(scales + static_cast<size_t>(w.y0 + di) * kMxScales);
+          const uint16_t* sp = reinterpret_cast<const uint16_t*>(scales + static_cast<size_t>(yr) * kMxScales);
 #pragma unroll
           for (int j = 0; j < 9; ++j) sc[j] = __ldg(sp + j);
         }
@@ -601,9 +650,10 @@ __device__ void run_dequant(const DecodeParams& p, SharedState* sh, uint8_t* rin
         }
       }
       if (t + 1 < ntiles) {
-        const Window wn = tile_window<2>(s, t + 1);
-        if (wn.y0 + di >= 0) {
-          const uint16_t* sp = reinterpret_cast<const uint16_t*>(scales + static_cast<size_t>(wn.y0 + di) * kMxScales);
+        const Window wn = tile_window<2, PG>(p, s, t + 1);
+        const int yn = PG ? (di < kBN / 2 ? wn.y0 + di : wn.y1 + di - kBN / 2) : wn.y0 + di;
+        if (yn >= 0) {
+          const uint16_t* sp = reinterpret_cast<const uint16_t*>(scales + static_cast<size_t>(yn) * kMxScales);
 #pragma unroll
           for (int j = 0; j < 9; ++j) scn[j] = __ldg(sp + j);
         }
@@ -704,12 +754,12 @@ __device__ __forceinline__ Descs make_descs(uint8_t* ring, uint8_t* rope, uint8_
 // Byte offset -> descriptor start-address increment.
 __device__ __forceinline__ uint64_t dofs(uint32_t bytes) { return static_cast<uint64_t>(bytes >> 4); }
 
-template <int KV>
+template <int KV, bool PG>
 __device__ void run_mma_qk(const DecodeParams& p, SharedState* sh, const Descs& ds, uint32_t tmem) {
   using C = Cfg<KV>;
   constexpr uint32_t idq = instr_desc(KV == 0 ? 1u : 0u, 0, 0, 128, C::kN);  // bf16 | e4m3, K-major A and B
   volatile int* abortf = &sh->abort;
-  SegIter it;
+  SegIter<PG> it;
   it.init(p, blockIdx.x, sh->seg_total, sh->seg_b0);
   Seg s;
   uint32_t g = 0, slot = 0, phase = 0;
@@ -761,12 +811,12 @@ __device__ void run_mma_qk(const DecodeParams& p, SharedState* sh, const Descs& 
 }
 
 // PV issuer `part` (0 or 1) issues the two 128-dim blocks 2*part, 2*part+1 of every tile.
-template <int KV>
+template <int KV, bool PG>
 __device__ void run_mma_pv(const DecodeParams& p, SharedState* sh, const Descs& ds, uint32_t tmem, int part) {
   using C = Cfg<KV>;
   constexpr uint32_t idp = instr_desc(KV == 0 ? 1u : 0u, 1, 1, 128, C::kN);  // MN-major A (V^T) and B (P^T)
   volatile int* abortf = &sh->abort;
-  SegIter it;
+  SegIter<PG> it;
   it.init(p, blockIdx.x, sh->seg_total, sh->seg_b0);
   Seg s;
   uint32_t g = 0, slot0 = 0;                      // ring slot of chunk 0 of tile g
@@ -1034,7 +1084,7 @@ __device__ void write_empty_result(const DecodeParams& p, const Seg& s, int ts) 
 // per-tile latency of this stage); kSoftWarps = 4 gives each thread all 16 heads.  The two
 // head groups never share a named barrier on a path the other may skip: every named
 // barrier below is reached by all softmax threads once per tile (or once per segment).
-template <int KV>
+template <int KV, bool PG>
 __device__ void run_softmax(const DecodeParams& p, SharedState* sh, uint8_t* qs, uint8_t* ps, uint32_t tmem) {
   using C = Cfg<KV>;
   constexpr int NW = C::kSoftWarps;
@@ -1052,16 +1102,16 @@ __device__ void run_softmax(const DecodeParams& p, SharedState* sh, uint8_t* qs,
   if constexpr (KV == 1) kv_scale = __ldg(reinterpret_cast<const float*>(p.kv_scale));
   const float xscale = p.logit_scale_log2 * kv_scale;    // raw dot product -> log2-domain logit
 
-  SegIter it;
+  SegIter<PG> it;
   it.init(p, blockIdx.x, sh->seg_total, sh->seg_b0);
   Seg cur, nxt;
   bool has_cur = it.next(p, cur);
   // Stage q of the first non-empty segment (the iterator may first yield empty ones).
-  auto stage_next_nonempty = [&](const SegIter& from, const Seg* first) {
+  auto stage_next_nonempty = [&](const SegIter<PG>& from, const Seg* first) {
     Seg sn;
     bool found = false;
     if (first != nullptr && first->n_hi > first->n_lo) { sn = *first; found = true; }
-    SegIter look = from;
+    SegIter<PG> look = from;
     while (!found && look.next(p, sn)) found = sn.n_hi > sn.n_lo;
     if (found && ts < 128) {
       if constexpr (KV == 0) stage_q_bf16(p, sn.b, qs, ts); else stage_q_fp8(p, sn.b, qs, sh->qscale, ts);
@@ -1088,7 +1138,7 @@ __device__ void run_softmax(const DecodeParams& p, SharedState* sh, uint8_t* qs,
     float mref[H], lpart[H];
     bool has_nxt = false;
     for (int t = 0; t < ntiles; ++t) {
-      const Window w = tile_window<KV>(cur, t);
+      const Window w = tile_window<KV, PG>(p, cur, t);
       bool okw = wait_bar(smem_u32(&sh->s_full[g & 1]), (g >> 1) & 1, abortf, p.status, p.wait_limit_ns);
       okw = __all_sync(0xffffffffu, okw);
       tc_fence_after();
@@ -1294,7 +1344,7 @@ __device__ void run_softmax(const DecodeParams& p, SharedState* sh, uint8_t* qs,
 }
 
 // ---------------------------------------------------------------- the kernel
-template <int KV>
+template <int KV, bool PG>
 __global__ void __launch_bounds__(Cfg<KV>::kThreads, 1) mla_split_kernel(const __grid_constant__ DecodeParams p) {
   using C = Cfg<KV>;
   extern __shared__ uint8_t smem_raw[];
@@ -1362,21 +1412,21 @@ __global__ void __launch_bounds__(Cfg<KV>::kThreads, 1) mla_split_kernel(const _
     if constexpr (KV == 2) regs_dec<C::kRegsIssue>();
     if (warp == 0) {
       if (lane == 0) {
-        if constexpr (KV == 2) run_producer_mx(p, sh, slabs); else run_producer<KV>(p, sh, ring, rope);
+        if constexpr (KV == 2) run_producer_mx<PG>(p, sh, slabs); else run_producer<KV, PG>(p, sh, ring, rope);
       }
     } else if (warp == 1) {
-      if (lane == 0) run_mma_qk<KV>(p, sh, make_descs(ring, rope, qs, ps), tmem);
+      if (lane == 0) run_mma_qk<KV, PG>(p, sh, make_descs(ring, rope, qs, ps), tmem);
     } else {
-      if (lane == 0) run_mma_pv<KV>(p, sh, make_descs(ring, rope, qs, ps), tmem, warp - 2);
+      if (lane == 0) run_mma_pv<KV, PG>(p, sh, make_descs(ring, rope, qs, ps), tmem, warp - 2);
     }
     __syncwarp();
   } else if (warp < 4 + C::kSoftWarps) {
     if constexpr (KV == 2) regs_inc<C::kRegsSoft>();
-    run_softmax<KV>(p, sh, qs, ps, tmem);
+    run_softmax<KV, PG>(p, sh, qs, ps, tmem);
   } else {
     if constexpr (KV == 2) {
       regs_dec<C::kRegsDeq>();
-      run_dequant(p, sh, ring, rope, slabs);
+      run_dequant<PG>(p, sh, ring, rope, slabs);
     }
   }
   tc_fence_before();
@@ -1387,36 +1437,43 @@ __global__ void __launch_bounds__(Cfg<KV>::kThreads, 1) mla_split_kernel(const _
   }
 }
 
-template <int KV>
+template <int KV, bool PG>
 cudaError_t launch_split_t(const DecodeParams& p, int grid, cudaStream_t stream) {
   static int configured_device = -1;  // attribute is per function; set once per device id
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (configured_device != dev) {
-    e = cudaFuncSetAttribute(mla_split_kernel<KV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(mla_split_kernel<KV, PG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem_bytes<KV>()));
     if (e != cudaSuccess) return e;
     if constexpr (KV == 2) {
       // The register split's increases only complete if the CTA launched with at least the
       // registers the split hands out: refuse to launch otherwise.
       cudaFuncAttributes fa;
-      e = cudaFuncGetAttributes(&fa, mla_split_kernel<KV>);
+      e = cudaFuncGetAttributes(&fa, mla_split_kernel<KV, PG>);
       if (e != cudaSuccess) return e;
       if (fa.numRegs * Cfg<KV>::kThreads < Cfg<KV>::kRegsNeeded) return cudaErrorInvalidConfiguration;
     }
     configured_device = dev;
   }
-  mla_split_kernel<KV><<<grid, Cfg<KV>::kThreads, smem_bytes<KV>(), stream>>>(p);
+  mla_split_kernel<KV, PG><<<grid, Cfg<KV>::kThreads, smem_bytes<KV>(), stream>>>(p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_split(int kv_dtype, const DecodeParams& p, int grid, cudaStream_t stream) {
-  if (kv_dtype == 0) return launch_split_t<0>(p, grid, stream);
-  if (kv_dtype == 1) return launch_split_t<1>(p, grid, stream);
-  if (kv_dtype == 2) return launch_split_t<2>(p, grid, stream);
+  if (kv_dtype == 0) return launch_split_t<0, false>(p, grid, stream);
+  if (kv_dtype == 1) return launch_split_t<1, false>(p, grid, stream);
+  if (kv_dtype == 2) return launch_split_t<2, false>(p, grid, stream);
+  return cudaErrorNotSupported;
+}
+
+cudaError_t launch_split_paged(int kv_dtype, const DecodeParams& p, int grid, cudaStream_t stream) {
+  if (kv_dtype == 0) return launch_split_t<0, true>(p, grid, stream);
+  if (kv_dtype == 1) return launch_split_t<1, true>(p, grid, stream);
+  if (kv_dtype == 2) return launch_split_t<2, true>(p, grid, stream);
   return cudaErrorNotSupported;
 }
 

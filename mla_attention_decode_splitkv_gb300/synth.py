@@ -198,3 +198,62 @@ def make_config(index: int, device="cpu", keep_src: bool = True) -> DecodeInputs
         lens = [spec.kv_len] * spec.batch
     return make_inputs(spec.batch, lens, spec.kv_dtype, spec.seed, device=device, keep_src=keep_src)
 
+
+
+@dataclasses.dataclass
+class PagedInputs:
+    """A paged copy of a DecodeInputs cache: the same rows, stored in shuffled physical pages."""
+    q: torch.Tensor
+    kv: torch.Tensor                # [num_pages * page_size, row width] (same encoding as the source)
+    kv_scale: Optional[torch.Tensor]  # None | fp32 [1] | uint8 [num_pages * page_size, 18]
+    page_indptr: torch.Tensor       # int32 [batch + 1]
+    page_indices: torch.Tensor      # int32 [sum of pages]
+    last_page_len: torch.Tensor     # int32 [batch]
+    page_size: int
+    kv_dtype: int
+    lens: List[int]
+
+    def to(self, device) -> "PagedInputs":
+        mv = lambda t: None if t is None else t.to(device)
+        return PagedInputs(mv(self.q), mv(self.kv), mv(self.kv_scale), mv(self.page_indptr), mv(self.page_indices),
+                           mv(self.last_page_len), self.page_size, self.kv_dtype, list(self.lens))
+
+
+def to_paged(inp: DecodeInputs, page_size: int, seed: int, spare_pages: int = 3) -> PagedInputs:
+    """Store the rows of `inp` in pages of `page_size` rows at shuffled physical page numbers
+    (plus `spare_pages` unused pages).  Rows of a page past a sequence's end, and the spare
+    pages, hold other rows of the same cache (valid encodings, so that nothing read there is
+    NaN) -- the decode must mask them."""
+    g = torch.Generator()
+    g.manual_seed(seed)
+    ip = inp.kv_indptr.cpu().tolist()
+    kv = inp.kv.cpu()
+    sc = inp.kv_scale.cpu() if inp.kv_scale is not None else None
+    rows = max(int(ip[-1]), 1)
+    npages = [(int(ip[b + 1] - ip[b]) + page_size - 1) // page_size for b in range(inp.batch)]
+    total = sum(npages) + spare_pages
+    perm = torch.randperm(total, generator=g)
+    filler = torch.randint(0, rows, (total * page_size,), generator=g)
+    kv_pages = kv[filler].clone() if ip[-1] > 0 else torch.zeros((total * page_size,) + tuple(kv.shape[1:]), dtype=kv.dtype)
+    sc_pages = None
+    if inp.kv_dtype == KV_MXFP4:
+        sc_pages = sc[filler].clone() if ip[-1] > 0 else torch.full((total * page_size, MX_SCALES), 127, dtype=torch.uint8)
+    elif sc is not None:
+        sc_pages = sc.clone()
+    indices, indptr, last = [], [0], []
+    k = 0
+    for b in range(inp.batch):
+        L = int(ip[b + 1] - ip[b])
+        for j in range(npages[b]):
+            pid = int(perm[k]); k += 1
+            n = min(page_size, L - j * page_size)
+            src = slice(int(ip[b]) + j * page_size, int(ip[b]) + j * page_size + n)
+            kv_pages[pid * page_size:pid * page_size + n] = kv[src]
+            if inp.kv_dtype == KV_MXFP4:
+                sc_pages[pid * page_size:pid * page_size + n] = sc[src]
+            indices.append(pid)
+        indptr.append(len(indices))
+        last.append(L - (npages[b] - 1) * page_size if npages[b] else 0)
+    return PagedInputs(inp.q.cpu(), kv_pages, sc_pages, torch.tensor(indptr, dtype=torch.int32),
+                       torch.tensor(indices if indices else [0], dtype=torch.int32),
+                       torch.tensor(last, dtype=torch.int32), page_size, inp.kv_dtype, list(inp.lens))

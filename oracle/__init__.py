@@ -17,6 +17,9 @@ Functions and what pins each one (see ``tests/test_oracle.py``):
   their decoded values) and the pages' 0.1/0.1 quantisation tolerance.
 * ``combine`` -- the merge of per-range partial results reproduces the full-range result.
 * ``split_range`` -- the ranges of all splits tile [0, L) in BN-rounded chunks.
+* ``paged_rows`` / ``decode_paged`` -- a hand-written page table's row lists; an identity
+  page table reproduces the contiguous decode; a shuffled one gives the same result as
+  the contiguous cache it was built from.
 """
 from __future__ import annotations
 
@@ -164,6 +167,43 @@ def decode(q, kv, kv_scale, kv_indptr, kv_dtype, nthreads: int = 0):
     if rc:
         raise MemoryError("oracle decode failed")
     return out, lse
+
+
+def paged_rows(page_indptr, page_indices, last_page_len, page_size: int):
+    """Physical cache rows of every sequence of a paged cache, in token order.
+
+    The page table of the paged MLA decode interface (amd-mixed-mla submission 700955,
+    persistent-state setup; submission 701211 harness inputs): sequence b owns the pages
+    page_indices[page_indptr[b] : page_indptr[b+1]], all full except the last, which holds
+    last_page_len[b] tokens.  Token t of sequence b therefore lives at physical row
+    page_indices[page_indptr[b] + t // page_size] * page_size + t % page_size.
+    Returns a list of int64 arrays, one per sequence."""
+    ip = _np(page_indptr, np.int64)
+    pi = _np(page_indices, np.int64)
+    last = _np(last_page_len, np.int64)
+    seqs = []
+    for b in range(len(last)):
+        pages = pi[ip[b]:ip[b + 1]]
+        L = (len(pages) - 1) * page_size + last[b] if len(pages) else 0
+        rows = [int(pages[t // page_size]) * page_size + t % page_size for t in range(L)]
+        seqs.append(np.asarray(rows, dtype=np.int64))
+    return seqs
+
+
+def decode_paged(q, kv, kv_scale, page_indptr, page_indices, last_page_len, page_size: int, kv_dtype,
+                 nthreads: int = 0):
+    """Whole decode over a paged cache -> (out fp64 [B, 16, 512], lse fp64 [B, 16]).
+    Each sequence's rows are gathered in token order (``paged_rows``) into a contiguous
+    cache (with their MXFP4 block scales; the fp8 scale is per tensor) and decoded there."""
+    seqs = paged_rows(page_indptr, page_indices, last_page_len, page_size)
+    idx = np.concatenate(seqs) if seqs else np.zeros((0,), np.int64)
+    indptr = np.zeros((len(seqs) + 1,), dtype=np.int32)
+    indptr[1:] = np.cumsum([len(r) for r in seqs])
+    k, s = _kv_args(kv, kv_scale, kv_dtype)
+    k = np.ascontiguousarray(k[idx]) if len(idx) else np.zeros((1,) + k.shape[1:], k.dtype)
+    if kv_dtype == KV_MXFP4:
+        s = np.ascontiguousarray(s[idx]) if len(idx) else np.zeros((1,) + s.shape[1:], s.dtype)
+    return decode(q, k, s, indptr, kv_dtype, nthreads)
 
 
 def combine(o_parts, lse_parts):

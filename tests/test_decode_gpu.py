@@ -238,3 +238,60 @@ def test_mxfp4_short_segments_repeated(pkg, lens):
         torch.cuda.synchronize()
         assert pkg.device_status(clear=True) == pkg.MLA_OK
         _check(out, ref, f"lens {lens} repetition {rep}")
+
+
+# ----------------------------------------------------------------------------- paged cache
+
+PAGED_LENS = [1, 129, 0, 1000, 2048, 64, 65, 127, 128]
+
+
+@pytest.mark.parametrize("kv_dtype", DTYPES)
+@pytest.mark.parametrize("page_size", [64, 128])
+@pytest.mark.parametrize("ns", [1, 2, 3, 0])
+def test_paged_cache_matches_oracle(pkg, kv_dtype, page_size, ns):
+    """Shuffled physical pages, partial last pages, empty and single-token sequences; the
+    oracle decodes the same pages through its own page-table gather."""
+    inp = synth.make_inputs(len(PAGED_LENS), PAGED_LENS, kv_dtype, seed=80 + kv_dtype)
+    pg = synth.to_paged(inp, page_size, seed=90 + page_size)
+    ref, _ = oracle.decode_paged(pg.q, pg.kv, pg.kv_scale, pg.page_indptr, pg.page_indices,
+                                 pg.last_page_len, page_size, kv_dtype)
+    g = pg.to("cuda")
+    out = pkg.decode_paged(g.q, g.kv, g.kv_scale, g.page_indptr, g.page_indices, g.last_page_len, page_size,
+                           kv_dtype, num_splits=ns)
+    torch.cuda.synchronize()
+    assert pkg.device_status(clear=True) == pkg.MLA_OK
+    _check(out, ref, f"paged P={page_size} ns={ns}")
+
+
+@pytest.mark.parametrize("kv_dtype", [synth.KV_FP8, synth.KV_MXFP4])
+def test_paged_workload_sampled_rows(pkg, kv_dtype):
+    """A full-size workload (64 x 8192 tokens) in shuffled 64-row pages at the bench's split
+    count; sampled batch rows against the oracle."""
+    B, L = 64, 8192
+    inp = synth.make_inputs(B, [L] * B, kv_dtype, seed=1236)
+    pg = synth.to_paged(inp, 64, seed=1243)
+    g = pg.to("cuda")
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    ns = max(1, sms // B)
+    out = pkg.decode_paged(g.q, g.kv, g.kv_scale, g.page_indptr, g.page_indices, g.last_page_len, 64,
+                           kv_dtype, num_splits=ns)
+    torch.cuda.synchronize()
+    assert pkg.device_status(clear=True) == pkg.MLA_OK
+    rows = [0, 17, B - 1]
+    sub_indptr = torch.tensor([0] + np.cumsum([int(pg.page_indptr[b + 1] - pg.page_indptr[b]) for b in rows]).tolist(),
+                              dtype=torch.int32)
+    sub_pages = torch.cat([pg.page_indices[int(pg.page_indptr[b]):int(pg.page_indptr[b + 1])] for b in rows])
+    ref, _ = oracle.decode_paged(pg.q[rows], pg.kv, pg.kv_scale, sub_indptr, sub_pages, pg.last_page_len[rows], 64,
+                                 kv_dtype)
+    for i, b in enumerate(rows):
+        _check(out[b], ref[i], f"paged workload row {b}")
+
+
+def test_paged_rejects_bad_page_size(pkg):
+    inp = synth.make_inputs(2, [100, 3], synth.KV_FP8, seed=5)
+    pg = synth.to_paged(inp, 64, seed=6).to("cuda")
+    out = torch.empty((2, 16, 512), dtype=torch.bfloat16, device="cuda")
+    for ps in (0, 32, 256):
+        rc = pkg.mla_decode_paged(pg.q, pg.kv, pg.kv_scale, pg.page_indptr, pg.page_indices, pg.last_page_len, ps,
+                                  out, 2, 1, synth.KV_FP8)
+        assert rc == pkg.MLA_ERR_INVALID_ARG

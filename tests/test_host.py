@@ -70,6 +70,30 @@ def test_argument_checks_precede_any_device_work(lib):
     assert _call(lib, ns=4097) == INV
 
 
+def _call_paged(lib, q=256, kv=512, scale=1024, ip=2048, pi=3072, last=3584, ps=64, out=4096, batch=2, ns=0,
+                dtype=1):
+    vp = ctypes.c_void_p
+    a = lambda x: vp(x) if x else None
+    return lib.mla_decode_paged(a(q), a(kv), a(scale), a(ip), a(pi), a(last), ps, a(out), batch, ns, dtype, None)
+
+
+def test_paged_argument_checks_precede_any_device_work(lib):
+    INV = -1
+    for ps in (0, 1, 16, 32, 96, 256, -64):
+        assert _call_paged(lib, ps=ps) == INV          # page size must be 64 or 128
+    assert _call_paged(lib, pi=0) == INV
+    assert _call_paged(lib, last=0) == INV
+    assert _call_paged(lib, ip=0) == INV
+    assert _call_paged(lib, pi=3074) == INV             # page list not 4-byte aligned
+    assert _call_paged(lib, last=3586) == INV
+    assert _call_paged(lib, q=258) == INV
+    assert _call_paged(lib, kv=520) == INV
+    assert _call_paged(lib, scale=0, dtype=2) == INV
+    assert _call_paged(lib, batch=0) == INV
+    assert _call_paged(lib, ns=4097) == INV
+    assert _call_paged(lib, dtype=3) == INV
+
+
 def test_valid_call_without_a_gpu_fails_cleanly(lib):
     try:
         import torch
@@ -79,6 +103,7 @@ def test_valid_call_without_a_gpu_fails_cleanly(lib):
         pass
     rc = _call(lib, scale=0, dtype=0)
     assert rc in (-2, -3)  # MLA_ERR_UNSUPPORTED or MLA_ERR_CUDA, never a crash
+    assert _call_paged(lib, ps=128) in (-2, -3)
 
 
 @pytest.mark.parametrize("dtype", [0, 1, 2])

@@ -296,3 +296,37 @@ def test_quantised_cache_within_pages_tolerance_of_bf16_source(kv_dtype, lens):
     oq, _ = oracle.decode(inp.q, inp.kv, inp.kv_scale, inp.kv_indptr, kv_dtype)
     ob, _ = oracle.decode(inp.q, inp.kv_src, None, inp.kv_indptr, synth.KV_BF16)
     np.testing.assert_allclose(oq, ob, rtol=0.1, atol=0.1)
+
+
+# ----------------------------------------------------------------------------- paged cache
+
+def test_paged_rows_of_a_hand_written_page_table():
+    # page size 4; sequence 0 owns pages 5 then 1 (3 tokens in page 1), sequence 1 has no
+    # pages, sequence 2 owns page 0 in full.
+    seqs = oracle.paged_rows(np.array([0, 2, 2, 3], np.int32), np.array([5, 1, 0], np.int32),
+                             np.array([3, 4, 4], np.int32), 4)
+    assert [s.tolist() for s in seqs] == [[20, 21, 22, 23, 4, 5, 6], [], [0, 1, 2, 3]]
+
+
+@pytest.mark.parametrize("kv_dtype", [synth.KV_BF16, synth.KV_FP8, synth.KV_MXFP4])
+def test_identity_page_table_reproduces_the_contiguous_decode(kv_dtype):
+    # Lengths 8 and 7 at page size 4: the contiguous cache already is pages 0-1 and 2-3.
+    inp = synth.make_inputs(2, [8, 7], kv_dtype, seed=34)
+    o1, l1 = oracle.decode(inp.q, inp.kv, inp.kv_scale, inp.kv_indptr, kv_dtype)
+    o2, l2 = oracle.decode_paged(inp.q, inp.kv, inp.kv_scale, np.array([0, 2, 4], np.int32),
+                                 np.array([0, 1, 2, 3], np.int32), np.array([4, 3], np.int32), 4, kv_dtype)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(l1, l2)
+
+
+@pytest.mark.parametrize("kv_dtype", [synth.KV_BF16, synth.KV_FP8, synth.KV_MXFP4])
+@pytest.mark.parametrize("page_size", [64, 128])
+def test_shuffled_pages_give_the_contiguous_result(kv_dtype, page_size):
+    inp = synth.make_inputs(4, [1, 130, 0, 257], kv_dtype, seed=35)
+    pg = synth.to_paged(inp, page_size, seed=36)
+    assert pg.page_indices.tolist() != sorted(pg.page_indices.tolist())   # pages out of order
+    o1, l1 = oracle.decode(inp.q, inp.kv, inp.kv_scale, inp.kv_indptr, kv_dtype)
+    o2, l2 = oracle.decode_paged(pg.q, pg.kv, pg.kv_scale, pg.page_indptr, pg.page_indices,
+                                 pg.last_page_len, page_size, kv_dtype)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(l1, l2)
