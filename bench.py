@@ -53,7 +53,7 @@ def parse():
                     help="timed steps only (no clock soak, e2e or CPU baseline); for profiler runs")
     ap.add_argument("--page-size", type=int, default=0, choices=[0, 64, 128],
                     help="with --quick: store the workload's cache in shuffled pages of this many rows "
-                         "and time mla_decode_paged (uniform splits)")
+                         "and time mla_decode_paged")
     return ap.parse_args()
 
 
@@ -289,8 +289,6 @@ def main():
         kv_bytes = inp.kv_bytes()
         inp.kv = None                    # free the contiguous copy
         torch.cuda.empty_cache()
-        if ns < 1:                       # a paged cache takes uniform splits only
-            ns = max(1, min(sms // B, 4096))
     pkg.reserve_workspace(pkg.workspace_slots(B, ns, sms))
     out = torch.empty((B, 16, 512), dtype=torch.bfloat16, device=dev)
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)

@@ -107,8 +107,11 @@ int mla_decode(const void* q, const void* kv, const void* kv_scale, const int32_
  *                   1 .. page_size (ignored for a sequence with no pages, which has length 0).
  *                   Sequence b has (npages_b - 1) * page_size + kv_last_page_len[b] tokens.
  *  page_size        64 or 128.
- *  num_splits       >= 1: uniform splits as mla_decode; <= 0: min(floor(SMs / batch), 4096),
- *                   at least 1, uniform splits (there is no balanced mode for paged caches).
+ *  num_splits       as mla_decode.  In the balanced mode (<= 0) the token positions are
+ *                   those of the page space (sequence b starts at kv_page_indptr[b] *
+ *                   page_size; the unused rows of its last page belong to no CTA's work)
+ *                   and the CTAs' cut points are rounded down to multiples of 128, so that
+ *                   every 128-token tile starts on a page boundary.
  * Every page number times page_size plus page_size must be a row inside kv, and every
  * index read must lie inside kv_page_indices; violations are undefined behaviour, as with
  * kv_indptr.  Errors: as mla_decode, plus MLA_ERR_INVALID_ARG for a page_size other than

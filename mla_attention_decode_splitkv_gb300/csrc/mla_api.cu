@@ -6,7 +6,6 @@
 #include <cstdint>
 #include <cstdio>
 #include <cstdlib>
-#include <algorithm>
 #include <mutex>
 #include <vector>
 
@@ -252,7 +251,6 @@ static int decode_impl(const void* q, const void* kv, const void* kv_scale, cons
   if (cc != 103) return MLA_ERR_UNSUPPORTED;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   int ns = num_splits >= 1 ? num_splits : 0;
-  if (page_size != 0 && ns == 0) ns = std::max(1, std::min(sms / batch, mla::kMaxSplits));   // paged: uniform only
   const long long grid_ll = ns >= 1 ? static_cast<long long>(batch) * ns : sms;
   if (grid_ll > 0x7fffffffLL) return MLA_ERR_INVALID_ARG;
 

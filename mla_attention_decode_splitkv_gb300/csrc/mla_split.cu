@@ -32,6 +32,7 @@
 // all roles leave their loops; in-flight copies and MMAs are drained (bounded) before the
 // tensor memory is released.
 #include <cstddef>
+#include <type_traits>
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -186,15 +187,25 @@ __device__ __forceinline__ int balanced_ctas(long long total, int G) {
   if (need < 1) need = 1;
   return static_cast<int>(need < G ? need : G);
 }
+// Paged cache: positions are rows of the page space (page-list entry i covers positions
+// [i P, (i + 1) P)), and the cut points are rounded down to multiples of 128 so that every
+// tile starts on a page boundary.  Consecutive cut points stay more than 128 apart (each
+// CTA is given at least 256 positions before rounding), so no range is empty.
+template <bool PG>
 __device__ __forceinline__ long long cta_lo(int c, long long total, int Ge) {
+  if constexpr (PG) {
+    if (c >= Ge) return total;
+    return static_cast<long long>(c) * total / Ge / kBN * kBN;
+  }
   return static_cast<long long>(c) * total / Ge;
 }
 // Largest CTA index whose range starts at or before token x.
+template <bool PG>
 __device__ __forceinline__ int cta_of_token(long long x, long long total, int Ge) {
   int lo = 0, hi = Ge - 1;
   while (lo < hi) {
     int mid = (lo + hi + 1) >> 1;
-    if (cta_lo(mid, total, Ge) <= x) lo = mid; else hi = mid - 1;
+    if (cta_lo<PG>(mid, total, Ge) <= x) lo = mid; else hi = mid - 1;
   }
   return lo;
 }
@@ -247,8 +258,8 @@ struct SegIter {
     uniform = false;
     int Ge = balanced_ctas(total, p.num_ctas);
     if (c >= Ge) { done = true; return; }
-    lo = cta_lo(c, total, Ge);
-    hi = cta_lo(c + 1, total, Ge);
+    lo = cta_lo<PG>(c, total, Ge);
+    hi = cta_lo<PG>(c + 1, total, Ge);
     last_cta = (c == Ge - 1);
     b = b0;
   }
@@ -275,18 +286,27 @@ struct SegIter {
     // belongs to the CTA with lo <= x < hi (the last CTA also owns x == total); it is
     // returned as an empty direct segment so that its output row gets written as zeros.
     while (b < p.batch) {
-      int r0 = p.kv_indptr[b], r1 = p.kv_indptr[b + 1];
+      // [r0, r1): the sequence's positions (paged: its tokens in the page space; the rest
+      // of its last page belongs to no sequence).  row0: its first cache row (paged: its
+      // first page-list entry).
+      using Pos = typename std::conditional<PG, long long, int>::type;
+      Pos r0 = p.kv_indptr[b], r1 = p.kv_indptr[b + 1];
+      const int row0 = static_cast<int>(r0);
+      if constexpr (PG) {
+        r1 = r1 > r0 ? r0 * p.page_size + (r1 - r0 - 1) * p.page_size + p.last_page_len[b] : r0 * p.page_size;
+        r0 *= p.page_size;
+      }
       if (r0 > hi || (r0 == hi && !last_cta)) break;
       int bb = b++;
       if (r1 > r0) {
         long long a = lo > r0 ? lo : r0, e = hi < r1 ? hi : r1;
         if (e > a) {
-          s.b = bb; s.row0 = r0; s.n_lo = (int)(a - r0); s.n_hi = (int)(e - r0); s.n_total = r1 - r0;
+          s.b = bb; s.row0 = row0; s.n_lo = (int)(a - r0); s.n_hi = (int)(e - r0); s.n_total = (int)(r1 - r0);
           s.slot = bb + cta; s.direct = (a == r0 && e == r1);
           return true;
         }
       } else if (r0 >= lo && (r0 < hi || last_cta)) {
-        s.b = bb; s.row0 = r0; s.n_lo = 0; s.n_hi = 0; s.n_total = 0; s.slot = bb + cta; s.direct = true;
+        s.b = bb; s.row0 = row0; s.n_lo = 0; s.n_hi = 0; s.n_total = 0; s.slot = bb + cta; s.direct = true;
         return true;
       }
     }
@@ -305,21 +325,29 @@ struct Window {
   int y1;     // paged: first cached row of the window's second half (page size 64)
 };
 // Contiguous cache: the window ends at the segment's last row (rows before cached row 0 are
-// the TMA's zero fill).  Paged cache (uniform splits, tiles start at multiples of 128 tokens
-// of the sequence, hence on page boundaries): window row i is token 128 t + i; its first
-// half is page (128 t) / P of the sequence, its second half (P = 64) the next page, or the
+// the TMA's zero fill).  Paged cache (tiles start on page boundaries: the segment starts on
+// one, and a tile is 128 tokens): window row i is token start + i of the sequence; its first
+// half is page start / P of the sequence, its second half (P = 64) the next page, or the
 // same page again when the sequence has no next page (rows that are masked).
-template <int KV, bool PG>
+// ROWS = false: only shift and cnt are wanted (no page-list loads).
+template <bool PG>
+__device__ __forceinline__ int paged_entry(const DecodeParams& p, const Seg& s, int t, int i) {
+  const int P = p.page_size;
+  const int np = (s.n_total + P - 1) / P;
+  return p.page_indices[s.row0 + min((s.n_lo + t * kBN + i) / P, np - 1)];
+}
+template <int KV, bool PG, bool ROWS = true>
 __device__ __forceinline__ Window tile_window(const DecodeParams& p, const Seg& s, int t) {
   Window w;
   if constexpr (PG) {
     const int start = s.n_lo + t * kBN;
     const int P = p.page_size;
-    const int np = (s.n_total + P - 1) / P;
-    const int pg0 = start / P;
-    const int pg1 = (P == kBN || pg0 + 1 >= np) ? pg0 : pg0 + 1;
-    w.y0 = p.page_indices[s.row0 + pg0] * P;
-    w.y1 = p.page_indices[s.row0 + pg1] * P + (P == kBN ? kBN / 2 : 0);
+    if constexpr (ROWS) {
+      w.y0 = paged_entry<PG>(p, s, t, 0) * P;
+      w.y1 = paged_entry<PG>(p, s, t, kBN / 2) * P + (P == kBN ? kBN / 2 : 0);
+    } else {
+      w.y0 = w.y1 = 0;
+    }
     w.shift = 0;
     w.cnt = min(kBN, s.n_hi - start);
   } else {
@@ -862,14 +890,20 @@ __device__ void run_mma_pv(const DecodeParams& p, SharedState* sh, const Descs& 
 
 // ---------------------------------------------------------------- softmax / epilogue (128 threads)
 // Pieces (partial results) of sequence b and their first workspace slot.
+template <bool PG>
 __device__ __forceinline__ int seq_pieces(const DecodeParams& p, int b, long long total, int* slot0) {
   if (p.num_splits >= 1) {
     *slot0 = b * p.num_splits;
     return p.num_splits;
   }
   const int Ge = balanced_ctas(total, p.num_ctas);
-  const int cf = cta_of_token(p.kv_indptr[b], total, Ge);
-  const int cl = cta_of_token(static_cast<long long>(p.kv_indptr[b + 1]) - 1, total, Ge);
+  long long r0 = p.kv_indptr[b], r1 = p.kv_indptr[b + 1];   // a merged sequence is non-empty
+  if constexpr (PG) {
+    r1 = r0 * p.page_size + (r1 - r0 - 1) * p.page_size + p.last_page_len[b];
+    r0 *= p.page_size;
+  }
+  const int cf = cta_of_token<PG>(r0, total, Ge);
+  const int cl = cta_of_token<PG>(r1 - 1, total, Ge);
   *slot0 = b + cf;
   return cl - cf + 1;
 }
@@ -1048,13 +1082,13 @@ __device__ void merge_pieces(const DecodeParams& p, int b, int slot0, int pieces
 // After this CTA wrote its piece of sequence s.b: count the piece; the CTA whose piece
 // completes the count merges all pieces and re-arms the counter for the next call.
 // Reached by all `nt` softmax threads.
-template <int KV>
+template <int KV, bool PG>
 __device__ void finish_piece(const DecodeParams& p, SharedState* sh, const Seg& s, int ts, int nt) {
   __threadfence();
   bar_sync(1, nt);
   if (ts == 0) {
     int slot0 = 0;
-    const int pieces = seq_pieces(p, s.b, sh->seg_total, &slot0);
+    const int pieces = seq_pieces<PG>(p, s.b, sh->seg_total, &slot0);
     const int old = atomicAdd(p.seq_count + s.b, 1);
     const bool last = (old == pieces - 1);
     if (last) {
@@ -1127,7 +1161,7 @@ __device__ void run_softmax(const DecodeParams& p, SharedState* sh, uint8_t* qs,
     const int n = cur.n_hi - cur.n_lo;
     if (n <= 0) {
       write_empty_result<KV>(p, cur, ts);
-      if (!cur.direct) finish_piece<KV>(p, sh, cur, ts, NT);
+      if (!cur.direct) finish_piece<KV, PG>(p, sh, cur, ts, NT);
       has_cur = it.next(p, cur);
       continue;
     }
@@ -1138,7 +1172,7 @@ __device__ void run_softmax(const DecodeParams& p, SharedState* sh, uint8_t* qs,
     float mref[H], lpart[H];
     bool has_nxt = false;
     for (int t = 0; t < ntiles; ++t) {
-      const Window w = tile_window<KV, PG>(p, cur, t);
+      const Window w = tile_window<KV, PG, false>(p, cur, t);
       bool okw = wait_bar(smem_u32(&sh->s_full[g & 1]), (g >> 1) & 1, abortf, p.status, p.wait_limit_ns);
       okw = __all_sync(0xffffffffu, okw);
       tc_fence_after();
@@ -1337,7 +1371,7 @@ __device__ void run_softmax(const DecodeParams& p, SharedState* sh, uint8_t* qs,
     }
     tc_fence_before();
     warp_arrive(smem_u32(&sh->o_free));
-    if (!cur.direct) finish_piece<KV>(p, sh, cur, ts, NT);
+    if (!cur.direct) finish_piece<KV, PG>(p, sh, cur, ts, NT);
     cur = nxt;
     has_cur = has_nxt;
   }
@@ -1394,11 +1428,15 @@ __global__ void __launch_bounds__(Cfg<KV>::kThreads, 1) mla_split_kernel(const _
     tmem_relinquish();
   }
   if (warp == 0 && p.num_splits < 1) {
-    const long long total = p.kv_indptr[p.batch];
+    const long long total = static_cast<long long>(p.kv_indptr[p.batch]) * (PG ? p.page_size : 1);
     const int Ge = balanced_ctas(total, p.num_ctas);
     int b0 = p.batch;
-    // first b with kv_indptr[b+1] >= lo: empty sequences sitting at lo are this CTA's too
-    if (static_cast<int>(blockIdx.x) < Ge) b0 = warp_first_seq(p.kv_indptr, p.batch, cta_lo(blockIdx.x, total, Ge) - 1);
+    // first b with kv_indptr[b+1] >= lo (paged: kv_indptr[b+1] * P >= lo): empty sequences
+    // sitting at lo are this CTA's too
+    if (static_cast<int>(blockIdx.x) < Ge) {
+      const long long lo = cta_lo<PG>(blockIdx.x, total, Ge);
+      b0 = warp_first_seq(p.kv_indptr, p.batch, PG ? (lo + p.page_size - 1) / p.page_size - 1 : lo - 1);
+    }
     if (lane == 0) { sh->seg_total = total; sh->seg_b0 = b0; }
   }
   tc_fence_before();

@@ -264,15 +264,16 @@ def test_paged_cache_matches_oracle(pkg, kv_dtype, page_size, ns):
 
 
 @pytest.mark.parametrize("kv_dtype", [synth.KV_FP8, synth.KV_MXFP4])
-def test_paged_workload_sampled_rows(pkg, kv_dtype):
-    """A full-size workload (64 x 8192 tokens) in shuffled 64-row pages at the bench's split
-    count; sampled batch rows against the oracle."""
+@pytest.mark.parametrize("balanced", [False, True])
+def test_paged_workload_sampled_rows(pkg, kv_dtype, balanced):
+    """A full-size workload (64 x 8192 tokens) in shuffled 64-row pages, in uniform splits
+    (one wave) and in the balanced mode; sampled batch rows against the oracle."""
     B, L = 64, 8192
     inp = synth.make_inputs(B, [L] * B, kv_dtype, seed=1236)
     pg = synth.to_paged(inp, 64, seed=1243)
     g = pg.to("cuda")
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    ns = max(1, sms // B)
+    ns = 0 if balanced else max(1, sms // B)
     out = pkg.decode_paged(g.q, g.kv, g.kv_scale, g.page_indptr, g.page_indices, g.last_page_len, 64,
                            kv_dtype, num_splits=ns)
     torch.cuda.synchronize()
@@ -295,3 +296,24 @@ def test_paged_rejects_bad_page_size(pkg):
         rc = pkg.mla_decode_paged(pg.q, pg.kv, pg.kv_scale, pg.page_indptr, pg.page_indices, pg.last_page_len, ps,
                                   out, 2, 1, synth.KV_FP8)
         assert rc == pkg.MLA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kv_dtype", DTYPES)
+@pytest.mark.parametrize("page_size", [64, 128])
+def test_paged_balanced_ragged_batch(pkg, kv_dtype, page_size):
+    """The balanced mode over a paged ragged batch: runs of empty and one-page sequences
+    between long ones, so that CTA ranges start and end inside sequences, at page ends
+    and on empty sequences."""
+    rng = np.random.default_rng(page_size + kv_dtype)
+    lens = [int(x) for x in rng.choice([0, 1, 63, 64, 65, 127, 128, 129, 700, 3000], size=60)]
+    inp = synth.make_inputs(len(lens), lens, kv_dtype, seed=300 + kv_dtype)
+    pg = synth.to_paged(inp, page_size, seed=301 + page_size)
+    ref, _ = oracle.decode_paged(pg.q, pg.kv, pg.kv_scale, pg.page_indptr, pg.page_indices,
+                                 pg.last_page_len, page_size, kv_dtype)
+    g = pg.to("cuda")
+    for rep in range(3 if kv_dtype == synth.KV_MXFP4 else 1):
+        out = pkg.decode_paged(g.q, g.kv, g.kv_scale, g.page_indptr, g.page_indices, g.last_page_len, page_size,
+                               kv_dtype, num_splits=0)
+        torch.cuda.synchronize()
+        assert pkg.device_status(clear=True) == pkg.MLA_OK
+        _check(out, ref, f"paged balanced P={page_size} rep {rep}")
