@@ -51,6 +51,8 @@ def parse():
                     help="--impl reference: total oracle time over all warm-up and timed steps")
     ap.add_argument("--quick", action="store_true",
                     help="timed steps only (no clock soak, e2e or CPU baseline); for profiler runs")
+    ap.add_argument("--q-len", type=int, default=1,
+                    help="with --page-size: query tokens per sequence (mla_decode_paged_multi when > 1)")
     ap.add_argument("--page-size", type=int, default=0, choices=[0, 64, 128],
                     help="with --quick: store the workload's cache in shuffled pages of this many rows "
                          "and time mla_decode_paged")
@@ -282,15 +284,21 @@ def main():
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     ns = pkg.resolve_splits(spec.num_splits, B, inp.rows // B, sms, spec.kv_dtype)
     paged = None
+    if args.q_len > 1 and not args.page_size:
+        raise SystemExit("--q-len > 1 needs --page-size")
     if args.page_size:
         if not args.quick:
             raise SystemExit("--page-size is a --quick measurement")
+        if args.q_len > 1:
+            ns = max(1, min(sms // (B * args.q_len), 4096))   # the library's multi-query default
         paged = synth.to_paged(inp, args.page_size, seed=spec.seed + 7).to(dev)
+        if args.q_len > 1:
+            mq, mqo = synth.make_queries([args.q_len] * B, seed=spec.seed + 8, device=dev)
         kv_bytes = inp.kv_bytes()
         inp.kv = None                    # free the contiguous copy
         torch.cuda.empty_cache()
-    pkg.reserve_workspace(pkg.workspace_slots(B, ns, sms))
-    out = torch.empty((B, 16, 512), dtype=torch.bfloat16, device=dev)
+    pkg.reserve_workspace(pkg.workspace_slots(B * max(1, args.q_len), ns, sms))
+    out = torch.empty((B * max(1, args.q_len), 16, 512), dtype=torch.bfloat16, device=dev)
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     evict = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     evict_sum = torch.empty((), dtype=torch.float32, device=dev)
@@ -301,7 +309,11 @@ def main():
     stream = torch.cuda.current_stream(dev)
 
     def call():
-        if paged is not None:
+        if paged is not None and args.q_len > 1:
+            rc = pkg.mla_decode_paged_multi(mq, mqo, B * args.q_len, paged.kv, paged.kv_scale, paged.page_indptr,
+                                            paged.page_indices, paged.last_page_len, args.page_size, out, B, ns,
+                                            spec.kv_dtype, stream)
+        elif paged is not None:
             rc = pkg.mla_decode_paged(paged.q, paged.kv, paged.kv_scale, paged.page_indptr, paged.page_indices,
                                       paged.last_page_len, args.page_size, out, B, ns, spec.kv_dtype, stream)
         else:
@@ -348,7 +360,8 @@ def main():
     if args.quick:
         if rank == 0:
             kvb = kv_bytes if paged is not None else inp.kv_bytes()
-            print(json.dumps({"workload": spec.name, "page_size": args.page_size, "num_splits": ns,
+            print(json.dumps({"workload": spec.name, "page_size": args.page_size, "q_len": args.q_len,
+                              "num_splits": ns,
                               "us_per_call": ms * 1e3, "split_kernel_us": split_ms * 1e3,
                               "kv_bytes_per_call": kvb, "split_gbs": kvb / (split_ms * 1e-3) / 1e9}), flush=True)
         return

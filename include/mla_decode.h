@@ -122,6 +122,36 @@ int mla_decode_paged(const void* q, const void* kv, const void* kv_scale, const 
                      int batch, int num_splits, int kv_dtype, void* stream);
 
 /*
+ * mla_decode_paged_multi -- mla_decode_paged with several query tokens per sequence (the
+ * q_len > 1 form of the paged decode interface: the `qo_indptr` argument of the a16w8 path
+ * of amd-mixed-mla submission 700955, which the pages only call with one token per
+ * sequence).  The q_len_b = qo_indptr[b+1] - qo_indptr[b] new tokens of sequence b are the
+ * last q_len_b tokens of its cache (their keys and values already appended), and each sees
+ * the cache up to and including itself: query row qo_indptr[b] + t (0 <= t < q_len_b)
+ * attends to the first L_b - q_len_b + 1 + t cached tokens of sequence b (none if that is
+ * <= 0, which gives zeros).  Every (row, head) is otherwise exactly mla_decode's operation.
+ *
+ *  q            bf16 [total_q][16][576] (device), 16-byte aligned; rows grouped by sequence.
+ *  qo_indptr    int32 [batch+1] (device): qo_indptr[0] = 0, non-decreasing,
+ *               qo_indptr[batch] = total_q (a violation is undefined behaviour).
+ *  total_q      >= 1: query rows.
+ *  out          bf16 [total_q][16][512] (device).
+ *  batch        >= 1: sequences (entries of the page table).
+ *  num_splits   >= 1: uniform splits of each query row's visible range; <= 0: the library's
+ *               choice, max(1, floor(SMs / total_q)) uniform splits (no balanced mode).
+ *  kv, kv_scale, kv_page_indptr, kv_page_indices, kv_last_page_len, page_size, kv_dtype,
+ *  stream: as mla_decode_paged.
+ * Each query row reads its own visible range of the cache (rows of one sequence share the
+ * cache through L2, not in one pass).  Errors: as mla_decode_paged, plus
+ * MLA_ERR_INVALID_ARG for a null or misaligned qo_indptr or total_q <= 0.
+ */
+int mla_decode_paged_multi(const void* q, const int32_t* qo_indptr, int total_q, const void* kv,
+                           const void* kv_scale, const int32_t* kv_page_indptr,
+                           const int32_t* kv_page_indices, const int32_t* kv_last_page_len,
+                           int page_size, void* out, int batch, int num_splits, int kv_dtype,
+                           void* stream);
+
+/*
  * mla_decode_pick_splits -- host-only choice of num_splits for mla_decode.
  *     ns = min(floor(num_sms / batch), ceil(kv_len_hint / 256));  returns ns if ns >= 2,
  *     else 0 (the balanced persistent mode).

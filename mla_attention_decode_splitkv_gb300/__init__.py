@@ -5,9 +5,9 @@ in-tree by ``build.build()``); ``decode`` / ``mla_decode`` here only marshal arg
 ``synth`` makes seeded synthetic inputs.
 """
 from ._lib import (MLA_ERR_CUDA, MLA_ERR_INVALID_ARG, MLA_ERR_NO_MEMORY, MLA_ERR_TIMEOUT,  # noqa: F401
-                   MLA_ERR_UNSUPPORTED, MLA_OK, MLAError, decode, decode_paged, device_status, load, mla_decode,
-                   mla_decode_paged,
-                   pick_splits, profile_begin, profile_end, release_workspace, reserve_workspace, resolve_splits,
-                   set_test_stall, set_wait_limit_ns, workspace_slots)
+                   MLA_ERR_UNSUPPORTED, MLA_OK, MLAError, decode, decode_paged, decode_paged_multi, device_status,
+                   load, mla_decode, mla_decode_paged, mla_decode_paged_multi, pick_splits, profile_begin,
+                   profile_end, release_workspace, reserve_workspace, resolve_splits, set_test_stall,
+                   set_wait_limit_ns, workspace_slots)
 
 KV_BF16, KV_FP8, KV_MXFP4 = 0, 1, 2

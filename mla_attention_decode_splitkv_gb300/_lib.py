@@ -32,6 +32,7 @@ EXPORTED = (
     "mla_decode_profile_end",
     "mla_decode_noalloc",
     "mla_decode_paged",
+    "mla_decode_paged_multi",
     "mla_status_string",
     "mla_last_cuda_error",
 )
@@ -83,6 +84,8 @@ def load(path: str = LIB_PATH):
                                                ctypes.POINTER(c_int)]
         lib.mla_decode_paged.restype = c_int
         lib.mla_decode_paged.argtypes = [vp, vp, vp, vp, vp, vp, c_int, vp, c_int, c_int, c_int, vp]
+        lib.mla_decode_paged_multi.restype = c_int
+        lib.mla_decode_paged_multi.argtypes = [vp, vp, c_int, vp, vp, vp, vp, vp, c_int, vp, c_int, c_int, c_int, vp]
         lib.mla_decode_noalloc.restype = c_int
         lib.mla_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, c_int, c_int, c_int, vp]
         lib.mla_status_string.restype = ctypes.c_char_p
@@ -145,6 +148,30 @@ def decode_paged(q, kv, kv_scale, page_indptr, page_indices, last_page_len, page
                           num_splits, kv_dtype, stream)
     if rc != MLA_OK:
         raise MLAError(rc, "mla_decode_paged")
+    return out
+
+
+def mla_decode_paged_multi(q, qo_indptr, total_q: int, kv, kv_scale, page_indptr, page_indices, last_page_len,
+                           page_size: int, out, batch: int, num_splits: int, kv_dtype: int, stream=None) -> int:
+    """Raw C-ABI call: several query tokens per sequence over a paged cache; returns the mla_status code."""
+    lib = load()
+    return lib.mla_decode_paged_multi(_ptr(q), _ptr(qo_indptr), int(total_q), _ptr(kv), _ptr(kv_scale),
+                                      _ptr(page_indptr), _ptr(page_indices), _ptr(last_page_len), int(page_size),
+                                      _ptr(out), int(batch), int(num_splits), int(kv_dtype), _stream_handle(stream))
+
+
+def decode_paged_multi(q, qo_indptr, kv, kv_scale, page_indptr, page_indices, last_page_len, page_size: int,
+                       kv_dtype: int, num_splits: int = 0, out=None, stream=None):
+    """out [total_q, 16, 512] = causal multi-token MLA decode over a paged cache (GPU tensors); raises MLAError."""
+    import torch
+    total_q = q.shape[0]
+    batch = qo_indptr.shape[0] - 1
+    if out is None:
+        out = torch.empty((total_q, 16, 512), dtype=torch.bfloat16, device=q.device)
+    rc = mla_decode_paged_multi(q, qo_indptr, total_q, kv, kv_scale, page_indptr, page_indices, last_page_len,
+                                page_size, out, batch, num_splits, kv_dtype, stream)
+    if rc != MLA_OK:
+        raise MLAError(rc, "mla_decode_paged_multi")
     return out
 
 

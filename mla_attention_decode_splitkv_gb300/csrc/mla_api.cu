@@ -2,6 +2,7 @@
 // heuristic, the per-device partial-result workspace, tensor-map encoding and launches.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
@@ -228,16 +229,19 @@ int mla_decode_device_status(int clear) {
   return (v & mla::kStatusTimeout) ? MLA_ERR_TIMEOUT : MLA_OK;
 }
 
-// Shared by mla_decode (page_size 0) and mla_decode_paged.
+// Shared by mla_decode (page_size 0), mla_decode_paged and mla_decode_paged_multi
+// (qo_indptr != null: `batch` counts query rows, `num_seqs` sequences).
 static int decode_impl(const void* q, const void* kv, const void* kv_scale, const int32_t* kv_indptr,
-                       const int32_t* page_indices, const int32_t* last_page_len, int page_size, void* out,
-                       int batch, int num_splits, int kv_dtype, void* stream) {
+                       const int32_t* page_indices, const int32_t* last_page_len, int page_size,
+                       const int32_t* qo_indptr, int num_seqs, void* out, int batch, int num_splits, int kv_dtype,
+                       void* stream) {
   if (q == nullptr || kv == nullptr || kv_indptr == nullptr || out == nullptr) return MLA_ERR_INVALID_ARG;
   if (page_size != 0) {
     if (page_size != 64 && page_size != 128) return MLA_ERR_INVALID_ARG;
     if (page_indices == nullptr || last_page_len == nullptr) return MLA_ERR_INVALID_ARG;
     if (!aligned(page_indices, 4) || !aligned(last_page_len, 4)) return MLA_ERR_INVALID_ARG;
   }
+  if (qo_indptr != nullptr && (page_size == 0 || num_seqs <= 0 || !aligned(qo_indptr, 4))) return MLA_ERR_INVALID_ARG;
   if (batch <= 0 || num_splits > mla::kMaxSplits) return MLA_ERR_INVALID_ARG;
   if (kv_dtype != MLA_KV_BF16 && kv_dtype != MLA_KV_FP8_E4M3 && kv_dtype != MLA_KV_MXFP4) return MLA_ERR_INVALID_ARG;
   if (kv_dtype != MLA_KV_BF16 && kv_scale == nullptr) return MLA_ERR_INVALID_ARG;
@@ -251,6 +255,7 @@ static int decode_impl(const void* q, const void* kv, const void* kv_scale, cons
   if (cc != 103) return MLA_ERR_UNSUPPORTED;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   int ns = num_splits >= 1 ? num_splits : 0;
+  if (qo_indptr != nullptr && ns == 0) ns = std::max(1, std::min(sms / batch, mla::kMaxSplits));   // uniform only
   const long long grid_ll = ns >= 1 ? static_cast<long long>(batch) * ns : sms;
   if (grid_ll > 0x7fffffffLL) return MLA_ERR_INVALID_ARG;
 
@@ -273,6 +278,8 @@ static int decode_impl(const void* q, const void* kv, const void* kv_scale, cons
   p.page_size = page_size;
   p.page_indices = page_indices;
   p.last_page_len = last_page_len;
+  p.qo_indptr = qo_indptr;
+  p.num_seqs = num_seqs;
   p.q = static_cast<const uint16_t*>(q);
   p.kv = static_cast<const uint8_t*>(kv);
   p.kv_scale = kv_scale;
@@ -318,15 +325,25 @@ static int decode_impl(const void* q, const void* kv, const void* kv_scale, cons
 
 int mla_decode(const void* q, const void* kv, const void* kv_scale, const int32_t* kv_indptr, void* out, int batch,
                int num_splits, int kv_dtype, void* stream) {
-  return decode_impl(q, kv, kv_scale, kv_indptr, nullptr, nullptr, 0, out, batch, num_splits, kv_dtype, stream);
+  return decode_impl(q, kv, kv_scale, kv_indptr, nullptr, nullptr, 0, nullptr, 0, out, batch, num_splits, kv_dtype,
+                     stream);
 }
 
 int mla_decode_paged(const void* q, const void* kv, const void* kv_scale, const int32_t* kv_page_indptr,
                      const int32_t* kv_page_indices, const int32_t* kv_last_page_len, int page_size, void* out,
                      int batch, int num_splits, int kv_dtype, void* stream) {
   if (page_size == 0) return MLA_ERR_INVALID_ARG;
-  return decode_impl(q, kv, kv_scale, kv_page_indptr, kv_page_indices, kv_last_page_len, page_size, out, batch,
-                     num_splits, kv_dtype, stream);
+  return decode_impl(q, kv, kv_scale, kv_page_indptr, kv_page_indices, kv_last_page_len, page_size, nullptr, 0, out,
+                     batch, num_splits, kv_dtype, stream);
+}
+
+int mla_decode_paged_multi(const void* q, const int32_t* qo_indptr, int total_q, const void* kv, const void* kv_scale,
+                           const int32_t* kv_page_indptr, const int32_t* kv_page_indices,
+                           const int32_t* kv_last_page_len, int page_size, void* out, int batch, int num_splits,
+                           int kv_dtype, void* stream) {
+  if (page_size == 0 || qo_indptr == nullptr || total_q <= 0 || batch <= 0) return MLA_ERR_INVALID_ARG;
+  return decode_impl(q, kv, kv_scale, kv_page_indptr, kv_page_indices, kv_last_page_len, page_size, qo_indptr, batch,
+                     out, total_q, num_splits, kv_dtype, stream);
 }
 
 int mla_decode_profile_begin(void) {

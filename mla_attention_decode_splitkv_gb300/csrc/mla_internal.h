@@ -40,7 +40,11 @@ struct DecodeParams {
   // Paged cache (mla_decode_paged; 0 / null otherwise): kv_indptr indexes page_indices.
   int page_size;                   // rows per page: 64 or 128
   const int32_t* page_indices;     // [kv_indptr[batch]] physical page of each sequence page
-  const int32_t* last_page_len;    // [batch] rows used in each sequence's last page (1..page_size)
+  const int32_t* last_page_len;    // [sequences] rows used in each sequence's last page (1..page_size)
+  // Several query tokens per sequence (mla_decode_paged_multi; null otherwise, uniform splits
+  // only): batch counts query rows, qo_indptr [num_seqs + 1] maps sequences to query rows.
+  const int32_t* qo_indptr;
+  int num_seqs;
 };
 
 
@@ -56,7 +60,7 @@ int encode_rope_map(CUtensorMap* map, const void* kv);
 
 // Launches the split kernel for kv_dtype (geometry per dtype is internal to mla_split.cu).
 cudaError_t launch_split(int kv_dtype, const DecodeParams& p, int grid, cudaStream_t stream);
-// The same for a paged cache (uniform splits; page size 64 or 128, boxes of page_size rows).
+// The same for a paged cache (page size 64 or 128, boxes of page_size rows).
 cudaError_t launch_split_paged(int kv_dtype, const DecodeParams& p, int grid, cudaStream_t stream);
 // Tensor maps with boxes of `box_rows` rows (paged caches: box_rows = page size).
 int encode_kv_map_rows(CUtensorMap* map, const void* kv, int kv_dtype, int box_rows);

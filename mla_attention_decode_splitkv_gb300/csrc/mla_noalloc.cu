@@ -111,6 +111,8 @@ extern "C" int mla_decode_noalloc(const void* q, const void* kv, const void* kv_
   p.page_size = 0;
   p.page_indices = nullptr;
   p.last_page_len = nullptr;
+  p.qo_indptr = nullptr;
+  p.num_seqs = 0;
   if (mla::launch_split(kv_dtype, p, static_cast<int>(grid), st) != cudaSuccess) { cudaGetLastError(); return MLA_ERR_CUDA; }
   return MLA_OK;
 }

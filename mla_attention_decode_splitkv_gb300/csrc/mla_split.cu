@@ -267,10 +267,31 @@ struct SegIter {
   __device__ bool next(const DecodeParams& p, Seg& s) {
     if (done) return false;
     if (uniform) {
-      int r0 = p.kv_indptr[b];
-      long long L = static_cast<long long>(p.kv_indptr[b + 1]) - r0;
-      if constexpr (PG) {   // r0: the sequence's first entry in the page list
-        L = L > 0 ? (L - 1) * p.page_size + p.last_page_len[b] : 0;
+      int r0;
+      long long L;
+      if constexpr (PG) {
+        // b is a query row.  Several query tokens per sequence (qo_indptr): row b is token
+        // t of the q_len tokens of sequence sb and sees the first L - q_len + 1 + t tokens.
+        int sb = b;
+        if (p.qo_indptr != nullptr) {   // largest sb with qo_indptr[sb] <= b
+          int lo = 0, hi = p.num_seqs - 1;
+          while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (p.qo_indptr[mid] <= b) lo = mid; else hi = mid - 1;
+          }
+          sb = lo;
+        }
+        r0 = p.kv_indptr[sb];           // the sequence's first entry in the page list
+        L = static_cast<long long>(p.kv_indptr[sb + 1]) - r0;
+        L = L > 0 ? (L - 1) * p.page_size + p.last_page_len[sb] : 0;
+        if (p.qo_indptr != nullptr) {
+          const int qn = p.qo_indptr[sb + 1] - p.qo_indptr[sb];
+          L -= qn - 1 - (b - p.qo_indptr[sb]);
+          if (L < 0) L = 0;
+        }
+      } else {
+        r0 = p.kv_indptr[b];
+        L = static_cast<long long>(p.kv_indptr[b + 1]) - r0;
       }
       long long per = (L + ns - 1) / ns;
       long long chunk = ((per + kBN - 1) / kBN) * kBN;

@@ -257,3 +257,13 @@ def to_paged(inp: DecodeInputs, page_size: int, seed: int, spare_pages: int = 3)
     return PagedInputs(inp.q.cpu(), kv_pages, sc_pages, torch.tensor(indptr, dtype=torch.int32),
                        torch.tensor(indices if indices else [0], dtype=torch.int32),
                        torch.tensor(last, dtype=torch.int32), page_size, inp.kv_dtype, list(inp.lens))
+
+
+def make_queries(q_lens, seed: int, device="cpu"):
+    """Several query tokens per sequence: q bf16 [sum(q_lens), 16, 576] ~ N(0, 1) and the
+    int32 qo_indptr [len(q_lens) + 1]."""
+    q_lens = [int(n) for n in q_lens]
+    g = _gen(device, seed)
+    q = torch.randn((max(sum(q_lens), 1), NUM_HEADS, HEAD_DIM), generator=g, device=device,
+                    dtype=torch.float32).to(torch.bfloat16)[:sum(q_lens)]
+    return q, indptr_from_lengths(q_lens).to(device)

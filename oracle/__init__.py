@@ -20,6 +20,9 @@ Functions and what pins each one (see ``tests/test_oracle.py``):
 * ``paged_rows`` / ``decode_paged`` -- a hand-written page table's row lists; an identity
   page table reproduces the contiguous decode; a shuffled one gives the same result as
   the contiguous cache it was built from.
+* ``decode_paged_multi`` -- one token per sequence reproduces ``decode_paged``; each query
+  row of a hand-built two-token case equals the decode of its own hand-cut prefix; a first
+  query token that sees one cached token returns that token's value.
 """
 from __future__ import annotations
 
@@ -199,6 +202,32 @@ def decode_paged(q, kv, kv_scale, page_indptr, page_indices, last_page_len, page
     idx = np.concatenate(seqs) if seqs else np.zeros((0,), np.int64)
     indptr = np.zeros((len(seqs) + 1,), dtype=np.int32)
     indptr[1:] = np.cumsum([len(r) for r in seqs])
+    k, s = _kv_args(kv, kv_scale, kv_dtype)
+    k = np.ascontiguousarray(k[idx]) if len(idx) else np.zeros((1,) + k.shape[1:], k.dtype)
+    if kv_dtype == KV_MXFP4:
+        s = np.ascontiguousarray(s[idx]) if len(idx) else np.zeros((1,) + s.shape[1:], s.dtype)
+    return decode(q, k, s, indptr, kv_dtype, nthreads)
+
+
+def decode_paged_multi(q, qo_indptr, kv, kv_scale, page_indptr, page_indices, last_page_len, page_size: int,
+                       kv_dtype, nthreads: int = 0):
+    """Several query tokens per sequence -> (out fp64 [total_q, 16, 512], lse fp64 [total_q, 16]).
+
+    Reading of the q_len > 1 form of the paged interface (qo_indptr; the pages call it only
+    with one token per sequence): the q_len new tokens of sequence b are the last q_len of
+    its L cached tokens, and query row qo_indptr[b] + t attends causally to the first
+    L - q_len + 1 + t of them (none if that is <= 0).  Each query row is decoded on its own
+    visible rows, gathered in token order by ``paged_rows``."""
+    seqs = paged_rows(page_indptr, page_indices, last_page_len, page_size)
+    qo = _np(qo_indptr, np.int64)
+    vis = []
+    for b in range(len(seqs)):
+        qn = int(qo[b + 1] - qo[b])
+        for t in range(qn):
+            vis.append(seqs[b][:max(0, len(seqs[b]) - qn + 1 + t)])
+    idx = np.concatenate(vis) if vis else np.zeros((0,), np.int64)
+    indptr = np.zeros((len(vis) + 1,), dtype=np.int32)
+    indptr[1:] = np.cumsum([len(r) for r in vis])
     k, s = _kv_args(kv, kv_scale, kv_dtype)
     k = np.ascontiguousarray(k[idx]) if len(idx) else np.zeros((1,) + k.shape[1:], k.dtype)
     if kv_dtype == KV_MXFP4:

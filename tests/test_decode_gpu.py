@@ -317,3 +317,49 @@ def test_paged_balanced_ragged_batch(pkg, kv_dtype, page_size):
         torch.cuda.synchronize()
         assert pkg.device_status(clear=True) == pkg.MLA_OK
         _check(out, ref, f"paged balanced P={page_size} rep {rep}")
+
+
+# ----------------------------------------------------------------------------- several query tokens
+
+MQ_LENS = [1, 129, 0, 1000, 300, 2, 128]
+MQ_QLENS = [1, 2, 3, 4, 0, 3, 2]     # q_len 0, q_len > L (rows that see nothing) included
+
+
+@pytest.mark.parametrize("kv_dtype", DTYPES)
+@pytest.mark.parametrize("page_size", [64, 128])
+@pytest.mark.parametrize("ns", [1, 3, 0])
+def test_paged_multi_query_matches_oracle(pkg, kv_dtype, page_size, ns):
+    inp = synth.make_inputs(len(MQ_LENS), MQ_LENS, kv_dtype, seed=120 + kv_dtype)
+    pg = synth.to_paged(inp, page_size, seed=121)
+    q, qo = synth.make_queries(MQ_QLENS, seed=122)
+    ref, _ = oracle.decode_paged_multi(q, qo, pg.kv, pg.kv_scale, pg.page_indptr, pg.page_indices,
+                                       pg.last_page_len, page_size, kv_dtype)
+    g = pg.to("cuda")
+    out = pkg.decode_paged_multi(q.cuda(), qo.cuda(), g.kv, g.kv_scale, g.page_indptr, g.page_indices,
+                                 g.last_page_len, page_size, kv_dtype, num_splits=ns)
+    torch.cuda.synchronize()
+    assert pkg.device_status(clear=True) == pkg.MLA_OK
+    _check(out, ref, f"multi-query P={page_size} ns={ns}")
+
+
+def test_paged_multi_query_workload_sampled_rows(pkg):
+    """64 sequences x 8192 tokens, fp8, 64-row shuffled pages, two new tokens per sequence
+    (128 query rows) in the library's default split; sampled query rows against the oracle."""
+    B, L = 64, 8192
+    inp = synth.make_inputs(B, [L] * B, synth.KV_FP8, seed=1236)
+    pg = synth.to_paged(inp, 64, seed=1243)
+    q, qo = synth.make_queries([2] * B, seed=1244)
+    g = pg.to("cuda")
+    out = pkg.decode_paged_multi(q.cuda(), qo.cuda(), g.kv, g.kv_scale, g.page_indptr, g.page_indices,
+                                 g.last_page_len, 64, synth.KV_FP8)
+    torch.cuda.synchronize()
+    assert pkg.device_status(clear=True) == pkg.MLA_OK
+    seqs = [0, 33, B - 1]
+    sub_indptr = torch.tensor([0] + np.cumsum([int(pg.page_indptr[b + 1] - pg.page_indptr[b]) for b in seqs]).tolist(),
+                              dtype=torch.int32)
+    sub_pages = torch.cat([pg.page_indices[int(pg.page_indptr[b]):int(pg.page_indptr[b + 1])] for b in seqs])
+    qrows = [r for b in seqs for r in (2 * b, 2 * b + 1)]
+    ref, _ = oracle.decode_paged_multi(q[qrows], torch.tensor([0, 2, 4, 6], dtype=torch.int32), pg.kv, pg.kv_scale,
+                                       sub_indptr, sub_pages, pg.last_page_len[seqs], 64, synth.KV_FP8)
+    for i, r in enumerate(qrows):
+        _check(out[r], ref[i], f"multi-query workload row {r}")

@@ -94,6 +94,28 @@ def test_paged_argument_checks_precede_any_device_work(lib):
     assert _call_paged(lib, dtype=3) == INV
 
 
+def _call_multi(lib, q=256, qo=128, total_q=3, kv=512, scale=1024, ip=2048, pi=3072, last=3584, ps=64, out=4096,
+                batch=2, ns=0, dtype=1):
+    vp = ctypes.c_void_p
+    a = lambda x: vp(x) if x else None
+    return lib.mla_decode_paged_multi(a(q), a(qo), total_q, a(kv), a(scale), a(ip), a(pi), a(last), ps, a(out), batch,
+                                      ns, dtype, None)
+
+
+def test_multi_query_argument_checks_precede_any_device_work(lib):
+    INV = -1
+    assert _call_multi(lib, qo=0) == INV
+    assert _call_multi(lib, qo=130) == INV              # qo_indptr not 4-byte aligned
+    assert _call_multi(lib, total_q=0) == INV
+    assert _call_multi(lib, batch=0) == INV
+    for ps in (0, 32, 256):
+        assert _call_multi(lib, ps=ps) == INV
+    assert _call_multi(lib, pi=0) == INV
+    assert _call_multi(lib, q=258) == INV
+    assert _call_multi(lib, ns=4097) == INV
+    assert _call_multi(lib, dtype=5) == INV
+
+
 def test_valid_call_without_a_gpu_fails_cleanly(lib):
     try:
         import torch
@@ -104,6 +126,7 @@ def test_valid_call_without_a_gpu_fails_cleanly(lib):
     rc = _call(lib, scale=0, dtype=0)
     assert rc in (-2, -3)  # MLA_ERR_UNSUPPORTED or MLA_ERR_CUDA, never a crash
     assert _call_paged(lib, ps=128) in (-2, -3)
+    assert _call_multi(lib) in (-2, -3)
 
 
 @pytest.mark.parametrize("dtype", [0, 1, 2])

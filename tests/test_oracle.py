@@ -330,3 +330,41 @@ def test_shuffled_pages_give_the_contiguous_result(kv_dtype, page_size):
                                  pg.last_page_len, page_size, kv_dtype)
     np.testing.assert_array_equal(o1, o2)
     np.testing.assert_array_equal(l1, l2)
+
+
+def test_multi_query_with_one_token_per_sequence_is_the_paged_decode():
+    inp = synth.make_inputs(3, [5, 0, 9], synth.KV_MXFP4, seed=37)
+    pg = synth.to_paged(inp, 64, seed=38)
+    o1, l1 = oracle.decode_paged(pg.q, pg.kv, pg.kv_scale, pg.page_indptr, pg.page_indices, pg.last_page_len, 64,
+                                 synth.KV_MXFP4)
+    o2, l2 = oracle.decode_paged_multi(pg.q, np.array([0, 1, 2, 3], np.int32), pg.kv, pg.kv_scale, pg.page_indptr,
+                                       pg.page_indices, pg.last_page_len, 64, synth.KV_MXFP4)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(l1, l2)
+
+
+@pytest.mark.parametrize("kv_dtype", [synth.KV_BF16, synth.KV_FP8])
+def test_multi_query_rows_see_their_causal_prefix(kv_dtype):
+    # Page size 4, one sequence of 6 tokens in pages 1 then 0, three new tokens: the query
+    # rows see 4, 5 and 6 tokens.  Each is checked against the contiguous decode of its
+    # prefix (rows 4..7 of the cache, then 0..1).
+    inp = synth.make_inputs(1, [8], kv_dtype, seed=39)
+    q, qo = synth.make_queries([3], seed=40)
+    out, _ = oracle.decode_paged_multi(q, qo, inp.kv, inp.kv_scale, np.array([0, 2], np.int32),
+                                       np.array([1, 0], np.int32), np.array([2], np.int32), 4, kv_dtype)
+    order = [4, 5, 6, 7, 0, 1]
+    for t, n in enumerate([4, 5, 6]):
+        kv = inp.kv[order[:n]].contiguous()
+        ref, _ = oracle.decode(q[t:t + 1], kv, inp.kv_scale, np.array([0, n], np.int32), kv_dtype)
+        np.testing.assert_array_equal(out[t], ref[0])
+
+
+def test_multi_query_first_token_seeing_one_row_returns_its_value():
+    # L = q_len = 3: the first query row sees exactly the first cached token.
+    inp = synth.make_inputs(1, [3], synth.KV_FP8, seed=41)
+    q, qo = synth.make_queries([3], seed=42)
+    out, _ = oracle.decode_paged_multi(q, qo, inp.kv, inp.kv_scale, np.array([0, 1], np.int32),
+                                       np.array([0], np.int32), np.array([3], np.int32), 64, synth.KV_FP8)
+    v = torch_decode_rows(inp.kv[:1], inp.kv_scale, synth.KV_FP8)[0, :DV]
+    for h in range(NH):
+        np.testing.assert_allclose(out[0, h], v, rtol=0, atol=1e-12)
