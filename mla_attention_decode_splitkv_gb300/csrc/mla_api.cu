@@ -237,7 +237,8 @@ static int decode_impl(const void* q, const void* kv, const void* kv_scale, cons
                        void* stream) {
   if (q == nullptr || kv == nullptr || kv_indptr == nullptr || out == nullptr) return MLA_ERR_INVALID_ARG;
   if (page_size != 0) {
-    if (page_size != 64 && page_size != 128) return MLA_ERR_INVALID_ARG;
+    if (page_size < mla::kMinPage || page_size > mla::kBN || (page_size & (page_size - 1)) != 0)
+      return MLA_ERR_INVALID_ARG;
     if (page_indices == nullptr || last_page_len == nullptr) return MLA_ERR_INVALID_ARG;
     if (!aligned(page_indices, 4) || !aligned(last_page_len, 4)) return MLA_ERR_INVALID_ARG;
   }
@@ -276,6 +277,8 @@ static int decode_impl(const void* q, const void* kv, const void* kv_scale, cons
     if (rc) return rc;
   }
   p.page_size = page_size;
+  p.page_shift = 0;
+  while ((1 << p.page_shift) < page_size) ++p.page_shift;
   p.page_indices = page_indices;
   p.last_page_len = last_page_len;
   p.qo_indptr = qo_indptr;

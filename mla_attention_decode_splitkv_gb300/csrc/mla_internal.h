@@ -10,6 +10,7 @@ constexpr int kHeads = 16;
 constexpr int kDim = 576;
 constexpr int kDimV = 512;
 constexpr int kBN = 128;           // cached tokens per tile (= UMMA M)
+constexpr int kMinPage = 8;        // smallest page (rows) of a paged cache: one swizzle atom per TMA box
 constexpr int kMxBlock = 32;
 constexpr int kMxPacked = 288;     // bytes of e2m1 nibbles per row
 constexpr int kMxScales = 18;      // e8m0 scales per row
@@ -38,7 +39,8 @@ struct DecodeParams {
   unsigned long long wait_limit_ns;
   int test_stall;                  // test hook: the QK issuer waits on a barrier that never completes
   // Paged cache (mla_decode_paged; 0 / null otherwise): kv_indptr indexes page_indices.
-  int page_size;                   // rows per page: 64 or 128
+  int page_size;                   // rows per page: 8, 16, 32, 64 or 128
+  int page_shift;                  // log2(page_size)
   const int32_t* page_indices;     // [kv_indptr[batch]] physical page of each sequence page
   const int32_t* last_page_len;    // [sequences] rows used in each sequence's last page (1..page_size)
   // Several query tokens per sequence (mla_decode_paged_multi; null otherwise, uniform splits
@@ -60,7 +62,7 @@ int encode_rope_map(CUtensorMap* map, const void* kv);
 
 // Launches the split kernel for kv_dtype (geometry per dtype is internal to mla_split.cu).
 cudaError_t launch_split(int kv_dtype, const DecodeParams& p, int grid, cudaStream_t stream);
-// The same for a paged cache (page size 64 or 128, boxes of page_size rows).
+// The same for a paged cache (page size 8 .. 128, a power of two; boxes of page_size rows).
 cudaError_t launch_split_paged(int kv_dtype, const DecodeParams& p, int grid, cudaStream_t stream);
 // Tensor maps with boxes of `box_rows` rows (paged caches: box_rows = page size).
 int encode_kv_map_rows(CUtensorMap* map, const void* kv, int kv_dtype, int box_rows);

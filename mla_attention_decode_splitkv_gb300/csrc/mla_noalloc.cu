@@ -109,6 +109,7 @@ extern "C" int mla_decode_noalloc(const void* q, const void* kv, const void* kv_
   p.wait_limit_ns = 2000000000ull;
   p.test_stall = 0;
   p.page_size = 0;
+  p.page_shift = 0;
   p.page_indices = nullptr;
   p.last_page_len = nullptr;
   p.qo_indptr = nullptr;

@@ -340,35 +340,28 @@ struct SegIter {
 // segment's last row (it is shifted back instead; rows before 0 are zero-filled by TMA),
 // so the kernel reads no row outside [0, kv_indptr[batch]).
 struct Window {
-  int y0;     // first cached row of the window (may be negative)
+  int y0;     // first cached row of the window (may be negative; paged: unused)
   int shift;  // window row of the tile's first token
   int cnt;    // valid tokens in the tile
-  int y1;     // paged: first cached row of the window's second half (page size 64)
 };
 // Contiguous cache: the window ends at the segment's last row (rows before cached row 0 are
-// the TMA's zero fill).  Paged cache (tiles start on page boundaries: the segment starts on
-// one, and a tile is 128 tokens): window row i is token start + i of the sequence; its first
-// half is page start / P of the sequence, its second half (P = 64) the next page, or the
-// same page again when the sequence has no next page (rows that are masked).
-// ROWS = false: only shift and cnt are wanted (no page-list loads).
+// the TMA's zero fill).  Paged cache: tiles start on page boundaries (the segment starts on
+// one, a tile is 128 tokens and the page size divides 128), window row i is token start + i
+// of the sequence, and the rows come from the pages (paged_entry); shift is 0.
+// Page-list entry holding window row i of tile t (the sequence's last page again for rows
+// past its end, which are masked).
+// (Page arithmetic by shifts: page_size is a power of two, page_shift its log2.)
 template <bool PG>
 __device__ __forceinline__ int paged_entry(const DecodeParams& p, const Seg& s, int t, int i) {
-  const int P = p.page_size;
-  const int np = (s.n_total + P - 1) / P;
-  return p.page_indices[s.row0 + min((s.n_lo + t * kBN + i) / P, np - 1)];
+  const int np = (s.n_total + p.page_size - 1) >> p.page_shift;
+  return p.page_indices[s.row0 + min((s.n_lo + t * kBN + i) >> p.page_shift, np - 1)];
 }
-template <int KV, bool PG, bool ROWS = true>
+template <int KV, bool PG>
 __device__ __forceinline__ Window tile_window(const DecodeParams& p, const Seg& s, int t) {
   Window w;
   if constexpr (PG) {
     const int start = s.n_lo + t * kBN;
-    const int P = p.page_size;
-    if constexpr (ROWS) {
-      w.y0 = paged_entry<PG>(p, s, t, 0) * P;
-      w.y1 = paged_entry<PG>(p, s, t, kBN / 2) * P + (P == kBN ? kBN / 2 : 0);
-    } else {
-      w.y0 = w.y1 = 0;
-    }
+    w.y0 = 0;
     w.shift = 0;
     w.cnt = min(kBN, s.n_hi - start);
   } else {
@@ -378,7 +371,6 @@ __device__ __forceinline__ Window tile_window(const DecodeParams& p, const Seg& 
     w.y0 = y0;
     w.shift = row_start - y0;
     w.cnt = min(kBN, row_hi - row_start);
-    w.y1 = y0 + kBN / 2;
   }
   return w;
 }
@@ -486,6 +478,44 @@ __device__ void stage_q_fp8(const DecodeParams& p, int b, uint8_t* qs, float* qs
 // boxes, 64-byte swizzle): bytes [64c, 64c + 64) of the window's 128 rows for the value
 // chunks c = 0..3 and bytes [256, 288) for the rope chunk (the box's columns past 288 are
 // zero-filled).  The dequantisation frees each slab as soon as it has read it.
+// Paged producers: the physical first row of each page of tile t (one TMA box of P rows per
+// page, at row k P of the window), loaded once per tile; at most kBN / kMinPage pages.
+template <bool PG>
+__device__ __forceinline__ void tile_page_rows(const DecodeParams& p, const Seg& s, int t, int (&prow)[kBN / kMinPage]) {
+  const int nb = kBN >> p.page_shift;
+  const int np = (s.n_total + p.page_size - 1) >> p.page_shift;
+  const int* pl = p.page_indices + s.row0;
+  const int pg0 = (s.n_lo + t * kBN) >> p.page_shift;
+  if (nb <= 2) {   // 64- and 128-row pages: the common case stays short
+    prow[0] = pl[pg0] << p.page_shift;
+    prow[1] = pl[min(pg0 + 1, np - 1)] << p.page_shift;
+    return;
+  }
+#pragma unroll
+  for (int k = 0; k < kBN / kMinPage; ++k) prow[k] = k < nb ? pl[min(pg0 + k, np - 1)] << p.page_shift : 0;
+}
+// Issues the boxes of one slot: the whole 128-row window (contiguous) or one box per page
+// (paged; box k lands `bytes / pages` bytes after box k - 1, a multiple of the swizzle atom).
+template <bool PG>
+__device__ __forceinline__ void load_window(const DecodeParams& p, const CUtensorMap* map, uint32_t dst, int x,
+                                            uint32_t bytes, int y0, const int (&prow)[kBN / kMinPage], uint32_t fb) {
+  if constexpr (PG) {
+    static_assert(kBN == 128, "bytes / nb below assumes 128-row tiles");
+    const int nb = kBN >> p.page_shift;
+    if (nb <= 2) {
+      tma_load_2d(dst, map, x, prow[0], fb);
+      if (nb == 2) tma_load_2d(dst + (bytes >> 1), map, x, prow[1], fb);
+      return;
+    }
+    const uint32_t step = bytes >> (7 - p.page_shift);   // bytes / nb
+#pragma unroll
+    for (int k = 0; k < kBN / kMinPage; ++k)
+      if (k < nb) tma_load_2d(dst + k * step, map, x, prow[k], fb);
+  } else {
+    tma_load_2d(dst, map, x, y0, fb);
+  }
+}
+
 template <bool PG>
 __device__ void run_producer_mx(const DecodeParams& p, SharedState* sh, uint8_t* slabs) {
   volatile int* abortf = &sh->abort;
@@ -500,6 +530,8 @@ __device__ void run_producer_mx(const DecodeParams& p, SharedState* sh, uint8_t*
     const int ntiles = (n + kBN - 1) / kBN;
     for (int t = 0; t < ntiles && ok; ++t) {
       const Window w = tile_window<2, PG>(p, s, t);
+      int prow[kBN / kMinPage];
+      if constexpr (PG) tile_page_rows<PG>(p, s, t, prow);
       for (int c = 0; c < 5; ++c) {
         if (!wait_bar(smem_u32(&sh->slab_empty[slot]), phase ^ 1, abortf, p.status, p.wait_limit_ns)) {
           ok = false;
@@ -507,12 +539,7 @@ __device__ void run_producer_mx(const DecodeParams& p, SharedState* sh, uint8_t*
         }
         const uint32_t fb = smem_u32(&sh->slab_full[slot]);
         mbar_arrive_expect_tx(fb, kSlabBytes);
-        if (PG && p.page_size < kBN) {   // two 64-row boxes: the window's two pages
-          tma_load_2d(smem_u32(slabs + slot * kSlabBytes), &p.tmap, 64 * c, w.y0, fb);
-          tma_load_2d(smem_u32(slabs + slot * kSlabBytes + kSlabBytes / 2), &p.tmap, 64 * c, w.y1, fb);
-        } else {
-          tma_load_2d(smem_u32(slabs + slot * kSlabBytes), &p.tmap, 64 * c, w.y0, fb);
-        }
+        load_window<PG>(p, &p.tmap, smem_u32(slabs + slot * kSlabBytes), 64 * c, kSlabBytes, w.y0, prow, fb);
         ++idx;
         if (++slot == kSlabs) { slot = 0; phase ^= 1; }
       }
@@ -540,6 +567,8 @@ __device__ void run_producer(const DecodeParams& p, SharedState* sh, uint8_t* ri
     const int ntiles = (n + kBN - 1) / kBN;
     for (int t = 0; t < ntiles && ok; ++t) {
       const Window w = tile_window<KV, PG>(p, s, t);
+      int prow[kBN / kMinPage];
+      if constexpr (PG) tile_page_rows<PG>(p, s, t, prow);
       for (int c = 0; c < C::kRingPT; ++c) {
         if (!wait_bar(smem_u32(&sh->empty[slot]), phase ^ 1, abortf, p.status, p.wait_limit_ns)) {
           ok = false;
@@ -547,17 +576,7 @@ __device__ void run_producer(const DecodeParams& p, SharedState* sh, uint8_t* ri
         }
         const uint32_t dst = smem_u32(ring + slot * C::kSlotBytes);
         const uint32_t fb = smem_u32(&sh->full[slot]);
-        // A box is 128 rows (contiguous cache, 128-row pages) or 64 rows (64-row pages: the
-        // window's two pages land in the two halves of the box's SMEM footprint).
-        const bool halves = PG && p.page_size < kBN;
-        auto box = [&](uint32_t d, int x, uint32_t bytes) {
-          if (halves) {
-            tma_load_2d(d, &p.tmap, x, w.y0, fb);
-            tma_load_2d(d + bytes / 2, &p.tmap, x, w.y1, fb);
-          } else {
-            tma_load_2d(d, &p.tmap, x, w.y0, fb);
-          }
-        };
+        auto box = [&](uint32_t d, int x, uint32_t bytes) { load_window<PG>(p, &p.tmap, d, x, bytes, w.y0, prow, fb); };
         if constexpr (KV == 0) {
           if (c < 4) {
             mbar_arrive_expect_tx(fb, 32768);
@@ -584,12 +603,7 @@ __device__ void run_producer(const DecodeParams& p, SharedState* sh, uint8_t* ri
         }
         const uint32_t fb = smem_u32(&sh->rope_full[rs]);
         mbar_arrive_expect_tx(fb, kRopeBytes);
-        if (PG && p.page_size < kBN) {
-          tma_load_2d(smem_u32(rope + rs * kRopeBytes), &p.tmap_rope, kDimV, w.y0, fb);
-          tma_load_2d(smem_u32(rope + rs * kRopeBytes + kRopeBytes / 2), &p.tmap_rope, kDimV, w.y1, fb);
-        } else {
-          tma_load_2d(smem_u32(rope + rs * kRopeBytes), &p.tmap_rope, kDimV, w.y0, fb);
-        }
+        load_window<PG>(p, &p.tmap_rope, smem_u32(rope + rs * kRopeBytes), kDimV, kRopeBytes, w.y0, prow, fb);
         ++ridx;
       }
     }
@@ -678,7 +692,7 @@ __device__ void run_dequant(const DecodeParams& p, SharedState* sh, uint8_t* rin
       int emax = 127;
       uint32_t kpk[3] = {0u, 0u, 0u};
       // Cached row of this thread's window row (paged: its page's physical row).
-      const int yr = PG ? (di < kBN / 2 ? w.y0 + di : w.y1 + di - kBN / 2) : w.y0 + di;
+      const int yr = PG ? (paged_entry<PG>(p, s, t, di) << p.page_shift) + (di & (p.page_size - 1)) : w.y0 + di;
       if (yr >= 0) {
         uint32_t sc[9];
         if (t > 0) {
@@ -700,7 +714,7 @@ __device__ void run_dequant(const DecodeParams& p, SharedState* sh, uint8_t* rin
       }
       if (t + 1 < ntiles) {
         const Window wn = tile_window<2, PG>(p, s, t + 1);
-        const int yn = PG ? (di < kBN / 2 ? wn.y0 + di : wn.y1 + di - kBN / 2) : wn.y0 + di;
+        const int yn = PG ? (paged_entry<PG>(p, s, t + 1, di) << p.page_shift) + (di & (p.page_size - 1)) : wn.y0 + di;
         if (yn >= 0) {
           const uint16_t* sp = reinterpret_cast<const uint16_t*>(scales + static_cast<size_t>(yn) * kMxScales);
 #pragma unroll
@@ -1193,7 +1207,7 @@ __device__ void run_softmax(const DecodeParams& p, SharedState* sh, uint8_t* qs,
     float mref[H], lpart[H];
     bool has_nxt = false;
     for (int t = 0; t < ntiles; ++t) {
-      const Window w = tile_window<KV, PG, false>(p, cur, t);
+      const Window w = tile_window<KV, PG>(p, cur, t);
       bool okw = wait_bar(smem_u32(&sh->s_full[g & 1]), (g >> 1) & 1, abortf, p.status, p.wait_limit_ns);
       okw = __all_sync(0xffffffffu, okw);
       tc_fence_after();

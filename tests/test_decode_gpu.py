@@ -245,8 +245,11 @@ def test_mxfp4_short_segments_repeated(pkg, lens):
 PAGED_LENS = [1, 129, 0, 1000, 2048, 64, 65, 127, 128]
 
 
+PAGE_SIZES = [8, 16, 32, 64, 128]
+
+
 @pytest.mark.parametrize("kv_dtype", DTYPES)
-@pytest.mark.parametrize("page_size", [64, 128])
+@pytest.mark.parametrize("page_size", PAGE_SIZES)
 @pytest.mark.parametrize("ns", [1, 2, 3, 0])
 def test_paged_cache_matches_oracle(pkg, kv_dtype, page_size, ns):
     """Shuffled physical pages, partial last pages, empty and single-token sequences; the
@@ -263,18 +266,18 @@ def test_paged_cache_matches_oracle(pkg, kv_dtype, page_size, ns):
     _check(out, ref, f"paged P={page_size} ns={ns}")
 
 
-@pytest.mark.parametrize("kv_dtype", [synth.KV_FP8, synth.KV_MXFP4])
+@pytest.mark.parametrize("kv_dtype,page_size", [(synth.KV_FP8, 64), (synth.KV_MXFP4, 64), (synth.KV_FP8, 8)])
 @pytest.mark.parametrize("balanced", [False, True])
-def test_paged_workload_sampled_rows(pkg, kv_dtype, balanced):
-    """A full-size workload (64 x 8192 tokens) in shuffled 64-row pages, in uniform splits
-    (one wave) and in the balanced mode; sampled batch rows against the oracle."""
+def test_paged_workload_sampled_rows(pkg, kv_dtype, page_size, balanced):
+    """A full-size workload (64 x 8192 tokens) in shuffled pages, in uniform splits (one
+    wave) and in the balanced mode; sampled batch rows against the oracle."""
     B, L = 64, 8192
     inp = synth.make_inputs(B, [L] * B, kv_dtype, seed=1236)
-    pg = synth.to_paged(inp, 64, seed=1243)
+    pg = synth.to_paged(inp, page_size, seed=1243)
     g = pg.to("cuda")
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     ns = 0 if balanced else max(1, sms // B)
-    out = pkg.decode_paged(g.q, g.kv, g.kv_scale, g.page_indptr, g.page_indices, g.last_page_len, 64,
+    out = pkg.decode_paged(g.q, g.kv, g.kv_scale, g.page_indptr, g.page_indices, g.last_page_len, page_size,
                            kv_dtype, num_splits=ns)
     torch.cuda.synchronize()
     assert pkg.device_status(clear=True) == pkg.MLA_OK
@@ -282,8 +285,8 @@ def test_paged_workload_sampled_rows(pkg, kv_dtype, balanced):
     sub_indptr = torch.tensor([0] + np.cumsum([int(pg.page_indptr[b + 1] - pg.page_indptr[b]) for b in rows]).tolist(),
                               dtype=torch.int32)
     sub_pages = torch.cat([pg.page_indices[int(pg.page_indptr[b]):int(pg.page_indptr[b + 1])] for b in rows])
-    ref, _ = oracle.decode_paged(pg.q[rows], pg.kv, pg.kv_scale, sub_indptr, sub_pages, pg.last_page_len[rows], 64,
-                                 kv_dtype)
+    ref, _ = oracle.decode_paged(pg.q[rows], pg.kv, pg.kv_scale, sub_indptr, sub_pages, pg.last_page_len[rows],
+                                 page_size, kv_dtype)
     for i, b in enumerate(rows):
         _check(out[b], ref[i], f"paged workload row {b}")
 
@@ -292,14 +295,14 @@ def test_paged_rejects_bad_page_size(pkg):
     inp = synth.make_inputs(2, [100, 3], synth.KV_FP8, seed=5)
     pg = synth.to_paged(inp, 64, seed=6).to("cuda")
     out = torch.empty((2, 16, 512), dtype=torch.bfloat16, device="cuda")
-    for ps in (0, 32, 256):
+    for ps in (0, 4, 48, 256):
         rc = pkg.mla_decode_paged(pg.q, pg.kv, pg.kv_scale, pg.page_indptr, pg.page_indices, pg.last_page_len, ps,
                                   out, 2, 1, synth.KV_FP8)
         assert rc == pkg.MLA_ERR_INVALID_ARG
 
 
 @pytest.mark.parametrize("kv_dtype", DTYPES)
-@pytest.mark.parametrize("page_size", [64, 128])
+@pytest.mark.parametrize("page_size", PAGE_SIZES)
 def test_paged_balanced_ragged_batch(pkg, kv_dtype, page_size):
     """The balanced mode over a paged ragged batch: runs of empty and one-page sequences
     between long ones, so that CTA ranges start and end inside sequences, at page ends
@@ -326,7 +329,7 @@ MQ_QLENS = [1, 2, 3, 4, 0, 3, 2]     # q_len 0, q_len > L (rows that see nothing
 
 
 @pytest.mark.parametrize("kv_dtype", DTYPES)
-@pytest.mark.parametrize("page_size", [64, 128])
+@pytest.mark.parametrize("page_size", [8, 64, 128])
 @pytest.mark.parametrize("ns", [1, 3, 0])
 def test_paged_multi_query_matches_oracle(pkg, kv_dtype, page_size, ns):
     inp = synth.make_inputs(len(MQ_LENS), MQ_LENS, kv_dtype, seed=120 + kv_dtype)
