@@ -478,46 +478,50 @@ __device__ void stage_q_fp8(const DecodeParams& p, int b, uint8_t* qs, float* qs
 // boxes, 64-byte swizzle): bytes [64c, 64c + 64) of the window's 128 rows for the value
 // chunks c = 0..3 and bytes [256, 288) for the rope chunk (the box's columns past 288 are
 // zero-filled).  The dequantisation frees each slab as soon as it has read it.
-// Paged producers: the physical first row of each page of tile t (one TMA box of P rows per
-// page, at row k P of the window), loaded once per tile; at most kBN / kMinPage pages.
+// Paged producers run on the whole warp: lane k < 128/P owns page k of the tile (one TMA
+// box of P rows, at window row k P).  Its physical first row, loaded once per tile:
 template <bool PG>
-__device__ __forceinline__ void tile_page_rows(const DecodeParams& p, const Seg& s, int t, int (&prow)[kBN / kMinPage]) {
+__device__ __forceinline__ int lane_page_row(const DecodeParams& p, const Seg& s, int t, int lane) {
   const int nb = kBN >> p.page_shift;
   const int np = (s.n_total + p.page_size - 1) >> p.page_shift;
-  const int* pl = p.page_indices + s.row0;
-  const int pg0 = (s.n_lo + t * kBN) >> p.page_shift;
-  if (nb <= 2) {   // 64- and 128-row pages: the common case stays short
-    prow[0] = pl[pg0] << p.page_shift;
-    prow[1] = pl[min(pg0 + 1, np - 1)] << p.page_shift;
-    return;
-  }
-#pragma unroll
-  for (int k = 0; k < kBN / kMinPage; ++k) prow[k] = k < nb ? pl[min(pg0 + k, np - 1)] << p.page_shift : 0;
+  const int pg = min(((s.n_lo + t * kBN) >> p.page_shift) + min(lane, nb - 1), np - 1);
+  return p.page_indices[s.row0 + pg] << p.page_shift;
 }
-// Issues the boxes of one slot: the whole 128-row window (contiguous) or one box per page
-// (paged; box k lands `bytes / pages` bytes after box k - 1, a multiple of the swizzle atom).
+// Issues the boxes of one slot: the whole 128-row window (contiguous, one lane) or one box
+// per page (paged, lane k: box k lands k * bytes * P / 128 bytes into the slot, a multiple
+// of the swizzle atom for P >= 8).
 template <bool PG>
 __device__ __forceinline__ void load_window(const DecodeParams& p, const CUtensorMap* map, uint32_t dst, int x,
-                                            uint32_t bytes, int y0, const int (&prow)[kBN / kMinPage], uint32_t fb) {
+                                            uint32_t bytes, int y0, int lane, int lane_row, uint32_t fb) {
   if constexpr (PG) {
-    static_assert(kBN == 128, "bytes / nb below assumes 128-row tiles");
-    const int nb = kBN >> p.page_shift;
-    if (nb <= 2) {
-      tma_load_2d(dst, map, x, prow[0], fb);
-      if (nb == 2) tma_load_2d(dst + (bytes >> 1), map, x, prow[1], fb);
-      return;
-    }
-    const uint32_t step = bytes >> (7 - p.page_shift);   // bytes / nb
-#pragma unroll
-    for (int k = 0; k < kBN / kMinPage; ++k)
-      if (k < nb) tma_load_2d(dst + k * step, map, x, prow[k], fb);
+    static_assert(kBN == 128, "bytes * P / 128 below assumes 128-row tiles");
+    if (lane < (kBN >> p.page_shift)) tma_load_2d(dst + ((lane * bytes) >> (7 - p.page_shift)), map, x, lane_row, fb);
   } else {
     tma_load_2d(dst, map, x, y0, fb);
   }
 }
+// Sets the slot's expected bytes: one lane (contiguous) or lane 0 of the paged warp, before
+// any lane issues a box.
+template <bool PG>
+__device__ __forceinline__ void expect_slot(uint32_t fb, uint32_t bytes, int lane) {
+  if constexpr (PG) {
+    if (lane == 0) mbar_arrive_expect_tx(fb, bytes);
+    __syncwarp();
+  } else {
+    mbar_arrive_expect_tx(fb, bytes);
+  }
+}
+// The warp-wide (paged) producer agrees on every wait's outcome.
+template <bool PG>
+__device__ __forceinline__ bool producer_wait(uint32_t bar, uint32_t parity, volatile int* abortf, int* status,
+                                              uint64_t limit) {
+  const bool ok = wait_bar(bar, parity, abortf, status, limit);
+  if constexpr (PG) return __all_sync(0xffffffffu, ok);
+  return ok;
+}
 
 template <bool PG>
-__device__ void run_producer_mx(const DecodeParams& p, SharedState* sh, uint8_t* slabs) {
+__device__ void run_producer_mx(const DecodeParams& p, SharedState* sh, uint8_t* slabs, int lane) {
   volatile int* abortf = &sh->abort;
   SegIter<PG> it;
   it.init(p, blockIdx.x, sh->seg_total, sh->seg_b0);
@@ -530,16 +534,16 @@ __device__ void run_producer_mx(const DecodeParams& p, SharedState* sh, uint8_t*
     const int ntiles = (n + kBN - 1) / kBN;
     for (int t = 0; t < ntiles && ok; ++t) {
       const Window w = tile_window<2, PG>(p, s, t);
-      int prow[kBN / kMinPage];
-      if constexpr (PG) tile_page_rows<PG>(p, s, t, prow);
+      int lrow = 0;
+      if constexpr (PG) lrow = lane_page_row<PG>(p, s, t, lane);
       for (int c = 0; c < 5; ++c) {
-        if (!wait_bar(smem_u32(&sh->slab_empty[slot]), phase ^ 1, abortf, p.status, p.wait_limit_ns)) {
+        if (!producer_wait<PG>(smem_u32(&sh->slab_empty[slot]), phase ^ 1, abortf, p.status, p.wait_limit_ns)) {
           ok = false;
           break;
         }
         const uint32_t fb = smem_u32(&sh->slab_full[slot]);
-        mbar_arrive_expect_tx(fb, kSlabBytes);
-        load_window<PG>(p, &p.tmap, smem_u32(slabs + slot * kSlabBytes), 64 * c, kSlabBytes, w.y0, prow, fb);
+        expect_slot<PG>(fb, kSlabBytes, lane);
+        load_window<PG>(p, &p.tmap, smem_u32(slabs + slot * kSlabBytes), 64 * c, kSlabBytes, w.y0, lane, lrow, fb);
         ++idx;
         if (++slot == kSlabs) { slot = 0; phase ^= 1; }
       }
@@ -553,7 +557,7 @@ __device__ void run_producer_mx(const DecodeParams& p, SharedState* sh, uint8_t*
 }
 
 template <int KV, bool PG>
-__device__ void run_producer(const DecodeParams& p, SharedState* sh, uint8_t* ring, uint8_t* rope) {
+__device__ void run_producer(const DecodeParams& p, SharedState* sh, uint8_t* ring, uint8_t* rope, int lane) {
   using C = Cfg<KV>;
   volatile int* abortf = &sh->abort;
   SegIter<PG> it;
@@ -567,27 +571,27 @@ __device__ void run_producer(const DecodeParams& p, SharedState* sh, uint8_t* ri
     const int ntiles = (n + kBN - 1) / kBN;
     for (int t = 0; t < ntiles && ok; ++t) {
       const Window w = tile_window<KV, PG>(p, s, t);
-      int prow[kBN / kMinPage];
-      if constexpr (PG) tile_page_rows<PG>(p, s, t, prow);
+      int lrow = 0;
+      if constexpr (PG) lrow = lane_page_row<PG>(p, s, t, lane);
       for (int c = 0; c < C::kRingPT; ++c) {
-        if (!wait_bar(smem_u32(&sh->empty[slot]), phase ^ 1, abortf, p.status, p.wait_limit_ns)) {
+        if (!producer_wait<PG>(smem_u32(&sh->empty[slot]), phase ^ 1, abortf, p.status, p.wait_limit_ns)) {
           ok = false;
           break;
         }
         const uint32_t dst = smem_u32(ring + slot * C::kSlotBytes);
         const uint32_t fb = smem_u32(&sh->full[slot]);
-        auto box = [&](uint32_t d, int x, uint32_t bytes) { load_window<PG>(p, &p.tmap, d, x, bytes, w.y0, prow, fb); };
+        auto box = [&](uint32_t d, int x, uint32_t bytes) { load_window<PG>(p, &p.tmap, d, x, bytes, w.y0, lane, lrow, fb); };
         if constexpr (KV == 0) {
           if (c < 4) {
-            mbar_arrive_expect_tx(fb, 32768);
+            expect_slot<PG>(fb, 32768, lane);
             box(dst, 128 * c, 16384);
             box(dst + 16384, 128 * c + 64, 16384);
           } else {
-            mbar_arrive_expect_tx(fb, 16384);
+            expect_slot<PG>(fb, 16384, lane);
             box(dst, 512, 16384);
           }
         } else {
-          mbar_arrive_expect_tx(fb, 16384);
+          expect_slot<PG>(fb, 16384, lane);
           box(dst, 128 * c, 16384);
         }
         ++idx;
@@ -596,14 +600,14 @@ __device__ void run_producer(const DecodeParams& p, SharedState* sh, uint8_t* ri
       if constexpr (C::kRopeSlots > 0) {   // fp8: the rope chunk (64 B of each row) into its own slots
         if (!ok) break;
         const uint32_t rs = ridx % C::kRopeSlots;
-        if (!wait_bar(smem_u32(&sh->rope_empty[rs]), ((ridx / C::kRopeSlots) & 1) ^ 1, abortf, p.status,
-                      p.wait_limit_ns)) {
+        if (!producer_wait<PG>(smem_u32(&sh->rope_empty[rs]), ((ridx / C::kRopeSlots) & 1) ^ 1, abortf, p.status,
+                               p.wait_limit_ns)) {
           ok = false;
           break;
         }
         const uint32_t fb = smem_u32(&sh->rope_full[rs]);
-        mbar_arrive_expect_tx(fb, kRopeBytes);
-        load_window<PG>(p, &p.tmap_rope, smem_u32(rope + rs * kRopeBytes), kDimV, kRopeBytes, w.y0, prow, fb);
+        expect_slot<PG>(fb, kRopeBytes, lane);
+        load_window<PG>(p, &p.tmap_rope, smem_u32(rope + rs * kRopeBytes), kDimV, kRopeBytes, w.y0, lane, lrow, fb);
         ++ridx;
       }
     }
@@ -1484,8 +1488,8 @@ __global__ void __launch_bounds__(Cfg<KV>::kThreads, 1) mla_split_kernel(const _
   if (warp < 4) {
     if constexpr (KV == 2) regs_dec<C::kRegsIssue>();
     if (warp == 0) {
-      if (lane == 0) {
-        if constexpr (KV == 2) run_producer_mx<PG>(p, sh, slabs); else run_producer<KV, PG>(p, sh, ring, rope);
+      if (PG || lane == 0) {   // paged: the whole warp (one lane per page)
+        if constexpr (KV == 2) run_producer_mx<PG>(p, sh, slabs, lane); else run_producer<KV, PG>(p, sh, ring, rope, lane);
       }
     } else if (warp == 1) {
       if (lane == 0) run_mma_qk<KV, PG>(p, sh, make_descs(ring, rope, qs, ps), tmem);
