@@ -89,3 +89,48 @@ def test_same_seed_same_inputs():
     a = synth.make_inputs(2, [3, 5], synth.KV_MXFP4, seed=9)
     b = synth.make_inputs(2, [3, 5], synth.KV_MXFP4, seed=9)
     assert torch.equal(a.q, b.q) and torch.equal(a.kv, b.kv) and torch.equal(a.kv_scale, b.kv_scale)
+
+
+@pytest.mark.parametrize("kv_dtype", [synth.KV_BF16, synth.KV_FP8, synth.KV_MXFP4])
+@pytest.mark.parametrize("page_size", [8, 64, 128])
+def test_paged_copy_holds_every_row_once_at_its_page_position(kv_dtype, page_size):
+    """The page table of to_paged: pages are distinct, in range and not in order; every
+    cached row (and its MXFP4 block scales) sits at page_indices[...] * P + t % P; the
+    last-page lengths give back the sequence lengths."""
+    lens = [1, 0, 200, 64, 129]
+    inp = synth.make_inputs(len(lens), lens, kv_dtype, seed=50)
+    pg = synth.to_paged(inp, page_size, seed=51)
+    ip, pi, last = pg.page_indptr.tolist(), pg.page_indices.tolist(), pg.last_page_len.tolist()
+    assert ip[0] == 0 and len(ip) == len(lens) + 1
+    used = pi[:ip[-1]]
+    assert len(set(used)) == len(used)
+    assert all(0 <= x < pg.kv.shape[0] // page_size for x in used)
+    assert pg.kv.shape[0] % page_size == 0
+    src_ip = inp.kv_indptr.tolist()
+    for b, L in enumerate(lens):
+        n = ip[b + 1] - ip[b]
+        assert n == (L + page_size - 1) // page_size
+        assert (n - 1) * page_size + last[b] == L if n else L == 0
+        for t in range(L):
+            row = pi[ip[b] + t // page_size] * page_size + t % page_size
+            assert torch.equal(pg.kv[row], inp.kv[src_ip[b] + t])
+            if kv_dtype == synth.KV_MXFP4:
+                assert torch.equal(pg.kv_scale[row], inp.kv_scale[src_ip[b] + t])
+    if kv_dtype == synth.KV_FP8:
+        assert torch.equal(pg.kv_scale, inp.kv_scale)
+
+
+def test_paged_copy_is_seeded_and_shuffled():
+    inp = synth.make_inputs(3, [300, 5, 700], synth.KV_FP8, seed=52)
+    a, b, c = (synth.to_paged(inp, 64, seed=s) for s in (53, 53, 54))
+    assert torch.equal(a.page_indices, b.page_indices) and torch.equal(a.kv, b.kv)
+    assert not torch.equal(a.page_indices, c.page_indices)
+    assert a.page_indices.tolist() != sorted(a.page_indices.tolist())
+
+
+def test_make_queries_rows_and_indptr():
+    q, qo = synth.make_queries([2, 0, 3], seed=55)
+    assert q.shape == (5, synth.NUM_HEADS, synth.HEAD_DIM) and q.dtype == torch.bfloat16
+    assert qo.tolist() == [0, 2, 2, 5] and qo.dtype == torch.int32
+    q2, _ = synth.make_queries([2, 0, 3], seed=55)
+    assert torch.equal(q, q2)
