@@ -349,6 +349,16 @@ def main():
         call()
     torch.cuda.synchronize()
     split_ms_sum, call_ms_sum, ncalls = pkg.profile_end()
+    # warm calls (no flush between them), each timed on its own, for the latency medians
+    # (not in --quick runs, whose launch sequence the profiler commands count on)
+    n_warm = 0 if args.quick else max(20, args.steps)
+    wevs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_warm)]
+    for a, b in wevs:
+        a.record(stream)
+        call()
+        b.record(stream)
+    torch.cuda.synchronize()
+    warm_us = [a.elapsed_time(b) * 1e3 for a, b in wevs]
     if ws > 1:
         torch.distributed.barrier()
     clocks = sampler.stop()
@@ -413,6 +423,8 @@ def main():
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms, "us_per_call": ms * 1e3, "frac_of_8tbs": value / ws / 8000.0,
+        "latency_us": {"cold_median": statistics.median(step_ms) * 1e3, "warm_median": statistics.median(warm_us),
+                       "cold_calls": len(step_ms), "warm_calls": len(warm_us)},
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": {0: "bf16", 1: "e4m3", 2: "e4m3"}[spec.kv_dtype],
         "data": "synthetic (seeded N(0,1) q and KV, stored per the workload's cache encoding)",

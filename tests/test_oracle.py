@@ -368,3 +368,22 @@ def test_multi_query_first_token_seeing_one_row_returns_its_value():
     v = torch_decode_rows(inp.kv[:1], inp.kv_scale, synth.KV_FP8)[0, :DV]
     for h in range(NH):
         np.testing.assert_allclose(out[0, h], v, rtol=0, atol=1e-12)
+
+
+def test_value_translation_adds_the_constant():
+    """O(V + c) = O(V) + c.  V is the first 512 features of the cached row, so the query's
+    first 512 features are zero (logits from the rope features only).  Values are multiples
+    of 1/8 and c = 2, so V + c is exact in bf16."""
+    g = torch.Generator().manual_seed(44)
+    L = 23
+    k = (torch.randint(-48, 49, (L, D), generator=g).double() / 8).to(torch.bfloat16)
+    k2 = k.clone()
+    k2[:, :DV] = (k[:, :DV].double() + 2.0).to(torch.bfloat16)
+    assert torch.equal(k2[:, :DV].double(), k[:, :DV].double() + 2.0)
+    q = torch.randn((1, NH, D), generator=g).to(torch.bfloat16)
+    q[:, :, :DV] = 0
+    ip = np.array([0, L], np.int32)
+    o1, l1 = oracle.decode(q, k, None, ip, synth.KV_BF16)
+    o2, l2 = oracle.decode(q, k2, None, ip, synth.KV_BF16)
+    np.testing.assert_allclose(o2, o1 + 2.0, rtol=0, atol=1e-12)
+    np.testing.assert_array_equal(l1, l2)
