@@ -154,16 +154,19 @@ int mla_decode_paged_multi(const void* q, const int32_t* qo_indptr, int total_q,
 
 /*
  * mla_decode_pick_splits -- host-only choice of num_splits for mla_decode.
- *     ns = min(floor(num_sms / batch), ceil(kv_len_hint / 256));  returns ns if ns >= 2,
- *     else 0 (the balanced persistent mode).
+ *     ns = min(floor(num_sms / batch), ceil(kv_len_hint / 256), floor(sqrt(kv_len_hint / 32)));
+ *     returns ns if ns >= 2; else 1 if kv_len_hint <= 2048; else 0 (the balanced mode).
  * That is: one wave of uniform splits (each CTA works on one contiguous piece of one
- * sequence, every piece at least two 128-row tiles) when the batch leaves at least two
- * SMs per sequence; otherwise one CTA per SM over the concatenated cached rows, which
- * also suits ragged batches.  (Measured on GB300: a CTA that crosses from one sequence
- * into the next pays a pipeline drain, so a one-wave uniform split beats the balanced
- * mode for short uniform batches; the pages' analytic split model, submission 700955
- * `_estimate_custom_splits`, targets another GPU and is not used.)
- * Returns ns = 0 or ns >= 2, or MLA_ERR_INVALID_ARG for batch <= 0, kv_len_hint < 0,
+ * sequence, every piece at least two 128-row tiles, at most floor(sqrt(L/32)) pieces
+ * because the merge of a sequence reads all its pieces in one CTA) when the batch leaves
+ * at least two SMs per sequence.  Otherwise one split per sequence for short sequences,
+ * and one CTA per SM over the concatenated cached rows (which also suits ragged batches)
+ * for long ones.  (Measured on GB300: a CTA that crosses from one sequence into the next
+ * pays a pipeline drain, so uniform splits beat the balanced mode for short uniform
+ * batches, e.g. 256 x 1024 fp8 47.7 against 62.1 us; 16 pieces beat 32 at 4 x 8192.  The
+ * pages' analytic split model, submission 700955 `_estimate_custom_splits`, targets
+ * another GPU and is not used.)
+ * Returns ns = 0, 1 or >= 2, or MLA_ERR_INVALID_ARG for batch <= 0, kv_len_hint < 0,
  * num_sms <= 0 or an unknown kv_dtype.
  */
 int mla_decode_pick_splits(int batch, int kv_len_hint, int num_sms, int kv_dtype);

@@ -178,11 +178,22 @@ void mla_decode_set_test_stall(int on) { g_test_stall = on ? 1 : 0; }
 int mla_decode_pick_splits(int batch, int kv_len_hint, int num_sms, int kv_dtype) {
   if (batch <= 0 || kv_len_hint < 0 || num_sms <= 0 || kv_dtype < 0 || kv_dtype > 2) return MLA_ERR_INVALID_ARG;
   // One wave of uniform splits (every CTA one segment, no segment switches inside a CTA)
-  // when the batch leaves at least two SMs per sequence; each piece keeps >= 2 tiles.
+  // when the batch leaves at least two SMs per sequence.  Each piece keeps >= 2 tiles, and
+  // the pieces of a sequence are at most floor(sqrt(L / 32)): its merge (one CTA reading
+  // every piece) grows with ns while the streaming time shrinks as L / ns.
+  const long long L = kv_len_hint;
   const long long per_seq = num_sms / batch;
-  const long long max_pieces = (static_cast<long long>(kv_len_hint) + 2 * mla::kBN - 1) / (2 * mla::kBN);
-  const long long ns = per_seq < max_pieces ? per_seq : max_pieces;
-  return ns >= 2 ? static_cast<int>(ns) : 0;   // else: balanced persistent mode
+  const long long by_tiles = (L + 2 * mla::kBN - 1) / (2 * mla::kBN);
+  const long long q = L / 32;
+  long long by_merge = static_cast<long long>(std::sqrt(static_cast<double>(q)));
+  while (by_merge * by_merge > q) --by_merge;
+  while ((by_merge + 1) * (by_merge + 1) <= q) ++by_merge;
+  const long long ns = std::min(per_seq, std::min(by_tiles, by_merge));
+  if (ns >= 2) return static_cast<int>(ns);
+  // More sequences than half the SMs: one CTA per short sequence (the balanced mode's CTAs
+  // would cross many sequence boundaries); the balanced persistent mode for long or
+  // ragged ones.
+  return L <= 2048 ? 1 : 0;
 }
 
 int mla_decode_workspace_slots(int batch, int num_splits, int num_sms) {

@@ -132,15 +132,19 @@ def test_valid_call_without_a_gpu_fails_cleanly(lib):
 @pytest.mark.parametrize("dtype", [0, 1, 2])
 def test_pick_splits_follows_the_documented_rule(lib, dtype):
     for batch in (1, 4, 32, 64, 75, 76, 77, 128, 151, 152, 153, 256, 1000):
-        for L in (0, 1, 100, 256, 257, 1024, 4000, 8192, 65536):
+        for L in (0, 1, 100, 127, 128, 256, 257, 1024, 2048, 2049, 4000, 8192, 65536, 10**6):
             for sms in (148, 152):
-                ns = min(sms // batch, -(-L // 256))
-                want = ns if ns >= 2 else 0
+                ns = min(sms // batch, -(-L // 256), math.isqrt(L // 32))
+                want = ns if ns >= 2 else (1 if L <= 2048 else 0)
                 assert lib.mla_decode_pick_splits(batch, L, sms, dtype) == want, (batch, L, sms)
-    # the workloads: batch 64 x 8192 -> 2 splits, 32 x 1024 -> 4, 256 x 8192 -> balanced
+    # the workloads: 64 x 8192 -> 2 splits, 32 x 1024 -> 4, 256 x 8192 -> balanced, a ragged
+    # batch of 128 (mean length 4096) -> balanced; 256 x 1024 -> 1, 4 x 8192 -> 16
     assert lib.mla_decode_pick_splits(64, 8192, 152, 1) == 2
     assert lib.mla_decode_pick_splits(32, 1024, 152, 1) == 4
     assert lib.mla_decode_pick_splits(256, 8192, 152, 2) == 0
+    assert lib.mla_decode_pick_splits(128, 4096, 152, 1) == 0
+    assert lib.mla_decode_pick_splits(256, 1024, 152, 1) == 1
+    assert lib.mla_decode_pick_splits(4, 8192, 152, 1) == 16
 
 
 def test_pick_splits_rejects_bad_arguments(lib):
