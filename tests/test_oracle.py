@@ -387,3 +387,19 @@ def test_value_translation_adds_the_constant():
     o2, l2 = oracle.decode(q, k2, None, ip, synth.KV_BF16)
     np.testing.assert_allclose(o2, o1 + 2.0, rtol=0, atol=1e-12)
     np.testing.assert_array_equal(l1, l2)
+
+
+def test_multi_query_rows_that_see_no_token_give_zero():
+    # L = 2 cached tokens, q_len = 4: rows 0 and 1 see nothing (zeros, lse -inf), rows 2 and
+    # 3 see 1 and 2 tokens (row 2 returns the first token's value).
+    inp = synth.make_inputs(1, [2], synth.KV_BF16, seed=45)
+    q, qo = synth.make_queries([4], seed=46)
+    out, lse = oracle.decode_paged_multi(q, qo, inp.kv, None, np.array([0, 1], np.int32), np.array([0], np.int32),
+                                         np.array([2], np.int32), 8, synth.KV_BF16)
+    assert np.all(out[:2] == 0.0) and np.all(np.isneginf(lse[:2]))
+    assert np.all(np.isfinite(lse[2:]))
+    v0 = inp.kv[0, :DV].double().numpy()
+    for h in range(NH):
+        np.testing.assert_allclose(out[2, h], v0, rtol=0, atol=1e-12)
+    ref, _ = oracle.decode(q[3:4], inp.kv, None, np.array([0, 2], np.int32), synth.KV_BF16)
+    np.testing.assert_array_equal(out[3], ref[0])
