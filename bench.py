@@ -46,6 +46,8 @@ def parse():
     ap.add_argument("--config", type=int, default=DEFAULT_CONFIG)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the per-workload timings of all five workloads")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-seconds", type=float, default=60.0,
                     help="--impl reference: total oracle time over all warm-up and timed steps")
@@ -246,6 +248,86 @@ def run_reference(args, ws, rank):
     print(json.dumps(line), flush=True)
 
 
+def measure_workload(pkg, index, dev, steps, flush_l2, with_oracle=True):
+    """One workload of the five, in the library's own launch configuration: cold calls (L2
+    flushed before each), back-to-back warm calls, the split kernel's own time (library
+    events), KV GB/s and its fraction of the measured HBM peak, the ncu traffic ratio when
+    the committed counters match this kernel source, and the largest error against the
+    CPU oracle over a few sampled batch rows."""
+    import numpy as np
+    import torch
+    from mla_attention_decode_splitkv_gb300 import synth
+
+    spec = synth.CONFIGS[index]
+    inp = synth.make_config(index, device=dev, keep_src=False)
+    B = inp.batch
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    ns = pkg.resolve_splits(spec.num_splits, B, inp.rows // B, sms, spec.kv_dtype)
+    pkg.reserve_workspace(pkg.workspace_slots(B, ns, sms))
+    out = torch.empty((B, 16, 512), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def call():
+        rc = pkg.mla_decode(inp.q, inp.kv, inp.kv_scale, inp.kv_indptr, out, B, ns, spec.kv_dtype, stream)
+        if rc != pkg.MLA_OK:
+            raise pkg.MLAError(rc, "mla_decode")
+
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for i in range(steps):
+        flush_l2(i)
+        evs[i][0].record(stream)
+        call()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    cold_us = [a.elapsed_time(b) * 1e3 for a, b in evs]
+    # the same cold calls again, with the library's own events around its kernel
+    pkg.profile_begin()
+    for i in range(steps):
+        flush_l2(i)
+        call()
+    torch.cuda.synchronize()
+    split_ms_sum, _, ncalls = pkg.profile_end()
+    wevs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, b in wevs:
+        a.record(stream)
+        call()
+        b.record(stream)
+    torch.cuda.synchronize()
+    warm_us = [a.elapsed_time(b) * 1e3 for a, b in wevs]
+    if pkg.device_status(clear=True) != pkg.MLA_OK:
+        raise RuntimeError(f"kernel reported a pipeline timeout on {spec.name}")
+    kv_bytes = inp.kv_bytes()
+    kernel_us = split_ms_sum / max(1, ncalls) * 1e3
+    peak, _ = peaks()
+    res = {"workload": spec.name, "num_splits": ns, "kv_bytes_per_call": kv_bytes,
+           "cold_us_median": statistics.median(cold_us), "warm_us_median": statistics.median(warm_us),
+           "kernel_us": kernel_us, "gbs": kv_bytes / (statistics.median(cold_us) * 1e-6) / 1e9,
+           "kernel_gbs": kv_bytes / (kernel_us * 1e-6) / 1e9}
+    res["frac_of_measured_peak"] = res["kernel_gbs"] / peak
+    tr = ncu_traffic(spec.name)
+    res["traffic_ratio"] = None if tr is None else tr / kv_bytes
+    if with_oracle:
+        import oracle
+        ip = inp.kv_indptr.cpu().tolist()
+        rows = sorted({0, B - 1} | set(np.random.default_rng(index).choice(B, size=min(B, 2), replace=False).tolist()))
+        worst = 0.0
+        got_all = out.float().cpu().numpy()
+        for b in rows:
+            kv_rows = inp.kv[ip[b]:ip[b + 1]].cpu()
+            scale = None if inp.kv_scale is None else (
+                inp.kv_scale[ip[b]:ip[b + 1]].cpu() if spec.kv_dtype == synth.KV_MXFP4 else inp.kv_scale.cpu())
+            o, _ = oracle.attend(inp.q[b].cpu(), kv_rows, scale, spec.kv_dtype, 0, ip[b + 1] - ip[b])
+            worst = max(worst, float(np.abs(got_all[b] - o).max()))
+        res["max_abs_err_vs_oracle"] = worst
+        res["oracle_rows_checked"] = len(rows)
+    del inp, out
+    torch.cuda.empty_cache()
+    return res
+
+
 def config_dict(spec, inp, ns=None):
     """ns: the num_splits the timed calls use (None: not applicable, e.g. the oracle arm)."""
     from mla_attention_decode_splitkv_gb300 import synth
@@ -257,7 +339,9 @@ def config_dict(spec, inp, ns=None):
                            (f"{ns} per sequence (uniform)" if ns else "balanced (persistent, one CTA per SM)")
                            + ("" if spec.num_splits is not None else ", chosen by mla_decode_pick_splits")),
             "heads": 16, "head_dim": 576, "v_dim": 512, "kv_bytes_per_call": inp.kv_bytes(),
-            "l2": "flushed between timed calls (256 MiB write, then 256 MiB read to retire the dirty lines)"}
+            "l2": "flushed between timed calls (256 MiB write, then 256 MiB read to retire the dirty lines)",
+            "headline": "value and roofline are this workload's; the metric is per workload, and all five "
+                        "(in their own launch configurations) are in per_config"}
 
 
 def main():
@@ -442,6 +526,13 @@ def main():
         r, t, n, threads = oracle_sample_rate(inp, 12.0)
         line["cpu_baseline"] = {"value": r, "unit": "GB/s", "cores": threads, "kind": "oracle",
                                 "sample": f"{n} whole batch rows of the workload ({t:.1f} s)"}
+    if not args.no_per_config:
+        # The metric is per workload: every one of the five, in its own launch configuration.
+        del inp, q_d, kv_d, q_h, kv_h
+        torch.cuda.empty_cache()
+        line["per_config"] = [measure_workload(pkg, i, dev, max(10, min(args.steps, 30)), flush_l2,
+                                               with_oracle=not args.no_cpu_baseline)
+                              for i in range(len(synth.CONFIGS))]
     print(json.dumps(line), flush=True)
 
 

@@ -84,8 +84,14 @@ typedef enum {
  * not compute capability 10.3; MLA_ERR_NO_MEMORY if the workspace cannot grow;
  * MLA_ERR_CUDA if a launch fails (the CUDA error is cleared and its name is available
  * from mla_last_cuda_error()).
- * The partial-result workspace is library-owned (one per device, grow-only, guarded by a
- * mutex): growing it frees the old buffer with cudaFree, which synchronises the device.
+ * The partial-result workspace is library-owned (one per device, grow-only).  A call
+ * holds the library's workspace mutex from the workspace check until its kernel is
+ * enqueued, and a grow synchronises the device before it frees the old buffers, so
+ * concurrent calls from several host threads never see a freed buffer.  The kernels of
+ * every call on a device share that one workspace, though: two calls whose kernels may
+ * overlap on the GPU (different streams with no ordering between them) race on its
+ * partial results and piece counters and may return wrong results.  Order such calls
+ * (one stream, or events).
  */
 int mla_decode(const void* q, const void* kv, const void* kv_scale, const int32_t* kv_indptr,
                void* out, int batch, int num_splits, int kv_dtype, void* stream);
@@ -225,20 +231,25 @@ int mla_decode_profile_end(double* split_ms, double* call_ms, int* calls);
  *  - The first call on each device (with that device current) looks up the array's device
  *    address once (cudaGetSymbolAddress) and caches it; make that first call before any
  *    stream capture.
- *  - All calls share the one array, which keeps the previous call's contents; the call
- *    clears the status word it needs at zero (stream-ordered).  Calls that overlap on the
- *    GPU (different streams with no ordering between them) race on the array: serialise
- *    them on one stream or order them with events.
- *  - A pipeline timeout inside these kernels is recorded only in the array's status word,
- *    which mla_decode_device_status does not read.  After a timeout the piece counters
- *    may be left non-zero; the results of later calls that split sequences are then
- *    undefined until the process restarts (mla_decode: release and re-reserve the
- *    workspace, which re-zeroes its counters).
+ *  - All calls share the one array, which keeps the previous call's contents.  Every call
+ *    first clears, with one stream-ordered memset on `stream`, the status word and the
+ *    piece counters it uses, so a call that a pipeline timeout cut short leaves nothing
+ *    behind for the next one.  Calls that overlap on the GPU (different streams with no
+ *    ordering between them) race on the array: serialise them on one stream or order
+ *    them with events.
+ *  - A pipeline timeout (the limit set by mla_decode_set_wait_limit_ns) is recorded in
+ *    the array's own status word: read it with mla_decode_noalloc_status after the call
+ *    and before the next one (the next call clears it).
  * Errors as mla_decode, plus MLA_ERR_NO_MEMORY when the scratch is too small.
  */
 #define MLA_NOALLOC_MAX_SLOTS 512
 int mla_decode_noalloc(const void* q, const void* kv, const void* kv_scale, const int32_t* kv_indptr,
                        void* out, int batch, int num_splits, int kv_dtype, void* stream);
+
+/* Status of the most recent mla_decode_noalloc call on the current device: waits for the
+ * device (cudaMemcpy), returns MLA_OK or MLA_ERR_TIMEOUT, and resets the word if
+ * clear != 0.  Allocates nothing. */
+int mla_decode_noalloc_status(int clear);
 
 /* Static string for a status code; never NULL. */
 const char* mla_status_string(int status);

@@ -31,6 +31,7 @@ EXPORTED = (
     "mla_decode_profile_begin",
     "mla_decode_profile_end",
     "mla_decode_noalloc",
+    "mla_decode_noalloc_status",
     "mla_decode_paged",
     "mla_decode_paged_multi",
     "mla_status_string",
@@ -88,6 +89,8 @@ def load(path: str = LIB_PATH):
         lib.mla_decode_paged_multi.argtypes = [vp, vp, c_int, vp, vp, vp, vp, vp, c_int, vp, c_int, c_int, c_int, vp]
         lib.mla_decode_noalloc.restype = c_int
         lib.mla_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, c_int, c_int, c_int, vp]
+        lib.mla_decode_noalloc_status.restype = c_int
+        lib.mla_decode_noalloc_status.argtypes = [c_int]
         lib.mla_status_string.restype = ctypes.c_char_p
         lib.mla_status_string.argtypes = [c_int]
         lib.mla_last_cuda_error.restype = ctypes.c_char_p
@@ -238,3 +241,8 @@ def mla_decode_noalloc(q, kv, kv_scale, kv_indptr, out, batch: int, num_splits: 
     lib = load()
     return lib.mla_decode_noalloc(_ptr(q), _ptr(kv), _ptr(kv_scale), _ptr(kv_indptr), _ptr(out), int(batch),
                                   int(num_splits), int(kv_dtype), _stream_handle(stream))
+
+
+def noalloc_status(clear: bool = True) -> int:
+    """Status of the most recent mla_decode_noalloc call (MLA_OK or MLA_ERR_TIMEOUT)."""
+    return load().mla_decode_noalloc_status(1 if clear else 0)

@@ -3,6 +3,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
@@ -28,10 +29,10 @@ struct Workspace {
 
 std::mutex g_mu;
 Workspace g_ws[kMaxDevices];
-int g_sm_count[kMaxDevices];
-int g_cc[kMaxDevices];
-unsigned long long g_wait_limit_ns = 2000000000ull;
-int g_test_stall = 0;
+std::atomic<int> g_sm_count[kMaxDevices];
+std::atomic<int> g_cc[kMaxDevices];
+std::atomic<unsigned long long> g_wait_limit_ns{2000000000ull};
+std::atomic<int> g_test_stall{0};
 thread_local const char* t_last_cuda_error = "";
 
 // Optional timing of each call's split kernel (events recorded on the call's stream).
@@ -54,23 +55,26 @@ int device_info(int* dev_out, int* sms_out, int* cc_out) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return note_cuda(e);
   if (dev < 0 || dev >= kMaxDevices) return MLA_ERR_UNSUPPORTED;
-  if (g_sm_count[dev] == 0) {
-    int sms = 0, major = 0, minor = 0;
+  int sms = g_sm_count[dev].load(std::memory_order_acquire);
+  if (sms == 0) {
+    int major = 0, minor = 0;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return note_cuda(e);
     if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess) return note_cuda(e);
     if ((e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess) return note_cuda(e);
-    g_cc[dev] = major * 10 + minor;
-    g_sm_count[dev] = sms;
+    g_cc[dev].store(major * 10 + minor, std::memory_order_relaxed);
+    g_sm_count[dev].store(sms, std::memory_order_release);   // published after the capability
   }
   *dev_out = dev;
-  *sms_out = g_sm_count[dev];
-  *cc_out = g_cc[dev];
+  *sms_out = sms;
+  *cc_out = g_cc[dev].load(std::memory_order_relaxed);
   return MLA_OK;
 }
 
 // Grow-only workspace of `slots` partial results and `counters` per-sequence counters on
 // device `dev` (caller holds g_mu).  Counters are zeroed when allocated; the kernel leaves
-// them at zero after every complete call.
+// them at zero after every complete call.  A buffer is only replaced after a device-wide
+// synchronisation, so no kernel still in flight (on any stream, enqueued by any thread)
+// can use a freed buffer.
 int ensure_workspace(int dev, long long slots, long long counters) {
   Workspace& w = g_ws[dev];
   if (w.status == nullptr) {
@@ -78,7 +82,12 @@ int ensure_workspace(int dev, long long slots, long long counters) {
     if (e != cudaSuccess) { w.status = nullptr; cudaGetLastError(); return MLA_ERR_NO_MEMORY; }
     if ((e = cudaMemset(w.status, 0, sizeof(int))) != cudaSuccess) return note_cuda(e);
   }
-  if (counters > w.counters) {
+  const bool grow_counters = counters > w.counters, grow_slots = slots > w.slots;
+  if ((grow_counters && w.seq_count != nullptr) || (grow_slots && w.part_o != nullptr)) {
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return note_cuda(e);
+  }
+  if (grow_counters) {
     if (w.seq_count) { cudaFree(w.seq_count); w.seq_count = nullptr; }
     w.counters = 0;
     cudaError_t e = cudaMalloc(&w.seq_count, static_cast<size_t>(counters) * sizeof(int));
@@ -87,7 +96,7 @@ int ensure_workspace(int dev, long long slots, long long counters) {
     if ((e = cudaDeviceSynchronize()) != cudaSuccess) return note_cuda(e);
     w.counters = counters;
   }
-  if (slots <= w.slots) return MLA_OK;
+  if (!grow_slots) return MLA_OK;
   if (w.part_o) { cudaFree(w.part_o); w.part_o = nullptr; }
   if (w.part_lse) { cudaFree(w.part_lse); w.part_lse = nullptr; }
   w.slots = 0;
@@ -144,6 +153,8 @@ static int encode_map(CUtensorMap* map, const void* kv, int kv_dtype, bool rope,
   return r == CUDA_SUCCESS ? MLA_OK : MLA_ERR_CUDA;
 }
 
+unsigned long long pipeline_wait_limit_ns() { return g_wait_limit_ns.load(); }
+
 int encode_kv_map(CUtensorMap* map, const void* kv, int kv_dtype) { return encode_map(map, kv, kv_dtype, false); }
 int encode_rope_map(CUtensorMap* map, const void* kv) { return encode_map(map, kv, MLA_KV_FP8_E4M3, true); }
 int encode_kv_map_rows(CUtensorMap* map, const void* kv, int kv_dtype, int box_rows) {
@@ -171,7 +182,7 @@ const char* mla_status_string(int status) {
 
 const char* mla_last_cuda_error(void) { return t_last_cuda_error; }
 
-void mla_decode_set_wait_limit_ns(unsigned long long ns) { g_wait_limit_ns = ns ? ns : 1ull; }
+void mla_decode_set_wait_limit_ns(unsigned long long ns) { g_wait_limit_ns.store(ns ? ns : 1ull); }
 
 void mla_decode_set_test_stall(int on) { g_test_stall = on ? 1 : 0; }
 
@@ -271,13 +282,12 @@ static int decode_impl(const void* q, const void* kv, const void* kv_scale, cons
   const long long grid_ll = ns >= 1 ? static_cast<long long>(batch) * ns : sms;
   if (grid_ll > 0x7fffffffLL) return MLA_ERR_INVALID_ARG;
 
-  Workspace ws;
-  {
-    std::lock_guard<std::mutex> lk(g_mu);
-    rc = ensure_workspace(dev, slots_needed(batch, ns, sms), ns == 1 ? 0 : batch);
-    if (rc) return rc;
-    ws = g_ws[dev];
-  }
+  // The workspace lock is held until the launch is enqueued: a concurrent call (or a
+  // reserve / release) on another host thread cannot replace these buffers in between.
+  std::lock_guard<std::mutex> ws_lock(g_mu);
+  rc = ensure_workspace(dev, slots_needed(batch, ns, sms), ns == 1 ? 0 : batch);
+  if (rc) return rc;
+  const Workspace ws = g_ws[dev];
 
   mla::DecodeParams p;
   const int box_rows = page_size != 0 ? page_size : mla::kBN;
@@ -307,8 +317,8 @@ static int decode_impl(const void* q, const void* kv, const void* kv_scale, cons
   p.num_splits = ns;
   p.num_ctas = static_cast<int>(grid_ll);
   p.logit_scale_log2 = static_cast<float>((1.0 / std::sqrt(static_cast<double>(mla::kDim))) * 1.4426950408889634);
-  p.wait_limit_ns = g_wait_limit_ns;
-  p.test_stall = g_test_stall;
+  p.wait_limit_ns = g_wait_limit_ns.load();
+  p.test_stall = g_test_stall.load();
 
   ProfRecord rec{nullptr, nullptr, nullptr};
   bool prof = false;

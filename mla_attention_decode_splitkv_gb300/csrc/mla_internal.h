@@ -60,6 +60,9 @@ int encode_kv_map(CUtensorMap* map, const void* kv, int kv_dtype);
 // fp8 caches: the same rows with 64-byte boxes and 64-byte swizzle (the rope chunk).
 int encode_rope_map(CUtensorMap* map, const void* kv);
 
+// The pipeline wait limit set by mla_decode_set_wait_limit_ns (default 2 s).
+unsigned long long pipeline_wait_limit_ns();
+
 // Launches the split kernel for kv_dtype (geometry per dtype is internal to mla_split.cu).
 cudaError_t launch_split(int kv_dtype, const DecodeParams& p, int grid, cudaStream_t stream);
 // The same for a paged cache (page size 8 .. 128, a power of two; boxes of page_size rows).

@@ -33,13 +33,35 @@ constexpr size_t kCounterBytes = static_cast<size_t>(MLA_NOALLOC_MAX_SLOTS) * si
 constexpr size_t kNoallocScratchBytes =
     static_cast<size_t>(MLA_NOALLOC_MAX_SLOTS) * (kSlotBytes + kLseBytes) + kStatusBytes + kCounterBytes;
 
-// Layout: [status word (256 B)] [partial O: slots x 16 x 512 fp32] [partial lse: slots x 16 fp32]
-//         [piece counters: slots x int32; zero at load, left at zero by every complete call]
-// A call needing partial slots has batch <= slots, so the counters always fit.
+// Layout: [status word (256 B)] [piece counters: slots x int32] [partial O: slots x 16 x 512 fp32]
+//         [partial lse: slots x 16 fp32]
+// The status word and the counters are contiguous so that one stream-ordered memset per
+// call re-arms both (a call that splits sequences uses counters [0, batch), and a call
+// needing partial slots has batch <= slots, so the counters always fit).
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
+
+constexpr size_t kCountersOffset = kStatusBytes;
+constexpr size_t kPartOOffset = kStatusBytes + kCounterBytes;
+constexpr size_t kPartLseOffset = kPartOOffset + static_cast<size_t>(MLA_NOALLOC_MAX_SLOTS) * kSlotBytes;
+static_assert(kPartOOffset % 256 == 0, "partial outputs must stay 16-byte aligned");
 
 std::mutex g_mu;
 void* g_addr[kMaxDevices];
+
+// Device address of the scratch array on the current device (looked up once per device,
+// with that device current); nullptr on failure.
+unsigned char* scratch_base(int dev) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_addr[dev] == nullptr) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    g_addr[dev] = ptr;
+  }
+  return static_cast<unsigned char*>(g_addr[dev]);
+}
 }  // namespace
 
 extern "C" int mla_decode_noalloc(const void* q, const void* kv, const void* kv_scale, const int32_t* kv_indptr,
@@ -66,28 +88,18 @@ extern "C" int mla_decode_noalloc(const void* q, const void* kv, const void* kv_
   const long long slots = ns == 1 ? 0 : (ns >= 2 ? static_cast<long long>(batch) * ns : static_cast<long long>(batch) + sms - 1);
   if (slots > MLA_NOALLOC_MAX_SLOTS || grid > 0x7fffffffLL) return MLA_ERR_NO_MEMORY;  // beyond the fixed scratch
 
-  void* base = nullptr;
-  {
-    std::lock_guard<std::mutex> lk(g_mu);
-    if (g_addr[dev] == nullptr) {
-      void* ptr = nullptr;
-      if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) {
-        cudaGetLastError();
-        return MLA_ERR_CUDA;
-      }
-      g_addr[dev] = ptr;
-    }
-    base = g_addr[dev];
-  }
-  unsigned char* b = static_cast<unsigned char*>(base);
+  unsigned char* b = scratch_base(dev);
+  if (b == nullptr) return MLA_ERR_CUDA;
   int* status = reinterpret_cast<int*>(b);
-  float* part_o = reinterpret_cast<float*>(b + kStatusBytes);
-  float* part_lse = reinterpret_cast<float*>(b + kStatusBytes + static_cast<size_t>(MLA_NOALLOC_MAX_SLOTS) * kSlotBytes);
-  int* seq_count = reinterpret_cast<int*>(b + kStatusBytes +
-                                          static_cast<size_t>(MLA_NOALLOC_MAX_SLOTS) * (kSlotBytes + kLseBytes));
+  int* seq_count = reinterpret_cast<int*>(b + kCountersOffset);
+  float* part_o = reinterpret_cast<float*>(b + kPartOOffset);
+  float* part_lse = reinterpret_cast<float*>(b + kPartLseOffset);
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // The status word must start each call at zero (the kernels only ever set bits in it).
-  if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess) { cudaGetLastError(); return MLA_ERR_CUDA; }
+  // Each call starts from a zero status word and zero piece counters: one stream-ordered
+  // memset over both (the kernels only ever set status bits, and a call cut short by a
+  // pipeline timeout may leave its counters mid-count).
+  const size_t clear_bytes = kStatusBytes + (ns == 1 ? 0 : static_cast<size_t>(batch) * sizeof(int));
+  if (cudaMemsetAsync(status, 0, clear_bytes, st) != cudaSuccess) { cudaGetLastError(); return MLA_ERR_CUDA; }
 
   mla::DecodeParams p;
   int rc = mla::encode_kv_map(&p.tmap, kv, kv_dtype);
@@ -106,7 +118,7 @@ extern "C" int mla_decode_noalloc(const void* q, const void* kv, const void* kv_
   p.num_splits = ns;
   p.num_ctas = static_cast<int>(grid);
   p.logit_scale_log2 = static_cast<float>((1.0 / std::sqrt(static_cast<double>(mla::kDim))) * 1.4426950408889634);
-  p.wait_limit_ns = 2000000000ull;
+  p.wait_limit_ns = mla::pipeline_wait_limit_ns();
   p.test_stall = 0;
   p.page_size = 0;
   p.page_shift = 0;
@@ -116,4 +128,15 @@ extern "C" int mla_decode_noalloc(const void* q, const void* kv, const void* kv_
   p.num_seqs = 0;
   if (mla::launch_split(kv_dtype, p, static_cast<int>(grid), st) != cudaSuccess) { cudaGetLastError(); return MLA_ERR_CUDA; }
   return MLA_OK;
+}
+
+extern "C" int mla_decode_noalloc_status(int clear) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) { cudaGetLastError(); return MLA_ERR_CUDA; }
+  unsigned char* b = scratch_base(dev);
+  if (b == nullptr) return MLA_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, b, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) { cudaGetLastError(); return MLA_ERR_CUDA; }
+  if (clear && v && cudaMemset(b, 0, sizeof(int)) != cudaSuccess) { cudaGetLastError(); return MLA_ERR_CUDA; }
+  return (v & mla::kStatusTimeout) ? MLA_ERR_TIMEOUT : MLA_OK;
 }

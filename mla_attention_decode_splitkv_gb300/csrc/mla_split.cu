@@ -32,6 +32,7 @@
 // all roles leave their loops; in-flight copies and MMAs are drained (bounded) before the
 // tensor memory is released.
 #include <cstddef>
+#include <mutex>
 #include <type_traits>
 
 #include <cuda_bf16.h>
@@ -120,6 +121,9 @@ constexpr int kPBytes = 4096;      // one P^T buffer: [128 tokens x 32 B] SW32
 constexpr int kSlabBytes = 8192;   // MXFP4 staging: 64 packed bytes (4 blocks) of each of 128 rows, SW64
 constexpr int kSlabs = 7;          // slab ring: a tile is 5 slabs (4 value chunks + rope)
 constexpr int kLutCount = 14;      // e2m1 -> e4m3 tables for block shifts 0..-12, then zero
+// Smallest MXFP4 row exponent e_i (biased): blocks more than 12 binades below it decode to
+// zero, so a row whose largest block is below 2^-64 (|value| < 6 * 2^-64) reads as zeros.
+constexpr int kRowExpFloor = 127 - 64;
 constexpr int kRopeBytes = 8192;   // one rope slot: [128 rows x 64 B] SW64 (fp8 cache bytes / MXFP4 carrier)
 
 struct SharedState {
@@ -707,7 +711,10 @@ __device__ void run_dequant(const DecodeParams& p, SharedState* sh, uint8_t* rin
 #pragma unroll
           for (int j = 0; j < 9; ++j) sc[j] = __ldg(sp + j);
         }
-        emax = 0;
+        // The row exponent never goes below kRowExpFloor: a row whose blocks all sit below
+        // 2^(kRowExpFloor - 127) (an all-zero row with e8m0 code 0, for instance) keeps a
+        // PV weight 2^(logit + e_i - 127) inside fp32's normal range.
+        emax = kRowExpFloor;
 #pragma unroll
         for (int j = 0; j < 9; ++j) emax = max(emax, max(static_cast<int>(sc[j] & 0xFF), static_cast<int>(sc[j] >> 8)));
 #pragma unroll
@@ -752,6 +759,13 @@ __device__ void run_dequant(const DecodeParams& p, SharedState* sh, uint8_t* rin
         uint4 v[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) v[q] = ld_shared_v4_volatile(srow + ((q ^ ssw) << 4));
+        // The slab goes back to the producer as soon as it has been read.  Its next fill is
+        // an async-proxy (TMA) write to the bytes these generic-proxy loads just read, and
+        // the mbarrier hand-off alone does not order the two proxies: the proxy fence comes
+        // first.  (Without it, about one balanced-mode call in twenty with one- or two-tile
+        // segments read a few MX blocks of a value chunk from the slab's next fill.)
+        fence_proxy_async_smem();
+        warp_arrive(smem_u32(&sh->slab_empty[si]));
         if (rc) {   // the rope buffer was last read by the QK MMAs of tile g - 1
           ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&sh->rope_empty[0]), (g & 1) ^ 1, abortf, p.status,
                                                 p.wait_limit_ns));
@@ -778,12 +792,6 @@ __device__ void run_dequant(const DecodeParams& p, SharedState* sh, uint8_t* rin
           }
           sh->etok[g & 3][di] = emax;
         }
-        // The slab is released only after this chunk's carrier stores.  Released right after
-        // its loads (the loads being complete, or not), about one call in fifteen of the
-        // balanced mode with one- or two-tile segments had a few MX blocks of one value chunk
-        // wrong; with the release here none in 1,500 calls.  A proxy fence after the PV wait,
-        // per-thread publish arrivals and a data-dependent early release did not remove it.
-        warp_arrive(smem_u32(&sh->slab_empty[si]));
         fence_proxy_async_smem();
         warp_arrive(rc ? smem_u32(&sh->rope_full[0]) : smem_u32(&sh->full[vslot0 + c]));
       }
@@ -1324,7 +1332,11 @@ __device__ void run_softmax(const DecodeParams& p, SharedState* sh, uint8_t* qs,
           *reinterpret_cast<uint4*>(prow + (((h0 / 8 + c) ^ sw) << 4)) =
               make_uint4(wv[4 * c], wv[4 * c + 1], wv[4 * c + 2], wv[4 * c + 3]);
       } else {
+        // Softmax sum: fp8 caches add the e4m3-rounded P (the values the PV MMAs weight V
+        // with).  MXFP4 rows add the fp32 P * 2^-eadd: a row of small magnitude (eadd << 0)
+        // can carry a large softmax weight with a PV weight too small for e4m3.
         const float einv = pow2i(-static_cast<int>(eadd) - 4);   // 2^-eadd / 16
+        const float escale = pow2i(-static_cast<int>(eadd));      // 2^-eadd
         uint32_t hw[H / 4], lw[H / 4];
 #pragma unroll
         for (int j = 0; j < H / 4; ++j) {
@@ -1336,9 +1348,14 @@ __device__ void run_softmax(const DecodeParams& p, SharedState* sh, uint8_t* qs,
             const uint32_t hp = pack_e4m3x2(y0, y1);
             const float2 hd = unpack_e4m3x2(hp);
             const uint32_t lp = pack_e4m3x2((y0 - hd.x) * 16.f, (y1 - hd.y) * 16.f);
-            const float2 ld = unpack_e4m3x2(lp);
-            lpart[h] += fmaf(ld.x, 0.0625f, hd.x) * einv;
-            lpart[h + 1] += fmaf(ld.y, 0.0625f, hd.y) * einv;
+            if constexpr (KV == 2) {
+              lpart[h] = fmaf(P[h], escale, lpart[h]);
+              lpart[h + 1] = fmaf(P[h + 1], escale, lpart[h + 1]);
+            } else {
+              const float2 ld = unpack_e4m3x2(lp);
+              lpart[h] += fmaf(ld.x, 0.0625f, hd.x) * einv;
+              lpart[h + 1] += fmaf(ld.y, 0.0625f, hd.y) * einv;
+            }
             a |= hp << (8 * k);
             b |= lp << (8 * k);
           }
@@ -1466,6 +1483,12 @@ __global__ void __launch_bounds__(Cfg<KV>::kThreads, 1) mla_split_kernel(const _
     tmem_alloc(smem_u32(&sh->tmem_base), C::kTmemCols);
     tmem_relinquish();
   }
+  // Programmatic dependent launch: the set-up above (barrier init, TMEM allocation) may run
+  // while the previous kernel in the stream finishes; every global memory access of this
+  // kernel comes after this wait.  The next kernel may begin its own set-up as soon as
+  // every CTA of this one is running.
+  grid_dep_launch_dependents();
+  grid_dep_wait();
   if (warp == 0 && p.num_splits < 1) {
     const long long total = static_cast<long long>(p.kv_indptr[p.batch]) * (PG ? p.page_size : 1);
     const int Ge = balanced_ctas(total, p.num_ctas);
@@ -1514,28 +1537,52 @@ __global__ void __launch_bounds__(Cfg<KV>::kThreads, 1) mla_split_kernel(const _
   }
 }
 
+constexpr int kMaxDevices = 64;
+
+// Per-device, once: the kernel's dynamic shared-memory limit (a per-function attribute
+// that each device context keeps) and, for MXFP4, the register-split check.  Thread-safe;
+// the outcome of the first attempt on a device is kept.
 template <int KV, bool PG>
-cudaError_t launch_split_t(const DecodeParams& p, int grid, cudaStream_t stream) {
-  static int configured_device = -1;  // attribute is per function; set once per device id
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (configured_device != dev) {
-    e = cudaFuncSetAttribute(mla_split_kernel<KV, PG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem_bytes<KV>()));
-    if (e != cudaSuccess) return e;
-    if constexpr (KV == 2) {
+cudaError_t configure_once(int dev) {
+  static std::once_flag once[kMaxDevices];
+  static cudaError_t result[kMaxDevices];
+  std::call_once(once[dev], [dev] {
+    cudaError_t e = cudaFuncSetAttribute(mla_split_kernel<KV, PG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem_bytes<KV>()));
+    if (e == cudaSuccess && KV == 2) {
       // The register split's increases only complete if the CTA launched with at least the
       // registers the split hands out: refuse to launch otherwise.
       cudaFuncAttributes fa;
       e = cudaFuncGetAttributes(&fa, mla_split_kernel<KV, PG>);
-      if (e != cudaSuccess) return e;
-      if (fa.numRegs * Cfg<KV>::kThreads < Cfg<KV>::kRegsNeeded) return cudaErrorInvalidConfiguration;
+      if (e == cudaSuccess && fa.numRegs * Cfg<KV>::kThreads < Cfg<2>::kRegsNeeded) e = cudaErrorInvalidConfiguration;
     }
-    configured_device = dev;
-  }
-  mla_split_kernel<KV, PG><<<grid, Cfg<KV>::kThreads, smem_bytes<KV>(), stream>>>(p);
-  return cudaGetLastError();
+    result[dev] = e;
+  });
+  return result[dev];
+}
+
+template <int KV, bool PG>
+cudaError_t launch_split_t(const DecodeParams& p, int grid, cudaStream_t stream) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if ((e = configure_once<KV, PG>(dev)) != cudaSuccess) return e;
+  // Launched with programmatic stream serialisation: the kernel's set-up overlaps the tail
+  // of the previous kernel in the stream (see grid_dep_wait in the kernel).
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(Cfg<KV>::kThreads);
+  cfg.dynamicSmemBytes = smem_bytes<KV>();
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, mla_split_kernel<KV, PG>, p);
+  if (e != cudaSuccess) cudaGetLastError();
+  return e;
 }
 
 }  // namespace

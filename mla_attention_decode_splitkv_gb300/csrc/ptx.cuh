@@ -20,6 +20,17 @@ __device__ __forceinline__ uint64_t globaltimer() {
   return t;
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// Waits until the grids this launch depends on (the previous kernel in the stream, when the
+// launch allows programmatic serialisation) have completed and their writes are visible;
+// returns at once when there is no such dependency.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the next grid in the stream begin launching (its own grid_dep_wait still orders its
+// memory accesses after this grid's completion).
+__device__ __forceinline__ void grid_dep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");

@@ -176,7 +176,8 @@ def paged_rows(page_indptr, page_indices, last_page_len, page_size: int):
     """Physical cache rows of every sequence of a paged cache, in token order.
 
     The page table of the paged MLA decode interface (amd-mixed-mla submission 700955,
-    persistent-state setup; submission 701211 harness inputs): sequence b owns the pages
+    `_get_a16w8_persistent_state`: a page-level kv_indptr, kv_indices and kv_last_page_len
+    for a given page_size): sequence b owns the pages
     page_indices[page_indptr[b] : page_indptr[b+1]], all full except the last, which holds
     last_page_len[b] tokens.  Token t of sequence b therefore lives at physical row
     page_indices[page_indptr[b] + t // page_size] * page_size + t % page_size.
