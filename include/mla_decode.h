@@ -159,21 +159,27 @@ int mla_decode_paged_multi(const void* q, const int32_t* qo_indptr, int total_q,
                            void* stream);
 
 /*
- * mla_decode_pick_splits -- host-only choice of num_splits for mla_decode.
- *     ns = min(floor(num_sms / batch), ceil(kv_len_hint / 256), floor(sqrt(kv_len_hint / 32)));
- *     returns ns if ns >= 2; else 1 if kv_len_hint <= 2048; else 0 (the balanced mode).
- * That is: one wave of uniform splits (each CTA works on one contiguous piece of one
- * sequence, every piece at least two 128-row tiles, at most floor(sqrt(L/32)) pieces
- * because the merge of a sequence reads all its pieces in one CTA) when the batch leaves
- * at least two SMs per sequence.  Otherwise one split per sequence for short sequences,
- * and one CTA per SM over the concatenated cached rows (which also suits ragged batches)
- * for long ones.  (Measured on GB300: a CTA that crosses from one sequence into the next
- * pays a pipeline drain, so uniform splits beat the balanced mode for short uniform
- * batches, e.g. 256 x 1024 fp8 47.7 against 62.1 us; 16 pieces beat 32 at 4 x 8192.  The
- * pages' analytic split model, submission 700955 `_estimate_custom_splits`, targets
- * another GPU and is not used.)
- * Returns ns = 0, 1 or >= 2, or MLA_ERR_INVALID_ARG for batch <= 0, kv_len_hint < 0,
- * num_sms <= 0 or an unknown kv_dtype.
+ * mla_decode_pick_splits -- host-only choice of num_splits for mla_decode on a batch of
+ * `batch` sequences of about kv_len_hint tokens each, on a GPU with num_sms SMs.
+ * The split model of amd-mixed-mla submission 700955 (`_compute_custom_splits`: utilisation
+ * of the CTA slots times L / (L + per-split overhead)), with this kernel's own costs counted
+ * in cache rows (a row = the bytes of one cached token: 1152 bf16, 576 fp8, 306 MXFP4, which
+ * is why kv_dtype is an argument):
+ *   c = 32,832 / row   one piece (16 x 513 fp32 partial output and log-sum-exp), written once
+ *                      and read once by the CTA that merges the sequence's ns pieces;
+ *   w = 222,000 / row  one wave of CTAs: a CTA's start-up and final drain (about 2 + 3 us,
+ *                      measured) times one SM's share of the HBM bandwidth (6.76 TB/s / 152);
+ *   x = 300,000 / row  a CTA moving from one sequence to the next in the balanced mode (the
+ *                      pipeline drain and refill: about 6.7 us, measured, times the same share).
+ * Time of the slowest CTA, in rows, with B = batch, L = kv_len_hint, S = num_sms:
+ *   uniform ns (1 <= ns <= ceil(L / 128)):  waves * (chunk + w + c) + ns * c   (no c terms for ns = 1),
+ *     waves = ceil(B ns / S), chunk = ceil(L / ns) rounded up to 128-row tiles;
+ *   balanced: R + w + s c + (s - 1) x + p c,  R = B L / S, s = ceil(R / L) + 1, p = ceil(L / R) + 1.
+ * Returns the uniform ns of least time (the smallest on ties), or 0 (the balanced mode) when
+ * that is faster.  The hint describes a batch of equal lengths; for a batch whose lengths
+ * vary widely call mla_decode with num_splits <= 0 (the balanced mode) directly.
+ * Returns MLA_ERR_INVALID_ARG for batch <= 0, kv_len_hint < 0, num_sms <= 0 or an unknown
+ * kv_dtype.
  */
 int mla_decode_pick_splits(int batch, int kv_len_hint, int num_sms, int kv_dtype);
 

@@ -188,23 +188,46 @@ void mla_decode_set_test_stall(int on) { g_test_stall = on ? 1 : 0; }
 
 int mla_decode_pick_splits(int batch, int kv_len_hint, int num_sms, int kv_dtype) {
   if (batch <= 0 || kv_len_hint < 0 || num_sms <= 0 || kv_dtype < 0 || kv_dtype > 2) return MLA_ERR_INVALID_ARG;
-  // One wave of uniform splits (every CTA one segment, no segment switches inside a CTA)
-  // when the batch leaves at least two SMs per sequence.  Each piece keeps >= 2 tiles, and
-  // the pieces of a sequence are at most floor(sqrt(L / 32)): its merge (one CTA reading
-  // every piece) grows with ns while the streaming time shrinks as L / ns.
-  const long long L = kv_len_hint;
-  const long long per_seq = num_sms / batch;
-  const long long by_tiles = (L + 2 * mla::kBN - 1) / (2 * mla::kBN);
-  const long long q = L / 32;
-  long long by_merge = static_cast<long long>(std::sqrt(static_cast<double>(q)));
-  while (by_merge * by_merge > q) --by_merge;
-  while ((by_merge + 1) * (by_merge + 1) <= q) ++by_merge;
-  const long long ns = std::min(per_seq, std::min(by_tiles, by_merge));
-  if (ns >= 2) return static_cast<int>(ns);
-  // More sequences than half the SMs: one CTA per short sequence (the balanced mode's CTAs
-  // would cross many sequence boundaries); the balanced persistent mode for long or
-  // ragged ones.
-  return L <= 2048 ? 1 : 0;
+  // The split model of amd-mixed-mla submission 700955 (`_compute_custom_splits`: score =
+  // utilisation of the CTA slots x L / (L + per-split overhead)), with this kernel's costs
+  // written out in rows of the cache (one row = the bytes one cached token occupies):
+  //  * a piece (partial output + log-sum-exp, 16 x 513 fp32) is written once, c rows, and
+  //    read once by the CTA that merges its sequence, which reads all ns pieces in turn;
+  //  * every wave of CTAs pays a CTA's start-up before its first copy and its drain after the
+  //    last one: w rows, that latency (about 2 + 3 us, measured on GB300) times one SM's
+  //    share of the HBM bandwidth (6.76 TB/s / 152 SMs);
+  //  * in the balanced mode a CTA that moves from one sequence to the next drains and
+  //    refills its pipeline (epilogue, piece count, q restaging): x rows, the crossing's
+  //    measured latency (about 6.7 us) times the same share.
+  // Time of the slowest CTA, in rows:
+  //   uniform ns:  waves * (chunk + w + c [ns > 1]) + ns * c [ns > 1],
+  //                waves = ceil(B ns / SMs), chunk = L / ns rounded up to 128-row tiles;
+  //   balanced:    R + w + s c + (s - 1) x + p c,  R = B L / SMs rows per CTA, s = ceil(R / L) + 1
+  //                sequences touched by a CTA, p = ceil(L / R) + 1 pieces per sequence.
+  // The best uniform split count is returned, or 0 when the balanced mode is faster.
+  // kv_dtype sets the row size, hence c, w and x in rows.
+  static constexpr double kPieceBytes = static_cast<double>(mla::kHeads) * (mla::kDimV + 1) * 4.0;  // 32,832
+  static constexpr double kWaveBytes = 222e3;
+  static constexpr double kCrossBytes = 300e3;
+  const double row = kv_dtype == MLA_KV_BF16 ? 2.0 * mla::kDim
+                     : kv_dtype == MLA_KV_FP8_E4M3 ? 1.0 * mla::kDim
+                     : static_cast<double>(mla::kMxPacked + mla::kMxScales);
+  const double c = kPieceBytes / row, w = kWaveBytes / row, x = kCrossBytes / row;
+  const long long L = std::max(kv_len_hint, 1), B = batch, S = num_sms, BN = mla::kBN;
+  const long long ns_max = std::min<long long>(mla::kMaxSplits, (L + BN - 1) / BN);
+  const double useful = static_cast<double>(B) * static_cast<double>(L) / static_cast<double>(S);
+  int best_ns = 1;
+  double best_t = 0.0;
+  for (long long ns = 1; ns <= ns_max; ++ns) {
+    const long long waves = (B * ns + S - 1) / S;
+    const long long chunk = ((L + ns - 1) / ns + BN - 1) / BN * BN;
+    const double t = waves * (chunk + w + (ns > 1 ? c : 0.0)) + (ns > 1 ? ns * c : 0.0);
+    if (ns == 1 || t < best_t) { best_t = t; best_ns = static_cast<int>(ns); }
+  }
+  const double R = useful;
+  const double s_seq = std::ceil(R / L) + 1.0, pieces = std::ceil(L / R) + 1.0;
+  const double t_bal = R + w + s_seq * c + (s_seq - 1.0) * x + pieces * c;
+  return t_bal < best_t ? 0 : best_ns;
 }
 
 int mla_decode_workspace_slots(int batch, int num_splits, int num_sms) {

@@ -119,7 +119,12 @@ static_assert(Cfg<2>::kRegsNeeded <= 65536, "MXFP4 register split exceeds the re
 
 constexpr int kPBytes = 4096;      // one P^T buffer: [128 tokens x 32 B] SW32
 constexpr int kSlabBytes = 8192;   // MXFP4 staging: 64 packed bytes (4 blocks) of each of 128 rows, SW64
-constexpr int kSlabs = 7;          // slab ring: a tile is 5 slabs (4 value chunks + rope)
+constexpr int kSlabs = 5;          // slab ring: a tile is 5 slabs (4 value chunks + rope)
+// MXFP4 tiles are fetched, converted and multiplied rope chunk first: its carrier buffer is
+// freed by the QK MMAs of the previous tile, so the dequantisation of tile g can start on it
+// while the PV MMAs of tile g - 2 still read the value slots it needs next.
+// Chunk i of an MXFP4 tile in fetch / conversion / QK order (4 = the rope chunk).
+__host__ __device__ constexpr int mx_chunk(int i) { return i == 0 ? 4 : i - 1; }
 constexpr int kLutCount = 14;      // e2m1 -> e4m3 tables for block shifts 0..-12, then zero
 // Smallest MXFP4 row exponent e_i (biased): blocks more than 12 binades below it decode to
 // zero, so a row whose largest block is below 2^-64 (|value| < 6 * 2^-64) reads as zeros.
@@ -540,7 +545,8 @@ __device__ void run_producer_mx(const DecodeParams& p, SharedState* sh, uint8_t*
       const Window w = tile_window<2, PG>(p, s, t);
       int lrow = 0;
       if constexpr (PG) lrow = lane_page_row<PG>(p, s, t, lane);
-      for (int c = 0; c < 5; ++c) {
+      for (int i = 0; i < 5; ++i) {
+        const int c = mx_chunk(i);
         if (!producer_wait<PG>(smem_u32(&sh->slab_empty[slot]), phase ^ 1, abortf, p.status, p.wait_limit_ns)) {
           ok = false;
           break;
@@ -732,23 +738,56 @@ __device__ void run_dequant(const DecodeParams& p, SharedState* sh, uint8_t* rin
           for (int j = 0; j < 9; ++j) scn[j] = __ldg(sp + j);
         }
       }
-      const uint32_t vslot0 = (g & 1) * C::kRingPT;
       // Fully unrolled over the 18 blocks so that the block indices are constants.
       // Rolled over the five chunks (the loop body holds one value chunk and the rope chunk),
       // so that the dequantisation code stays small next to the softmax and issue loops
       // sharing the SM's instruction cache.  Shift-table indices of blocks 0-15 come from
       // one 64-bit register by a run-time shift.
       const uint64_t kv64 = static_cast<uint64_t>(kpk[0]) | (static_cast<uint64_t>(kpk[1]) << 32);
+      // The rope chunk comes first (the producer fetches it first and the QK MMAs take it
+      // first): its carrier buffer was last read by the QK MMAs of tile g - 1, so it does
+      // not wait for the PV MMAs of tile g - 2, which the value chunks below do.
+      {
+        const uint32_t si = slab_i, sph = slab_ph;
+        if (++slab_i == kSlabs) { slab_i = 0; slab_ph ^= 1u; }
+        ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&sh->slab_full[si]), sph, abortf, p.status, p.wait_limit_ns));
+        if (!ok) break;
+        const uint32_t srow = smem_u32(slabs + si * kSlabBytes + di * 64);
+        const uint4 v0 = ld_shared_v4_volatile(srow + ((0 ^ ssw) << 4));
+        const uint4 v1 = ld_shared_v4_volatile(srow + ((1 ^ ssw) << 4));
+        // The slab goes back to the producer as soon as it has been read.  Its next fill is
+        // an async-proxy (TMA) write to the bytes these generic-proxy loads just read, and
+        // the mbarrier hand-off alone does not order the two proxies: the proxy fence comes
+        // first.  (Without it, about one balanced-mode call in twenty with one- or two-tile
+        // segments read a few MX blocks of a value chunk from the slab's next fill.)
+        fence_proxy_async_smem();
+        warp_arrive(smem_u32(&sh->slab_empty[si]));
+        ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&sh->rope_empty[0]), (g & 1) ^ 1, abortf, p.status,
+                                              p.wait_limit_ns));
+        if (!ok) break;
+        uint8_t* dst = rope + di * 64;                                        // [128 x 64 B] SW64
+        uint4 lo, hi;
+        deq_block(v0, sh->lut[kpk[2] & 15u], lo, hi);
+        *reinterpret_cast<uint4*>(dst + ((0 ^ ssw) << 4)) = lo;
+        *reinterpret_cast<uint4*>(dst + ((1 ^ ssw) << 4)) = hi;
+        deq_block(v1, sh->lut[(kpk[2] >> 4) & 15u], lo, hi);
+        *reinterpret_cast<uint4*>(dst + ((2 ^ ssw) << 4)) = lo;
+        *reinterpret_cast<uint4*>(dst + ((3 ^ ssw) << 4)) = hi;
+        sh->etok[g & 3][di] = emax;
+        fence_proxy_async_smem();
+        warp_arrive(smem_u32(&sh->rope_full[0]));
+      }
       // The value slots of tile g were last read by tile g - 2: one wait on its PV completion
       // covers all four (QK of g - 2 completed before its softmax, hence before its PV).
+      static_assert(C::kRing == 2 * C::kRingPT, "the MXFP4 value ring holds exactly two tiles");
       if (g >= 2) {
         ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&sh->pv_done[g & 1]), ((g >> 1) & 1) ^ 1, abortf, p.status,
                                               p.wait_limit_ns));
         if (!ok) break;
       }
+      const uint32_t vslot0 = (g & 1) * C::kRingPT;
 #pragma unroll 1
-      for (int c = 0; c < C::kSPT; ++c) {
-        const bool rc = (c == C::kSPT - 1);
+      for (int c = 0; c < C::kRingPT; ++c) {
         const uint32_t si = slab_i, sph = slab_ph;
         if (++slab_i == kSlabs) { slab_i = 0; slab_ph ^= 1u; }
         ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&sh->slab_full[si]), sph, abortf, p.status, p.wait_limit_ns));
@@ -759,41 +798,19 @@ __device__ void run_dequant(const DecodeParams& p, SharedState* sh, uint8_t* rin
         uint4 v[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) v[q] = ld_shared_v4_volatile(srow + ((q ^ ssw) << 4));
-        // The slab goes back to the producer as soon as it has been read.  Its next fill is
-        // an async-proxy (TMA) write to the bytes these generic-proxy loads just read, and
-        // the mbarrier hand-off alone does not order the two proxies: the proxy fence comes
-        // first.  (Without it, about one balanced-mode call in twenty with one- or two-tile
-        // segments read a few MX blocks of a value chunk from the slab's next fill.)
-        fence_proxy_async_smem();
+        fence_proxy_async_smem();   // generic reads before the slab's next async-proxy fill (above)
         warp_arrive(smem_u32(&sh->slab_empty[si]));
-        if (rc) {   // the rope buffer was last read by the QK MMAs of tile g - 1
-          ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&sh->rope_empty[0]), (g & 1) ^ 1, abortf, p.status,
-                                                p.wait_limit_ns));
-          if (!ok) break;
-        }
-        if (!rc) {
-          uint8_t* dst = ring + (vslot0 + c) * C::kSlotBytes + di * 128;     // [128 x 128 B] SW128
-          const uint32_t kc = static_cast<uint32_t>(kv64 >> (16 * c));        // blocks 4c .. 4c+3
+        uint8_t* dst = ring + (vslot0 + c) * C::kSlotBytes + di * 128;       // [128 x 128 B] SW128
+        const uint32_t kc = static_cast<uint32_t>(kv64 >> (16 * c));          // blocks 4c .. 4c+3
 #pragma unroll
-          for (int bk = 0; bk < 4; ++bk) {
-            uint4 lo, hi;
-            deq_block(v[bk], sh->lut[(kc >> (4 * bk)) & 15u], lo, hi);
-            *reinterpret_cast<uint4*>(dst + (((2 * bk) ^ (di & 7)) << 4)) = lo;
-            *reinterpret_cast<uint4*>(dst + (((2 * bk + 1) ^ (di & 7)) << 4)) = hi;
-          }
-        } else {
-          uint8_t* dst = rope + di * 64;                                      // [128 x 64 B] SW64
-#pragma unroll
-          for (int bk = 0; bk < 2; ++bk) {
-            uint4 lo, hi;
-            deq_block(v[bk], sh->lut[(kpk[2] >> (4 * bk)) & 15u], lo, hi);
-            *reinterpret_cast<uint4*>(dst + (((2 * bk) ^ ssw) << 4)) = lo;
-            *reinterpret_cast<uint4*>(dst + (((2 * bk + 1) ^ ssw) << 4)) = hi;
-          }
-          sh->etok[g & 3][di] = emax;
+        for (int bk = 0; bk < 4; ++bk) {
+          uint4 lo, hi;
+          deq_block(v[bk], sh->lut[(kc >> (4 * bk)) & 15u], lo, hi);
+          *reinterpret_cast<uint4*>(dst + (((2 * bk) ^ (di & 7)) << 4)) = lo;
+          *reinterpret_cast<uint4*>(dst + (((2 * bk + 1) ^ (di & 7)) << 4)) = hi;
         }
         fence_proxy_async_smem();
-        warp_arrive(rc ? smem_u32(&sh->rope_full[0]) : smem_u32(&sh->full[vslot0 + c]));
+        warp_arrive(smem_u32(&sh->full[vslot0 + c]));
       }
       if (!ok) break;
       warp_arrive(smem_u32(&sh->etok_full[g & 3]));
@@ -852,7 +869,8 @@ __device__ void run_mma_qk(const DecodeParams& p, SharedState* sh, const Descs& 
         break;
       const uint32_t d = tmem + (g & 1) * C::kSCols;
 #pragma unroll
-      for (int c = 0; c < C::kSPT; ++c) {
+      for (int i = 0; i < C::kSPT; ++i) {
+        const int c = KV == 2 ? mx_chunk(i) : i;                             // MXFP4: the dequantisation order
         const bool rope_sep = (C::kRingPT < C::kSPT) && c == C::kSPT - 1;   // rope outside the ring
         const uint32_t rs = C::kRopeSlots > 0 ? g % (C::kRopeSlots > 0 ? C::kRopeSlots : 1) : 0;
         const uint32_t rph = C::kRopeSlots > 0 ? (g / (C::kRopeSlots > 0 ? C::kRopeSlots : 1)) & 1 : 0;
@@ -871,7 +889,7 @@ __device__ void run_mma_qk(const DecodeParams& p, SharedState* sh, const Descs& 
         } else {
           const uint64_t b = c < 4 ? ds.q + dofs(c * 4096) : ds.q_rope;
 #pragma unroll
-          for (int k = 0; k < (c < 4 ? 4 : 2); ++k) mma_f8(d, a + dofs(32 * k), b + dofs(32 * k), idq, (c | k) != 0);
+          for (int k = 0; k < (c < 4 ? 4 : 2); ++k) mma_f8(d, a + dofs(32 * k), b + dofs(32 * k), idq, (i | k) != 0);
         }
         if (c == C::kSPT - 1)   // the rope chunk is read by QK only
           mma_commit(rope_sep ? smem_u32(&sh->rope_empty[rs]) : smem_u32(&sh->empty[slot]));

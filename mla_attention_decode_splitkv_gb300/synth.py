@@ -55,7 +55,9 @@ CONFIGS: List[ConfigSpec] = [
     ConfigSpec("fp8_b32_l1024", 32, 1024, KV_FP8, None, 1235),
     ConfigSpec("fp8_b64_l8192_splitkv", 64, 8192, KV_FP8, None, 1236),
     ConfigSpec("mxfp4_b256_l8192", 256, 8192, KV_MXFP4, None, 1237),
-    ConfigSpec("fp8_ragged_b128_l1to8192", 128, None, KV_FP8, None, 1238),
+    # A ragged batch runs in the balanced mode: the split model's length hint describes
+    # batches of equal lengths.
+    ConfigSpec("fp8_ragged_b128_l1to8192", 128, None, KV_FP8, 0, 1238),
 ]
 
 

@@ -129,22 +129,72 @@ def test_valid_call_without_a_gpu_fails_cleanly(lib):
     assert _call_multi(lib) in (-2, -3)
 
 
+ROW_BYTES = {0: 576 * 2, 1: 576, 2: 288 + 18}          # bf16, fp8, MXFP4 cache rows
+PIECE_BYTES = 16 * (512 + 1) * 4                          # fp32 partial output + log-sum-exp of 16 heads
+WAVE_BYTES = 222e3                                        # per-wave start-up + drain latency x one SM's HBM share
+CROSS_BYTES = 300e3                                       # crossing latency x one SM's HBM share
+
+
+def _model_splits(batch, L, sms, dtype):
+    """The split model as the header states it: cache-row costs c (a piece) and x (a sequence
+    crossing), time of the slowest CTA for each uniform split count and for the balanced mode."""
+    c, w, x = PIECE_BYTES / ROW_BYTES[dtype], WAVE_BYTES / ROW_BYTES[dtype], CROSS_BYTES / ROW_BYTES[dtype]
+    L = max(L, 1)
+    best_ns, best_t = 1, None
+    for ns in range(1, min(4096, -(-L // 128)) + 1):
+        waves = -(-batch * ns // sms)
+        chunk = -(-(-(-L // ns)) // 128) * 128
+        t = waves * (chunk + w + (c if ns > 1 else 0.0)) + (ns * c if ns > 1 else 0.0)
+        if best_t is None or t < best_t:
+            best_ns, best_t = ns, t
+    R = batch * L / sms
+    s = math.ceil(R / L) + 1
+    p = math.ceil(L / R) + 1
+    t_bal = R + w + s * c + (s - 1) * x + p * c
+    return 0 if t_bal < best_t else best_ns
+
+
+def test_split_model_piece_cost_is_the_partial_bytes():
+    # c in rows = one piece's bytes over one cached row's bytes
+    assert PIECE_BYTES == 32832
+    assert abs(PIECE_BYTES / ROW_BYTES[1] - 57.0) < 1e-9
+
+
 @pytest.mark.parametrize("dtype", [0, 1, 2])
-def test_pick_splits_follows_the_documented_rule(lib, dtype):
-    for batch in (1, 4, 32, 64, 75, 76, 77, 128, 151, 152, 153, 256, 1000):
-        for L in (0, 1, 100, 127, 128, 256, 257, 1024, 2048, 2049, 4000, 8192, 65536, 10**6):
+def test_pick_splits_follows_the_documented_model(lib, dtype):
+    for batch in (1, 4, 8, 32, 64, 75, 76, 77, 128, 151, 152, 153, 256, 1000):
+        for L in (0, 1, 100, 127, 128, 256, 257, 1024, 2048, 2049, 4000, 4096, 8192, 65536):
             for sms in (148, 152):
-                ns = min(sms // batch, -(-L // 256), math.isqrt(L // 32))
-                want = ns if ns >= 2 else (1 if L <= 2048 else 0)
-                assert lib.mla_decode_pick_splits(batch, L, sms, dtype) == want, (batch, L, sms)
-    # the workloads: 64 x 8192 -> 2 splits, 32 x 1024 -> 4, 256 x 8192 -> balanced, a ragged
-    # batch of 128 (mean length 4096) -> balanced; 256 x 1024 -> 1, 4 x 8192 -> 16
-    assert lib.mla_decode_pick_splits(64, 8192, 152, 1) == 2
-    assert lib.mla_decode_pick_splits(32, 1024, 152, 1) == 4
-    assert lib.mla_decode_pick_splits(256, 8192, 152, 2) == 0
-    assert lib.mla_decode_pick_splits(128, 4096, 152, 1) == 0
-    assert lib.mla_decode_pick_splits(256, 1024, 152, 1) == 1
-    assert lib.mla_decode_pick_splits(4, 8192, 152, 1) == 16
+                assert lib.mla_decode_pick_splits(batch, L, sms, dtype) == _model_splits(batch, L, sms, dtype), \
+                    (batch, L, sms)
+
+
+def test_pick_splits_reproduces_the_measured_choices(lib):
+    # GB300 (152 SMs), cold calls, each shape timed at the split counts shown; the model
+    # must pick the fastest (or, where two were equal, one of them):
+    #   fp8  256 x 4096: balanced 123.6, ns 1 125.6, ns 2 144.0, ns 4 154.3 us
+    #   fp8  256 x 8192: balanced 211.6, ns 1 219.8, ns 2 242.3, ns 4 244.4
+    #   MXFP4 256 x 8192: balanced 344.7, ns 1 379.5, ns 2 402.1, ns 4 385.7
+    #   fp8  64 x 8192: ns 2 72.4, balanced 82.5;  MXFP4: ns 2 105.2, balanced 109.2
+    #   bf16 64 x 8192: balanced 139.9, ns 2 142.0
+    #   fp8  152 x 8192: ns 1 129.7, balanced 131.7, ns 2 139.9
+    #   fp8  16 x 8192: ns 8 = ns 9 33.4, balanced 43.7;  4 x 8192: ns 13 = ns 16 25.2, ns 32 27.3
+    #   fp8  256 x 1024: ns 1 47.7, balanced 62.1;  256 x 2048: ns 1 70.3, balanced 84.6;
+    #   128 x 1024: ns 1 27.3, balanced 45.7
+    pick = lambda b, L, dt: lib.mla_decode_pick_splits(b, L, 152, dt)
+    assert pick(256, 4096, 1) == 0
+    assert pick(256, 8192, 1) == 0
+    assert pick(256, 8192, 2) == 0
+    assert pick(64, 8192, 1) == 2
+    assert pick(64, 8192, 2) == 2
+    assert pick(64, 8192, 0) == 0
+    assert pick(152, 8192, 1) == 1
+    assert pick(16, 8192, 1) in (8, 9)
+    assert pick(4, 8192, 1) in (13, 16)
+    for L in (1024, 2048):
+        assert pick(256, L, 1) == 1
+    assert pick(128, 1024, 1) == 1
+    assert pick(32, 1024, 1) == 4
 
 
 def test_pick_splits_rejects_bad_arguments(lib):
