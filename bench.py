@@ -55,7 +55,7 @@ def parse():
                     help="timed steps only (no clock soak, e2e or CPU baseline); for profiler runs")
     ap.add_argument("--q-len", type=int, default=1,
                     help="with --page-size: query tokens per sequence (mla_decode_paged_multi when > 1)")
-    ap.add_argument("--page-size", type=int, default=0, choices=[0, 8, 16, 32, 64, 128],
+    ap.add_argument("--page-size", type=int, default=0, choices=[0, 1, 2, 4, 8, 16, 32, 64, 128],
                     help="with --quick: store the workload's cache in shuffled pages of this many rows "
                          "and time mla_decode_paged")
     return ap.parse_args()

@@ -112,8 +112,9 @@ int mla_decode(const void* q, const void* kv, const void* kv_scale, const int32_
  *  kv_last_page_len int32 [batch] (device): rows used in the sequence's last page,
  *                   1 .. page_size (ignored for a sequence with no pages, which has length 0).
  *                   Sequence b has (npages_b - 1) * page_size + kv_last_page_len[b] tokens.
- *  page_size        8, 16, 32, 64 or 128 (one TMA box of page_size rows per page; a page of
- *                   fewer than 8 rows would break the 8-row swizzle atom of a box).
+ *  page_size        1, 2, 4, 8, 16, 32, 64 or 128.  Pages of 8 rows and more are loaded one
+ *                   TMA box per page; pages of 1, 2 or 4 rows (fewer than a box's 8-row swizzle
+ *                   atom; the pages' persistent default is 2) are copied 16 bytes at a time.
  *  num_splits       as mla_decode.  In the balanced mode (<= 0) the token positions are
  *                   those of the page space (sequence b starts at kv_page_indptr[b] *
  *                   page_size; the unused rows of its last page belong to no CTA's work)
@@ -122,7 +123,7 @@ int mla_decode(const void* q, const void* kv, const void* kv_scale, const int32_
  * Every page number times page_size plus page_size must be a row inside kv, and every
  * index read must lie inside kv_page_indices; violations are undefined behaviour, as with
  * kv_indptr.  Errors: as mla_decode, plus MLA_ERR_INVALID_ARG for a page_size that is not
- * a power of two in [8, 128] or a null page table.
+ * a power of two in [1, 128] or a null page table.
  */
 int mla_decode_paged(const void* q, const void* kv, const void* kv_scale, const int32_t* kv_page_indptr,
                      const int32_t* kv_page_indices, const int32_t* kv_last_page_len, int page_size, void* out,

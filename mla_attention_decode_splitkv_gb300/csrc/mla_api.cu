@@ -282,8 +282,7 @@ static int decode_impl(const void* q, const void* kv, const void* kv_scale, cons
                        void* stream) {
   if (q == nullptr || kv == nullptr || kv_indptr == nullptr || out == nullptr) return MLA_ERR_INVALID_ARG;
   if (page_size != 0) {
-    if (page_size < mla::kMinPage || page_size > mla::kBN || (page_size & (page_size - 1)) != 0)
-      return MLA_ERR_INVALID_ARG;
+    if (page_size < 1 || page_size > mla::kBN || (page_size & (page_size - 1)) != 0) return MLA_ERR_INVALID_ARG;
     if (page_indices == nullptr || last_page_len == nullptr) return MLA_ERR_INVALID_ARG;
     if (!aligned(page_indices, 4) || !aligned(last_page_len, 4)) return MLA_ERR_INVALID_ARG;
   }
@@ -313,7 +312,7 @@ static int decode_impl(const void* q, const void* kv, const void* kv_scale, cons
   const Workspace ws = g_ws[dev];
 
   mla::DecodeParams p;
-  const int box_rows = page_size != 0 ? page_size : mla::kBN;
+  const int box_rows = page_size >= mla::kMinPage ? page_size : mla::kBN;   // (pages below 8 rows use no TMA box)
   rc = mla::encode_kv_map_rows(&p.tmap, kv, kv_dtype, box_rows);
   if (rc) return rc;
   if (kv_dtype == MLA_KV_FP8_E4M3) {

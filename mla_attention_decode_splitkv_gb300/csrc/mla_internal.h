@@ -10,7 +10,7 @@ constexpr int kHeads = 16;
 constexpr int kDim = 576;
 constexpr int kDimV = 512;
 constexpr int kBN = 128;           // cached tokens per tile (= UMMA M)
-constexpr int kMinPage = 8;        // smallest page (rows) of a paged cache: one swizzle atom per TMA box
+constexpr int kMinPage = 8;        // smallest page (rows) a TMA box loads whole: one swizzle atom; 1-4 use cp.async
 constexpr int kMxBlock = 32;
 constexpr int kMxPacked = 288;     // bytes of e2m1 nibbles per row
 constexpr int kMxScales = 18;      // e8m0 scales per row
@@ -39,7 +39,7 @@ struct DecodeParams {
   unsigned long long wait_limit_ns;
   int test_stall;                  // test hook: the QK issuer waits on a barrier that never completes
   // Paged cache (mla_decode_paged; 0 / null otherwise): kv_indptr indexes page_indices.
-  int page_size;                   // rows per page: 8, 16, 32, 64 or 128
+  int page_size;                   // rows per page: a power of two, 1 .. 128
   int page_shift;                  // log2(page_size)
   const int32_t* page_indices;     // [kv_indptr[batch]] physical page of each sequence page
   const int32_t* last_page_len;    // [sequences] rows used in each sequence's last page (1..page_size)
@@ -65,7 +65,8 @@ unsigned long long pipeline_wait_limit_ns();
 
 // Launches the split kernel for kv_dtype (geometry per dtype is internal to mla_split.cu).
 cudaError_t launch_split(int kv_dtype, const DecodeParams& p, int grid, cudaStream_t stream);
-// The same for a paged cache (page size 8 .. 128, a power of two; boxes of page_size rows).
+// The same for a paged cache (page size 1 .. 128, a power of two; TMA boxes of page_size rows
+// from 8 rows up, 16-byte cp.async copies below).
 cudaError_t launch_split_paged(int kv_dtype, const DecodeParams& p, int grid, cudaStream_t stream);
 // Tensor maps with boxes of `box_rows` rows (paged caches: box_rows = page size).
 int encode_kv_map_rows(CUtensorMap* map, const void* kv, int kv_dtype, int box_rows);

@@ -151,6 +151,7 @@ struct SharedState {
   uint64_t rope_full[2];           // rope slots (fp8: TMA, MXFP4: dequant) / consumed by QK
   uint64_t rope_empty[2];
   int etok[4][128];                // per-row max block exponent of the last 4 tiles
+  int sp_rows[128];                // pages of 1-4 rows: the cache row of each window row of a tile
   uint2 lut[kLutCount];            // 8 e4m3 bytes per block shift
   long long seg_total;              // kv_indptr[batch] (balanced mode)
   int seg_b0;                      // first sequence of this CTA (balanced mode)
@@ -635,6 +636,115 @@ __device__ void run_producer(const DecodeParams& p, SharedState* sh, uint8_t* ri
   }
 }
 
+// ---------------------------------------------------------------- producer for pages of 1-4 rows (1 warp)
+// A TMA box of fewer than 8 rows would not fill whole 8-row swizzle atoms, so pages of 1, 2
+// or 4 rows are copied with 16-byte cp.async straight into the slot's swizzled layout (the
+// image a 128-row box would write): piece j of window row r lands at r * PITCH + ((j ^ s) <<
+// 4), s = r mod 8 (128-byte swizzle, PITCH 128) or (r / 2) mod 4 (64-byte swizzle, PITCH 64).
+// Every lane then arrives on the slot's full barrier when its own copies have landed (32
+// arrivals complete it).  These are generic-proxy writes: the MMA issuers that read such a
+// slot put a proxy fence after their wait.
+// Bytes [byte0, byte0 + W) of each of the tile's 128 window rows, whose cache rows are in
+// `rows`; lane = (row, piece) so that each warp-wide copy reads whole 32-byte sectors.
+template <int W, int PITCH>
+__device__ __forceinline__ void sp_copy(const uint8_t* kv, int row_bytes, const int* rows, uint32_t dst, int byte0,
+                                        int lane) {
+  constexpr int kPieces = W / 16;
+  constexpr int kRowsPer = 32 / kPieces;
+  const int piece = lane % kPieces;
+#pragma unroll 4
+  for (int r = lane / kPieces; r < kBN; r += kRowsPer) {
+    const uint8_t* src = kv + static_cast<size_t>(rows[r]) * row_bytes + byte0 + piece * 16;
+    const int sw = PITCH == 128 ? (r & 7) : ((r >> 1) & 3);
+    cp_async_16(dst + r * PITCH + ((piece ^ sw) << 4), src);
+  }
+}
+
+template <int KV>
+__device__ void run_producer_sp(const DecodeParams& p, SharedState* sh, uint8_t* ring, uint8_t* rope, uint8_t* slabs,
+                                int lane) {
+  using C = Cfg<KV>;
+  volatile int* abortf = &sh->abort;
+  const int rb = KV == 0 ? 2 * kDim : (KV == 1 ? kDim : kMxPacked);   // bytes per cache row
+  SegIter<true> it;
+  it.init(p, blockIdx.x, sh->seg_total, sh->seg_b0);
+  Seg s;
+  uint32_t idx = 0, slot = 0, phase = 0, ridx = 0;
+  constexpr int kSlots = KV == 2 ? kSlabs : C::kRing;
+  bool ok = true;
+  while (ok && it.next(p, s)) {
+    const int n = s.n_hi - s.n_lo;
+    if (n <= 0) continue;
+    const int ntiles = (n + kBN - 1) / kBN;
+    const int np = (s.n_total + p.page_size - 1) >> p.page_shift;
+    for (int t = 0; t < ntiles && ok; ++t) {
+      // Cache row of every window row (rows past the sequence reuse its last page; masked).
+      __syncwarp();
+      for (int r = lane; r < kBN; r += 32) {
+        const int tok = s.n_lo + t * kBN + r;
+        sh->sp_rows[r] = (p.page_indices[s.row0 + min(tok >> p.page_shift, np - 1)] << p.page_shift) +
+                         (tok & (p.page_size - 1));
+      }
+      __syncwarp();
+      const int* rows = sh->sp_rows;
+      for (int c0 = 0; c0 < (KV == 2 ? 5 : C::kRingPT); ++c0) {
+        const uint32_t eb = KV == 2 ? smem_u32(&sh->slab_empty[slot]) : smem_u32(&sh->empty[slot]);
+        if (!producer_wait<true>(eb, phase ^ 1, abortf, p.status, p.wait_limit_ns)) {
+          ok = false;
+          break;
+        }
+        if constexpr (KV == 2) {
+          const int c = mx_chunk(c0);
+          const uint32_t dst = smem_u32(slabs + slot * kSlabBytes);
+          if (c < 4) sp_copy<64, 64>(p.kv, rb, rows, dst, 64 * c, lane);
+          else sp_copy<32, 64>(p.kv, rb, rows, dst, 4 * 64, lane);   // the rope's 32 bytes (the rest unused)
+          cp_async_mbar_arrive(smem_u32(&sh->slab_full[slot]));
+        } else {
+          const uint32_t dst = smem_u32(ring + slot * C::kSlotBytes);
+          if constexpr (KV == 0) {
+            if (c0 < 4) {
+              sp_copy<128, 128>(p.kv, rb, rows, dst, 256 * c0, lane);
+              sp_copy<128, 128>(p.kv, rb, rows, dst + 16384, 256 * c0 + 128, lane);
+            } else {
+              sp_copy<128, 128>(p.kv, rb, rows, dst, 2 * kDimV, lane);
+            }
+          } else {
+            sp_copy<128, 128>(p.kv, rb, rows, dst, 128 * c0, lane);
+          }
+          cp_async_mbar_arrive(smem_u32(&sh->full[slot]));
+        }
+        ++idx;
+        if (++slot == static_cast<uint32_t>(kSlots)) { slot = 0; phase ^= 1; }
+      }
+      if constexpr (KV == 1) {   // the rope chunk (64 B of each row) into its own slots
+        if (!ok) break;
+        const uint32_t rs = ridx % C::kRopeSlots;
+        if (!producer_wait<true>(smem_u32(&sh->rope_empty[rs]), ((ridx / C::kRopeSlots) & 1) ^ 1, abortf, p.status,
+                                 p.wait_limit_ns)) {
+          ok = false;
+          break;
+        }
+        sp_copy<64, 64>(p.kv, rb, rows, smem_u32(rope + rs * kRopeBytes), kDimV, lane);
+        cp_async_mbar_arrive(smem_u32(&sh->rope_full[rs]));
+        ++ridx;
+      }
+    }
+  }
+  if (!ok) {  // drain copies already issued so that none lands after the CTA exits
+    const uint32_t first = idx > static_cast<uint32_t>(kSlots) ? idx - kSlots : 0u;
+    for (uint32_t j = first; j < idx; ++j) {
+      const uint32_t fb = KV == 2 ? smem_u32(&sh->slab_full[j % kSlots]) : smem_u32(&sh->full[j % kSlots]);
+      wait_bar(fb, (j / kSlots) & 1, abortf, p.status, kDrainLimitNs, false);
+    }
+    if constexpr (KV == 1) {
+      const uint32_t rfirst = ridx > (uint32_t)C::kRopeSlots ? ridx - C::kRopeSlots : 0u;
+      for (uint32_t j = rfirst; j < ridx; ++j)
+        wait_bar(smem_u32(&sh->rope_full[j % C::kRopeSlots]), (j / C::kRopeSlots) & 1, abortf, p.status,
+                 kDrainLimitNs, false);
+    }
+  }
+}
+
 // ---------------------------------------------------------------- MXFP4 dequantisation (128 threads)
 // Row i of a tile (thread i) becomes 576 e4m3 carrier bytes: block j of 32 elements is
 // e2m1 * 2^(E_j - e_i) with e_i = max_j E_j, looked up per nibble in an 8-entry table for
@@ -846,7 +956,7 @@ __device__ __forceinline__ Descs make_descs(uint8_t* ring, uint8_t* rope, uint8_
 // Byte offset -> descriptor start-address increment.
 __device__ __forceinline__ uint64_t dofs(uint32_t bytes) { return static_cast<uint64_t>(bytes >> 4); }
 
-template <int KV, bool PG>
+template <int KV, bool PG, bool SP>
 __device__ void run_mma_qk(const DecodeParams& p, SharedState* sh, const Descs& ds, uint32_t tmem) {
   using C = Cfg<KV>;
   constexpr uint32_t idq = instr_desc(KV == 0 ? 1u : 0u, 0, 0, 128, C::kN);  // bf16 | e4m3, K-major A and B
@@ -877,6 +987,7 @@ __device__ void run_mma_qk(const DecodeParams& p, SharedState* sh, const Descs& 
         const uint32_t fb = rope_sep ? smem_u32(&sh->rope_full[rs]) : smem_u32(&sh->full[slot]);
         if (!(ok = wait_bar(fb, rope_sep ? rph : phase, abortf, p.status, p.wait_limit_ns))) break;
         tc_fence_after();
+        if constexpr (SP && KV != 2) fence_proxy_async_smem();   // cp.async (generic-proxy) data, read by the MMAs
         const uint64_t a = rope_sep ? ds.rope + dofs(rs * kRopeBytes) : ds.ring_k + dofs(slot * C::kSlotBytes);
         if constexpr (KV == 0) {
           const uint64_t b = ds.q + dofs(2 * c * 2048);
@@ -904,7 +1015,7 @@ __device__ void run_mma_qk(const DecodeParams& p, SharedState* sh, const Descs& 
 }
 
 // PV issuer `part` (0 or 1) issues the two 128-dim blocks 2*part, 2*part+1 of every tile.
-template <int KV, bool PG>
+template <int KV, bool PG, bool SP>
 __device__ void run_mma_pv(const DecodeParams& p, SharedState* sh, const Descs& ds, uint32_t tmem, int part) {
   using C = Cfg<KV>;
   constexpr uint32_t idp = instr_desc(KV == 0 ? 1u : 0u, 1, 1, 128, C::kN);  // MN-major A (V^T) and B (P^T)
@@ -925,6 +1036,7 @@ __device__ void run_mma_pv(const DecodeParams& p, SharedState* sh, const Descs& 
           !(ok = wait_bar(smem_u32(&sh->o_free), (kseg - 1) & 1, abortf, p.status, p.wait_limit_ns)))
         break;
       tc_fence_after();
+      if constexpr (SP && KV != 2) fence_proxy_async_smem();     // cp.async (generic-proxy) data, read by the MMAs
       const bool first = (t == 0);
       const uint64_t b = ds.p + dofs((g & 1) * kPBytes);
 #pragma unroll
@@ -1452,7 +1564,8 @@ __device__ void run_softmax(const DecodeParams& p, SharedState* sh, uint8_t* qs,
 }
 
 // ---------------------------------------------------------------- the kernel
-template <int KV, bool PG>
+// PG: paged cache.  SP: pages of 1, 2 or 4 rows (copied by the producer warp with cp.async).
+template <int KV, bool PG, bool SP>
 __global__ void __launch_bounds__(Cfg<KV>::kThreads, 1) mla_split_kernel(const __grid_constant__ DecodeParams p) {
   using C = Cfg<KV>;
   extern __shared__ uint8_t smem_raw[];
@@ -1467,12 +1580,13 @@ __global__ void __launch_bounds__(Cfg<KV>::kThreads, 1) mla_split_kernel(const _
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::kRing; ++i) {
-      mbar_init(smem_u32(&sh->full[i]), KV == 2 ? C::kDeqWarps : 1);   // MXFP4: one arrival per dequant warp
+      // MXFP4: one arrival per dequant warp; pages of 1-4 rows: one cp.async arrival per producer lane
+      mbar_init(smem_u32(&sh->full[i]), KV == 2 ? C::kDeqWarps : (SP ? 32 : 1));
       mbar_init(smem_u32(&sh->empty[i]), 1);
     }
     if (KV == 2) {
       for (int i = 0; i < kSlabs; ++i) {
-        mbar_init(smem_u32(&sh->slab_full[i]), 1);
+        mbar_init(smem_u32(&sh->slab_full[i]), SP ? 32 : 1);
         mbar_init(smem_u32(&sh->slab_empty[i]), C::kDeqWarps);   // one arrival per dequant warp
       }
       for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&sh->etok_full[i]), C::kDeqWarps);
@@ -1481,7 +1595,7 @@ __global__ void __launch_bounds__(Cfg<KV>::kThreads, 1) mla_split_kernel(const _
     // softmax-side barriers count warps (one arrival per warp)
     mbar_init(smem_u32(&sh->q_ready), 4);       // the first four softmax warps stage q
     for (int i = 0; i < C::kRopeSlots; ++i) {
-      mbar_init(smem_u32(&sh->rope_full[i]), KV == 2 ? C::kDeqWarps : 1);   // MXFP4: per dequant warp; fp8: TMA
+      mbar_init(smem_u32(&sh->rope_full[i]), KV == 2 ? C::kDeqWarps : (SP ? 32 : 1));   // MXFP4: per dequant warp
       mbar_init(smem_u32(&sh->rope_empty[i]), 1);                          // QK commit
     }
     for (int i = 0; i < 2; ++i) {
@@ -1530,12 +1644,14 @@ __global__ void __launch_bounds__(Cfg<KV>::kThreads, 1) mla_split_kernel(const _
     if constexpr (KV == 2) regs_dec<C::kRegsIssue>();
     if (warp == 0) {
       if (PG || lane == 0) {   // paged: the whole warp (one lane per page)
-        if constexpr (KV == 2) run_producer_mx<PG>(p, sh, slabs, lane); else run_producer<KV, PG>(p, sh, ring, rope, lane);
+        if constexpr (SP) run_producer_sp<KV>(p, sh, ring, rope, slabs, lane);
+        else if constexpr (KV == 2) run_producer_mx<PG>(p, sh, slabs, lane);
+        else run_producer<KV, PG>(p, sh, ring, rope, lane);
       }
     } else if (warp == 1) {
-      if (lane == 0) run_mma_qk<KV, PG>(p, sh, make_descs(ring, rope, qs, ps), tmem);
+      if (lane == 0) run_mma_qk<KV, PG, SP>(p, sh, make_descs(ring, rope, qs, ps), tmem);
     } else {
-      if (lane == 0) run_mma_pv<KV, PG>(p, sh, make_descs(ring, rope, qs, ps), tmem, warp - 2);
+      if (lane == 0) run_mma_pv<KV, PG, SP>(p, sh, make_descs(ring, rope, qs, ps), tmem, warp - 2);
     }
     __syncwarp();
   } else if (warp < 4 + C::kSoftWarps) {
@@ -1560,18 +1676,18 @@ constexpr int kMaxDevices = 64;
 // Per-device, once: the kernel's dynamic shared-memory limit (a per-function attribute
 // that each device context keeps) and, for MXFP4, the register-split check.  Thread-safe;
 // the outcome of the first attempt on a device is kept.
-template <int KV, bool PG>
+template <int KV, bool PG, bool SP>
 cudaError_t configure_once(int dev) {
   static std::once_flag once[kMaxDevices];
   static cudaError_t result[kMaxDevices];
   std::call_once(once[dev], [dev] {
-    cudaError_t e = cudaFuncSetAttribute(mla_split_kernel<KV, PG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(mla_split_kernel<KV, PG, SP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem_bytes<KV>()));
     if (e == cudaSuccess && KV == 2) {
       // The register split's increases only complete if the CTA launched with at least the
       // registers the split hands out: refuse to launch otherwise.
       cudaFuncAttributes fa;
-      e = cudaFuncGetAttributes(&fa, mla_split_kernel<KV, PG>);
+      e = cudaFuncGetAttributes(&fa, mla_split_kernel<KV, PG, SP>);
       if (e == cudaSuccess && fa.numRegs * Cfg<KV>::kThreads < Cfg<2>::kRegsNeeded) e = cudaErrorInvalidConfiguration;
     }
     result[dev] = e;
@@ -1579,13 +1695,13 @@ cudaError_t configure_once(int dev) {
   return result[dev];
 }
 
-template <int KV, bool PG>
+template <int KV, bool PG, bool SP>
 cudaError_t launch_split_t(const DecodeParams& p, int grid, cudaStream_t stream) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  if ((e = configure_once<KV, PG>(dev)) != cudaSuccess) return e;
+  if ((e = configure_once<KV, PG, SP>(dev)) != cudaSuccess) return e;
   // Launched with programmatic stream serialisation: the kernel's set-up overlaps the tail
   // of the previous kernel in the stream (see grid_dep_wait in the kernel).
   cudaLaunchConfig_t cfg = {};
@@ -1598,7 +1714,7 @@ cudaError_t launch_split_t(const DecodeParams& p, int grid, cudaStream_t stream)
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, mla_split_kernel<KV, PG>, p);
+  e = cudaLaunchKernelEx(&cfg, mla_split_kernel<KV, PG, SP>, p);
   if (e != cudaSuccess) cudaGetLastError();
   return e;
 }
@@ -1606,16 +1722,22 @@ cudaError_t launch_split_t(const DecodeParams& p, int grid, cudaStream_t stream)
 }  // namespace
 
 cudaError_t launch_split(int kv_dtype, const DecodeParams& p, int grid, cudaStream_t stream) {
-  if (kv_dtype == 0) return launch_split_t<0, false>(p, grid, stream);
-  if (kv_dtype == 1) return launch_split_t<1, false>(p, grid, stream);
-  if (kv_dtype == 2) return launch_split_t<2, false>(p, grid, stream);
+  if (kv_dtype == 0) return launch_split_t<0, false, false>(p, grid, stream);
+  if (kv_dtype == 1) return launch_split_t<1, false, false>(p, grid, stream);
+  if (kv_dtype == 2) return launch_split_t<2, false, false>(p, grid, stream);
   return cudaErrorNotSupported;
 }
 
 cudaError_t launch_split_paged(int kv_dtype, const DecodeParams& p, int grid, cudaStream_t stream) {
-  if (kv_dtype == 0) return launch_split_t<0, true>(p, grid, stream);
-  if (kv_dtype == 1) return launch_split_t<1, true>(p, grid, stream);
-  if (kv_dtype == 2) return launch_split_t<2, true>(p, grid, stream);
+  if (p.page_size < kMinPage) {   // pages of 1, 2 or 4 rows: cp.async producer
+    if (kv_dtype == 0) return launch_split_t<0, true, true>(p, grid, stream);
+    if (kv_dtype == 1) return launch_split_t<1, true, true>(p, grid, stream);
+    if (kv_dtype == 2) return launch_split_t<2, true, true>(p, grid, stream);
+    return cudaErrorNotSupported;
+  }
+  if (kv_dtype == 0) return launch_split_t<0, true, false>(p, grid, stream);
+  if (kv_dtype == 1) return launch_split_t<1, true, false>(p, grid, stream);
+  if (kv_dtype == 2) return launch_split_t<2, true, false>(p, grid, stream);
   return cudaErrorNotSupported;
 }
 

@@ -353,7 +353,7 @@ def test_mxfp4_short_segments_repeated(pkg, lens):
 PAGED_LENS = [1, 129, 0, 1000, 2048, 64, 65, 127, 128]
 
 
-PAGE_SIZES = [8, 16, 32, 64, 128]
+PAGE_SIZES = [1, 2, 4, 8, 16, 32, 64, 128]     # 1-4: cp.async copies; 8 and up: one TMA box per page
 
 
 @pytest.mark.parametrize("kv_dtype", DTYPES)
@@ -374,7 +374,8 @@ def test_paged_cache_matches_oracle(pkg, kv_dtype, page_size, ns):
     _check(out, ref, f"paged P={page_size} ns={ns}")
 
 
-@pytest.mark.parametrize("kv_dtype,page_size", [(synth.KV_FP8, 64), (synth.KV_MXFP4, 64), (synth.KV_FP8, 8)])
+@pytest.mark.parametrize("kv_dtype,page_size", [(synth.KV_FP8, 64), (synth.KV_MXFP4, 64), (synth.KV_FP8, 8),
+                                                 (synth.KV_FP8, 2), (synth.KV_MXFP4, 4), (synth.KV_BF16, 1)])
 @pytest.mark.parametrize("balanced", [False, True])
 def test_paged_workload_sampled_rows(pkg, kv_dtype, page_size, balanced):
     """A full-size workload (64 x 8192 tokens) in shuffled pages, in uniform splits (one
@@ -403,7 +404,7 @@ def test_paged_rejects_bad_page_size(pkg):
     inp = synth.make_inputs(2, [100, 3], synth.KV_FP8, seed=5)
     pg = synth.to_paged(inp, 64, seed=6).to("cuda")
     out = torch.empty((2, 16, 512), dtype=torch.bfloat16, device="cuda")
-    for ps in (0, 4, 48, 256):
+    for ps in (0, 3, 48, 256):
         rc = pkg.mla_decode_paged(pg.q, pg.kv, pg.kv_scale, pg.page_indptr, pg.page_indices, pg.last_page_len, ps,
                                   out, 2, 1, synth.KV_FP8)
         assert rc == pkg.MLA_ERR_INVALID_ARG
@@ -437,7 +438,7 @@ MQ_QLENS = [1, 2, 3, 4, 0, 3, 2]     # q_len 0, q_len > L (rows that see nothing
 
 
 @pytest.mark.parametrize("kv_dtype", DTYPES)
-@pytest.mark.parametrize("page_size", [8, 64, 128])
+@pytest.mark.parametrize("page_size", [2, 8, 64, 128])
 @pytest.mark.parametrize("ns", [1, 3, 0])
 def test_paged_multi_query_matches_oracle(pkg, kv_dtype, page_size, ns):
     inp = synth.make_inputs(len(MQ_LENS), MQ_LENS, kv_dtype, seed=120 + kv_dtype)

@@ -79,8 +79,8 @@ def _call_paged(lib, q=256, kv=512, scale=1024, ip=2048, pi=3072, last=3584, ps=
 
 def test_paged_argument_checks_precede_any_device_work(lib):
     INV = -1
-    for ps in (0, 1, 2, 4, 12, 48, 96, 256, -64):
-        assert _call_paged(lib, ps=ps) == INV          # page size: a power of two in [8, 128]
+    for ps in (0, 3, 6, 12, 48, 96, 256, -64):
+        assert _call_paged(lib, ps=ps) == INV          # page size: a power of two in [1, 128]
     assert _call_paged(lib, pi=0) == INV
     assert _call_paged(lib, last=0) == INV
     assert _call_paged(lib, ip=0) == INV
@@ -108,7 +108,7 @@ def test_multi_query_argument_checks_precede_any_device_work(lib):
     assert _call_multi(lib, qo=130) == INV              # qo_indptr not 4-byte aligned
     assert _call_multi(lib, total_q=0) == INV
     assert _call_multi(lib, batch=0) == INV
-    for ps in (0, 4, 48, 256):
+    for ps in (0, 3, 48, 256):
         assert _call_multi(lib, ps=ps) == INV
     assert _call_multi(lib, pi=0) == INV
     assert _call_multi(lib, q=258) == INV
@@ -125,7 +125,8 @@ def test_valid_call_without_a_gpu_fails_cleanly(lib):
         pass
     rc = _call(lib, scale=0, dtype=0)
     assert rc in (-2, -3)  # MLA_ERR_UNSUPPORTED or MLA_ERR_CUDA, never a crash
-    assert _call_paged(lib, ps=128) in (-2, -3)
+    for ps in (1, 2, 4, 8, 128):
+        assert _call_paged(lib, ps=ps) in (-2, -3)
     assert _call_multi(lib) in (-2, -3)
 
 
