@@ -55,6 +55,8 @@ def parse():
                     help="timed steps only (no clock soak, e2e or CPU baseline); for profiler runs")
     ap.add_argument("--q-len", type=int, default=1,
                     help="with --page-size: query tokens per sequence (mla_decode_paged_multi when > 1)")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="with --quick: the workload with this many sequences instead (a smaller case for profilers)")
     ap.add_argument("--page-size", type=int, default=0, choices=[0, 1, 2, 4, 8, 16, 32, 64, 128],
                     help="with --quick: store the workload's cache in shuffled pages of this many rows "
                          "and time mla_decode_paged")
@@ -363,7 +365,15 @@ def main():
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     spec = synth.CONFIGS[args.config]
-    inp = synth.make_config(args.config, device=dev, keep_src=False)
+    if args.batch:
+        if not args.quick:
+            raise SystemExit("--batch is a --quick measurement")
+        import dataclasses
+        spec = dataclasses.replace(spec, name=f"{spec.name}_batch{args.batch}", batch=args.batch)
+        lens = ([spec.kv_len] * spec.batch if spec.kv_len else synth.ragged_lengths(spec.batch, 8192, spec.seed))
+        inp = synth.make_inputs(spec.batch, lens, spec.kv_dtype, spec.seed, device=dev, keep_src=False)
+    else:
+        inp = synth.make_config(args.config, device=dev, keep_src=False)
     B = inp.batch
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     ns = pkg.resolve_splits(spec.num_splits, B, inp.rows // B, sms, spec.kv_dtype)

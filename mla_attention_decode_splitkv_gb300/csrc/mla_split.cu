@@ -97,7 +97,7 @@ struct Cfg<2> {                    // MXFP4 cache: dequantised to an e4m3 carrie
   static constexpr int kRing = 8;            // value chunks of exactly two tiles
   static constexpr int kSPT = 5;
   static constexpr int kRingPT = 4;          // the rope chunk has its own [128 x 64 B] SW64 buffer
-  static constexpr int kRopeSlots = 1;
+  static constexpr int kRopeSlots = 2;       // rope carrier, double-buffered
   static constexpr int kN = 32;
   static constexpr int kQBytes = 4 * 4096 + 2048;
   static constexpr int kTmemCols = 256;
@@ -105,8 +105,9 @@ struct Cfg<2> {                    // MXFP4 cache: dequantised to an e4m3 carrie
   static constexpr int kOCols = 32;
   static constexpr float kTau = 4.0f;
   static constexpr int kSoftWarps = 8;
-  static constexpr int kDeqWarps = 4;
-  static constexpr int kThreads = 512;       // producer, QK, 2 PV, 8 softmax warps, 4 dequant warps
+  static constexpr int kRowThreads = 1;      // dequant threads per carrier row
+  static constexpr int kDeqWarps = 4 * kRowThreads;
+  static constexpr int kThreads = 32 * (4 + kSoftWarps + kDeqWarps);   // issuers, softmax, dequant
   // Registers per thread after the role split (launch: 128 each): the issuer and dequant
   // warpgroups give registers up to the softmax warpgroups.
   // 32 * (4 * 80 + 8 * 168 + 4 * 96) = 65536 = 512 * 128.
@@ -788,10 +789,15 @@ template <bool PG>
 __device__ void run_dequant(const DecodeParams& p, SharedState* sh, uint8_t* ring, uint8_t* rope, uint8_t* slabs) {
   using C = Cfg<2>;
   volatile int* abortf = &sh->abort;
-  const int di = threadIdx.x - 32 * (4 + C::kSoftWarps);   // carrier row of the tile
+  const int dt = threadIdx.x - 32 * (4 + C::kSoftWarps);   // dequant thread
+  const int di = dt % kBN;                                 // carrier row of the tile
+  // With kRowThreads = 2, thread half hh converts blocks {2 hh, 2 hh + 1} of each 4-block
+  // value chunk and block hh of the rope chunk.
+  constexpr int kRT = C::kRowThreads;
+  const int hh = dt / kBN;
   const uint8_t* scales = static_cast<const uint8_t*>(p.kv_scale);
-  if (di < kLutCount * 8) {
-    const int k = di >> 3, c = di & 7;
+  if (dt < kLutCount * 8) {
+    const int k = dt >> 3, c = dt & 7;
     const float mag = (c < 2) ? 0.5f * c : ldexpf(1.0f + 0.5f * (c & 1), (c >> 1) - 1);
     const uint32_t code = (k >= 13) ? 0u
         : static_cast<uint32_t>(__nv_cvt_float_to_fp8(ldexpf(mag, -k), __NV_SATFINITE, __NV_E4M3));
@@ -855,16 +861,21 @@ __device__ void run_dequant(const DecodeParams& p, SharedState* sh, uint8_t* rin
       // one 64-bit register by a run-time shift.
       const uint64_t kv64 = static_cast<uint64_t>(kpk[0]) | (static_cast<uint64_t>(kpk[1]) << 32);
       // The rope chunk comes first (the producer fetches it first and the QK MMAs take it
-      // first): its carrier buffer was last read by the QK MMAs of tile g - 1, so it does
-      // not wait for the PV MMAs of tile g - 2, which the value chunks below do.
+      // first): its carrier slot (one of two) was last read by the QK MMAs of tile g - 2, so
+      // it does not wait for the PV MMAs of tile g - 2, which the value chunks below do.
       {
         const uint32_t si = slab_i, sph = slab_ph;
         if (++slab_i == kSlabs) { slab_i = 0; slab_ph ^= 1u; }
         ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&sh->slab_full[si]), sph, abortf, p.status, p.wait_limit_ns));
         if (!ok) break;
         const uint32_t srow = smem_u32(slabs + si * kSlabBytes + di * 64);
-        const uint4 v0 = ld_shared_v4_volatile(srow + ((0 ^ ssw) << 4));
-        const uint4 v1 = ld_shared_v4_volatile(srow + ((1 ^ ssw) << 4));
+        uint4 v0, v1;
+        if constexpr (kRT == 1) {
+          v0 = ld_shared_v4_volatile(srow + ((0 ^ ssw) << 4));
+          v1 = ld_shared_v4_volatile(srow + ((1 ^ ssw) << 4));
+        } else {
+          v0 = ld_shared_v4_volatile(srow + ((hh ^ ssw) << 4));
+        }
         // The slab goes back to the producer as soon as it has been read.  Its next fill is
         // an async-proxy (TMA) write to the bytes these generic-proxy loads just read, and
         // the mbarrier hand-off alone does not order the two proxies: the proxy fence comes
@@ -872,20 +883,27 @@ __device__ void run_dequant(const DecodeParams& p, SharedState* sh, uint8_t* rin
         // segments read a few MX blocks of a value chunk from the slab's next fill.)
         fence_proxy_async_smem();
         warp_arrive(smem_u32(&sh->slab_empty[si]));
-        ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&sh->rope_empty[0]), (g & 1) ^ 1, abortf, p.status,
+        // Rope carrier slot g mod 2 was last read by the QK MMAs of tile g - 2.
+        ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&sh->rope_empty[g & 1]), ((g >> 1) & 1) ^ 1, abortf, p.status,
                                               p.wait_limit_ns));
         if (!ok) break;
-        uint8_t* dst = rope + di * 64;                                        // [128 x 64 B] SW64
+        uint8_t* dst = rope + (g & 1) * kRopeBytes + di * 64;                 // [128 x 64 B] SW64
         uint4 lo, hi;
-        deq_block(v0, sh->lut[kpk[2] & 15u], lo, hi);
-        *reinterpret_cast<uint4*>(dst + ((0 ^ ssw) << 4)) = lo;
-        *reinterpret_cast<uint4*>(dst + ((1 ^ ssw) << 4)) = hi;
-        deq_block(v1, sh->lut[(kpk[2] >> 4) & 15u], lo, hi);
-        *reinterpret_cast<uint4*>(dst + ((2 ^ ssw) << 4)) = lo;
-        *reinterpret_cast<uint4*>(dst + ((3 ^ ssw) << 4)) = hi;
-        sh->etok[g & 3][di] = emax;
+        if constexpr (kRT == 1) {
+          deq_block(v0, sh->lut[kpk[2] & 15u], lo, hi);
+          *reinterpret_cast<uint4*>(dst + ((0 ^ ssw) << 4)) = lo;
+          *reinterpret_cast<uint4*>(dst + ((1 ^ ssw) << 4)) = hi;
+          deq_block(v1, sh->lut[(kpk[2] >> 4) & 15u], lo, hi);
+          *reinterpret_cast<uint4*>(dst + ((2 ^ ssw) << 4)) = lo;
+          *reinterpret_cast<uint4*>(dst + ((3 ^ ssw) << 4)) = hi;
+        } else {
+          deq_block(v0, sh->lut[(kpk[2] >> (4 * hh)) & 15u], lo, hi);
+          *reinterpret_cast<uint4*>(dst + (((2 * hh) ^ ssw) << 4)) = lo;
+          *reinterpret_cast<uint4*>(dst + (((2 * hh + 1) ^ ssw) << 4)) = hi;
+        }
+        if (hh == 0) sh->etok[g & 3][di] = emax;
         fence_proxy_async_smem();
-        warp_arrive(smem_u32(&sh->rope_full[0]));
+        warp_arrive(smem_u32(&sh->rope_full[g & 1]));
       }
       // The value slots of tile g were last read by tile g - 2: one wait on its PV completion
       // covers all four (QK of g - 2 completed before its softmax, hence before its PV).
@@ -905,17 +923,20 @@ __device__ void run_dequant(const DecodeParams& p, SharedState* sh, uint8_t* rin
         // The packed words are read with volatile loads, which ptxas schedules better here
         // (256 x 8192: 376 -> 345 us).
         const uint32_t srow = smem_u32(slabs + si * kSlabBytes + di * 64);
-        uint4 v[4];
+        constexpr int kB = 4 / kRT;                                           // blocks per thread
+        const int b0 = kRT == 1 ? 0 : kB * hh;
+        uint4 v[kB];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) v[q] = ld_shared_v4_volatile(srow + ((q ^ ssw) << 4));
+        for (int q = 0; q < kB; ++q) v[q] = ld_shared_v4_volatile(srow + (((b0 + q) ^ ssw) << 4));
         fence_proxy_async_smem();   // generic reads before the slab's next async-proxy fill (above)
         warp_arrive(smem_u32(&sh->slab_empty[si]));
         uint8_t* dst = ring + (vslot0 + c) * C::kSlotBytes + di * 128;       // [128 x 128 B] SW128
-        const uint32_t kc = static_cast<uint32_t>(kv64 >> (16 * c));          // blocks 4c .. 4c+3
+        const uint32_t kc = static_cast<uint32_t>(kv64 >> (16 * c + 4 * b0)); // blocks 4c + b0 ..
 #pragma unroll
-        for (int bk = 0; bk < 4; ++bk) {
+        for (int q = 0; q < kB; ++q) {
+          const int bk = b0 + q;
           uint4 lo, hi;
-          deq_block(v[bk], sh->lut[(kc >> (4 * bk)) & 15u], lo, hi);
+          deq_block(v[q], sh->lut[(kc >> (4 * q)) & 15u], lo, hi);
           *reinterpret_cast<uint4*>(dst + (((2 * bk) ^ (di & 7)) << 4)) = lo;
           *reinterpret_cast<uint4*>(dst + (((2 * bk + 1) ^ (di & 7)) << 4)) = hi;
         }
