@@ -384,7 +384,7 @@ def main():
         if not args.quick:
             raise SystemExit("--page-size is a --quick measurement")
         if args.q_len > 1:
-            ns = max(1, min(sms // (B * args.q_len), 4096))   # the library's multi-query default
+            ns = 0          # the library's multi-query default (uniform splits over the query-token pairs)
         paged = synth.to_paged(inp, args.page_size, seed=spec.seed + 7).to(dev)
         if args.q_len > 1:
             mq, mqo = synth.make_queries([args.q_len] * B, seed=spec.seed + 8, device=dev)

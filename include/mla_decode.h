@@ -145,13 +145,17 @@ int mla_decode_paged(const void* q, const void* kv, const void* kv_scale, const 
  *  total_q      >= 1: query rows.
  *  out          bf16 [total_q][16][512] (device).
  *  batch        >= 1: sequences (entries of the page table).
- *  num_splits   >= 1: uniform splits of each query row's visible range; <= 0: the library's
- *               choice, max(1, floor(SMs / total_q)) uniform splits (no balanced mode).
+ *  num_splits   >= 1: uniform splits of the visible range; <= 0: the library's choice,
+ *               max(1, floor(SMs / U)) uniform splits (no balanced mode), U = ceil(total_q / 2)
+ *               for bf16 and fp8 caches, total_q for MXFP4.
  *  kv, kv_scale, kv_page_indptr, kv_page_indices, kv_last_page_len, page_size, kv_dtype,
  *  stream: as mla_decode_paged.
- * Each query row reads its own visible range of the cache (rows of one sequence share the
- * cache through L2, not in one pass).  Errors: as mla_decode_paged, plus
- * MLA_ERR_INVALID_ARG for a null or misaligned qo_indptr or total_q <= 0.
+ * bf16 and fp8 caches: the query tokens of a sequence are decoded two at a time (tokens 2i
+ * and 2i + 1 share one pass over the cache; the 32 query rows x heads sit on the MMA's N
+ * side and each keeps its own causal mask).  MXFP4 caches: each query row reads its own
+ * visible range (rows of one sequence share the cache through L2).  Errors: as
+ * mla_decode_paged, plus MLA_ERR_INVALID_ARG for a null or misaligned qo_indptr or
+ * total_q <= 0.
  */
 int mla_decode_paged_multi(const void* q, const int32_t* qo_indptr, int total_q, const void* kv,
                            const void* kv_scale, const int32_t* kv_page_indptr,

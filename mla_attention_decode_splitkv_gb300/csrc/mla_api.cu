@@ -300,7 +300,11 @@ static int decode_impl(const void* q, const void* kv, const void* kv_scale, cons
   if (cc != 103) return MLA_ERR_UNSUPPORTED;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
   int ns = num_splits >= 1 ? num_splits : 0;
-  if (qo_indptr != nullptr && ns == 0) ns = std::max(1, std::min(sms / batch, mla::kMaxSplits));   // uniform only
+  // Several query tokens per sequence: bf16 and fp8 caches decode them two at a time (the
+  // fused instances; the CTAs of odd-numbered tokens exit at once), MXFP4 one query row per CTA.
+  const bool pairs = qo_indptr != nullptr && kv_dtype != MLA_KV_MXFP4;
+  const int units = pairs ? (batch + 1) / 2 : batch;   // (an estimate: tokens per sequence may vary)
+  if (qo_indptr != nullptr && ns == 0) ns = std::max(1, std::min(sms / units, mla::kMaxSplits));   // uniform only
   const long long grid_ll = ns >= 1 ? static_cast<long long>(batch) * ns : sms;
   if (grid_ll > 0x7fffffffLL) return MLA_ERR_INVALID_ARG;
 
@@ -326,6 +330,7 @@ static int decode_impl(const void* q, const void* kv, const void* kv_scale, cons
   p.last_page_len = last_page_len;
   p.qo_indptr = qo_indptr;
   p.num_seqs = num_seqs;
+  p.pair_rows = pairs ? 1 : 0;
   p.q = static_cast<const uint16_t*>(q);
   p.kv = static_cast<const uint8_t*>(kv);
   p.kv_scale = kv_scale;

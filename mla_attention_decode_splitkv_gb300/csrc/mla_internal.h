@@ -47,6 +47,7 @@ struct DecodeParams {
   // only): batch counts query rows, qo_indptr [num_seqs + 1] maps sequences to query rows.
   const int32_t* qo_indptr;
   int num_seqs;
+  int pair_rows;                   // fused multi-token instances: a CTA decodes query rows t, t + 1 together
 };
 
 

@@ -118,7 +118,7 @@ struct Cfg<2> {                    // MXFP4 cache: dequantised to an e4m3 carrie
 };
 static_assert(Cfg<2>::kRegsNeeded <= 65536, "MXFP4 register split exceeds the register file");
 
-constexpr int kPBytes = 4096;      // one P^T buffer: [128 tokens x 32 B] SW32
+constexpr int kPBytes = 4096;      // one P^T buffer: [128 tokens x 32 B] SW32 (one query token)
 constexpr int kSlabBytes = 8192;   // MXFP4 staging: 64 packed bytes (4 blocks) of each of 128 rows, SW64
 constexpr int kSlabs = 5;          // slab ring: a tile is 5 slabs (4 value chunks + rope)
 // MXFP4 tiles are fetched, converted and multiplied rope chunk first: its carrier buffer is
@@ -143,9 +143,9 @@ struct SharedState {
   uint64_t o_free;
   uint64_t mma_done[3];
   uint64_t never;                  // test hook: a barrier nothing arrives on
-  alignas(16) float red[2][4][16];  // read as float4
-  alignas(16) float lsum[4][16];
-  alignas(16) float qscale[16];
+  alignas(16) float red[2][4][32];  // read as float4; [token * 16 + head]
+  alignas(16) float lsum[4][32];
+  alignas(16) float qscale[32];
   uint64_t slab_full[kSlabs];      // MXFP4 only
   uint64_t slab_empty[kSlabs];
   uint64_t etok_full[4];
@@ -165,6 +165,26 @@ struct SharedState {
 static_assert(offsetof(SharedState, red) % 16 == 0, "float4 reads of SharedState::red need 16-byte alignment");
 static_assert(offsetof(SharedState, lut) % 8 == 0, "uint2 reads of SharedState::lut need 8-byte alignment");
 
+// Geometry of a kernel instance that decodes QL query tokens of a sequence at once (QL = 2:
+// the fused multi-token instances).  The QL x 16 query rows (x 2 e4m3 terms for fp8) sit on
+// the MMAs' N side, so each cached tile is read once for all of them.  QL = 1 is Cfg<KV> as is.
+template <int KV, int QL>
+struct Geo {
+  using C = Cfg<KV>;
+  static_assert(QL == 1 || (QL == 2 && KV != 2), "fused multi-token instances: bf16 and fp8 caches");
+  static constexpr int kN = C::kN * QL;                 // MMA N: query rows (x2 for the e4m3 hi + lo terms)
+  static constexpr int kSCols = C::kSCols * QL;         // TMEM columns of one S buffer
+  static constexpr int kOCols = C::kOCols * QL;         // TMEM columns of one O block (128 dims)
+  static constexpr int kTokCols = C::kSCols;            // columns per query token (in S and in O)
+  static constexpr int kTmemCols = QL == 1 ? C::kTmemCols : (2 * kSCols + 4 * kOCols <= 256 ? 256 : 512);
+  static constexpr int kQBytes = C::kQBytes * QL;
+  static constexpr int kQChunk = (KV == 0 ? 2048 : 4096) * QL;   // one K-major q chunk [rows x 128 B]
+  static constexpr int kPBuf = kPBytes * QL;            // one P^T buffer: [128 tokens x 32 QL B]
+  // The second query token's q and P^T buffers take ring slots: fp8 keeps 9 (2.25 tiles),
+  // bf16 one tile's 5.
+  static constexpr int kRing = QL == 1 ? C::kRing : (KV == 1 ? 9 : C::kRingPT);
+};
+
 template <int KV>
 __host__ __device__ constexpr size_t raw_bytes() {
   return KV == 2 ? (size_t)kSlabs * kSlabBytes : 0;
@@ -173,18 +193,22 @@ template <int KV>
 __host__ __device__ constexpr size_t rope_bytes() {
   return (size_t)Cfg<KV>::kRopeSlots * kRopeBytes;
 }
-template <int KV>
+template <int KV, int QL = 1>
 __host__ __device__ constexpr size_t smem_bytes() {
-  return 1024 + (size_t)Cfg<KV>::kRing * Cfg<KV>::kSlotBytes + rope_bytes<KV>() + Cfg<KV>::kQBytes + 2 * kPBytes +
+  using G = Geo<KV, QL>;
+  return 1024 + (size_t)G::kRing * Cfg<KV>::kSlotBytes + rope_bytes<KV>() + G::kQBytes + 2 * G::kPBuf +
          raw_bytes<KV>() + sizeof(SharedState);
 }
 static_assert(smem_bytes<2>() <= 232448, "MXFP4 shared memory exceeds 227 KB");
 static_assert(smem_bytes<1>() <= 232448, "fp8 shared memory exceeds 227 KB");
 static_assert(smem_bytes<0>() <= 232448, "bf16 shared memory exceeds 227 KB");
+static_assert(smem_bytes<1, 2>() <= 232448, "fused two-token fp8 shared memory exceeds 227 KB");
+static_assert(smem_bytes<0, 2>() <= 232448, "fused two-token bf16 shared memory exceeds 227 KB");
 
 // ---------------------------------------------------------------- work decomposition
 struct Seg {
-  int b;       // batch row
+  int rows;    // query rows decoded together: 1, or 2 in the fused multi-token instances
+  int b;       // batch row (the first of the `rows` query rows)
   int row0;    // kv_indptr[b] (paged: the sequence's first entry in the page list)
   int n_total; // tokens in the sequence
   int n_lo;    // token range [n_lo, n_hi) within the sequence
@@ -280,6 +304,7 @@ struct SegIter {
     if (uniform) {
       int r0;
       long long L;
+      int rows = 1;
       if constexpr (PG) {
         // b is a query row.  Several query tokens per sequence (qo_indptr): row b is token
         // t of the q_len tokens of sequence sb and sees the first L - q_len + 1 + t tokens.
@@ -297,7 +322,16 @@ struct SegIter {
         L = L > 0 ? (L - 1) * p.page_size + p.last_page_len[sb] : 0;
         if (p.qo_indptr != nullptr) {
           const int qn = p.qo_indptr[sb + 1] - p.qo_indptr[sb];
-          L -= qn - 1 - (b - p.qo_indptr[sb]);
+          int t0 = b - p.qo_indptr[sb], last = t0;
+          if (p.pair_rows) {
+            // Fused instances: the CTAs of an even-numbered token t0 decode tokens t0 and
+            // t0 + 1 together (their segment is the visible range of the later one); those
+            // of an odd-numbered token have no work.
+            if (t0 & 1) { done = true; return false; }
+            if (t0 + 1 < qn) last = t0 + 1;
+            rows = last - t0 + 1;
+          }
+          L -= qn - 1 - last;
           if (L < 0) L = 0;
         }
       } else {
@@ -309,7 +343,7 @@ struct SegIter {
       long long a = split * chunk, e = a + chunk;
       if (a > L) a = L;
       if (e > L) e = L;
-      s.b = b; s.row0 = r0; s.n_lo = (int)a; s.n_hi = (int)e; s.n_total = (int)L;
+      s.rows = rows; s.b = b; s.row0 = r0; s.n_lo = (int)a; s.n_hi = (int)e; s.n_total = (int)L;
       s.slot = b * ns + split; s.direct = (ns == 1);
       done = true;
       return true;
@@ -333,12 +367,12 @@ struct SegIter {
       if (r1 > r0) {
         long long a = lo > r0 ? lo : r0, e = hi < r1 ? hi : r1;
         if (e > a) {
-          s.b = bb; s.row0 = row0; s.n_lo = (int)(a - r0); s.n_hi = (int)(e - r0); s.n_total = (int)(r1 - r0);
+          s.rows = 1; s.b = bb; s.row0 = row0; s.n_lo = (int)(a - r0); s.n_hi = (int)(e - r0); s.n_total = (int)(r1 - r0);
           s.slot = bb + cta; s.direct = (a == r0 && e == r1);
           return true;
         }
       } else if (r0 >= lo && (r0 < hi || last_cta)) {
-        s.b = bb; s.row0 = row0; s.n_lo = 0; s.n_hi = 0; s.n_total = 0; s.slot = bb + cta; s.direct = true;
+        s.rows = 1; s.b = bb; s.row0 = row0; s.n_lo = 0; s.n_hi = 0; s.n_total = 0; s.slot = bb + cta; s.direct = true;
         return true;
       }
     }
@@ -416,28 +450,38 @@ __device__ __forceinline__ void warp_arrive(uint32_t bar) {
 }
 
 // ---------------------------------------------------------------- q staging
-// bf16: Q[16 x 576] -> 9 K-major SW128 chunks [16 rows x 128 B].
-__device__ void stage_q_bf16(const DecodeParams& p, int b, uint8_t* qs, int ts) {
-  const uint4* src = reinterpret_cast<const uint4*>(p.q + static_cast<size_t>(b) * kHeads * kDim);
-  for (int i = ts; i < kHeads * 72; i += 128) {
+// bf16: Q[16 x 576] -> 9 K-major SW128 chunks [16 QL rows x 128 B]; query token j (staged by
+// threads 128 j .. 128 j + 127) fills rows 16 j .. 16 j + 15 of every chunk (zeros when the
+// token does not exist: `rows` query rows are staged).
+template <int QL>
+__device__ void stage_q_bf16(const DecodeParams& p, int b, int rows, uint8_t* qs, int ts) {
+  const int tok = ts >> 7, t = ts & 127;
+  const uint4* src = reinterpret_cast<const uint4*>(p.q + static_cast<size_t>(b + tok) * kHeads * kDim);
+  for (int i = t; i < kHeads * 72; i += 128) {
     int h = i / 72, pc = i % 72;
     int c = pc >> 3, j = pc & 7;
-    uint4 v = __ldg(src + h * 72 + pc);
-    *reinterpret_cast<uint4*>(qs + c * 2048 + h * 128 + ((j ^ (h & 7)) << 4)) = v;
+    const int r = 16 * tok + h;
+    uint4 v = tok < rows ? __ldg(src + h * 72 + pc) : make_uint4(0u, 0u, 0u, 0u);
+    *reinterpret_cast<uint4*>(qs + c * 2048 * QL + r * 128 + ((j ^ (r & 7)) << 4)) = v;
   }
 }
 
 // fp8 path: per head h, q*2^a_h = hi + lo/16 with hi, lo e4m3 (exact for every bf16 q whose
-// scaled magnitude is >= 2^-6; a_h puts the head's max near 2^8).  Rows 0-15 of each
-// [32 x 128 B] chunk hold hi, rows 16-31 hold lo.  qscale[h] = 2^-a_h.
-__device__ void stage_q_fp8(const DecodeParams& p, int b, uint8_t* qs, float* qscale, int ts) {
-  const int h = ts >> 3, t8 = ts & 7;
-  const uint4* src = reinterpret_cast<const uint4*>(p.q + (static_cast<size_t>(b) * kHeads + h) * kDim + 72 * t8);
+// scaled magnitude is >= 2^-6; a_h puts the head's max near 2^8).  For query token j (staged
+// by threads 128 j .. 128 j + 127), rows 32 j + 0..15 of each [32 QL x 128 B] chunk hold hi
+// and rows 32 j + 16..31 hold lo; qscale[16 j + h] = 2^-a_h.  A token that does not exist
+// (j >= rows) is staged as zeros.
+template <int QL>
+__device__ void stage_q_fp8(const DecodeParams& p, int b, int rows, uint8_t* qs, float* qscale, int ts) {
+  const int tok = ts >> 7;
+  const int h = (ts & 127) >> 3, t8 = ts & 7;
+  const uint4* src =
+      reinterpret_cast<const uint4*>(p.q + (static_cast<size_t>(b + tok) * kHeads + h) * kDim + 72 * t8);
   uint4 v[9];
   float amax = 0.f;
 #pragma unroll
   for (int i = 0; i < 9; ++i) {
-    v[i] = __ldg(src + i);
+    v[i] = tok < rows ? __ldg(src + i) : make_uint4(0u, 0u, 0u, 0u);
     const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -452,7 +496,7 @@ __device__ void stage_q_fp8(const DecodeParams& p, int b, uint8_t* qs, float* qs
   frexpf(amax, &e);
   const int a = amax > 0.f ? min(max(8 - e, -126), 126) : 0;
   const float sc = pow2i(a);
-  if (t8 == 0) qscale[h] = pow2i(-a);
+  if (t8 == 0) qscale[16 * tok + h] = pow2i(-a);
 #pragma unroll
   for (int i = 0; i < 9; ++i) {
     const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
@@ -470,15 +514,15 @@ __device__ void stage_q_fp8(const DecodeParams& p, int b, uint8_t* qs, float* qs
     }
     const int f0 = 72 * t8 + 8 * i;
     const int c = f0 >> 7, jb = f0 & 127, piece = jb >> 4, half = (jb >> 3) & 1;
-    if (c < 4) {   // value dims: [32 rows x 128 B] SW128 chunks
+    const int rh = 32 * tok + h, rl = rh + 16;
+    if (c < 4) {   // value dims: [32 QL rows x 128 B] SW128 chunks
       const int off = ((piece ^ (h & 7)) << 4) + half * 8;
-      *reinterpret_cast<uint2*>(qs + c * 4096 + h * 128 + off) = make_uint2(hi[0], hi[1]);
-      *reinterpret_cast<uint2*>(qs + c * 4096 + (16 + h) * 128 + off) = make_uint2(lo[0], lo[1]);
-    } else {       // rope dims: [32 rows x 64 B] SW64
-      const int rh = h, rl = 16 + h;
-      *reinterpret_cast<uint2*>(qs + 4 * 4096 + rh * 64 + ((piece ^ ((rh >> 1) & 3)) << 4) + half * 8) =
+      *reinterpret_cast<uint2*>(qs + c * 4096 * QL + rh * 128 + off) = make_uint2(hi[0], hi[1]);
+      *reinterpret_cast<uint2*>(qs + c * 4096 * QL + rl * 128 + off) = make_uint2(lo[0], lo[1]);
+    } else {       // rope dims: [32 QL rows x 64 B] SW64
+      *reinterpret_cast<uint2*>(qs + 4 * 4096 * QL + rh * 64 + ((piece ^ ((rh >> 1) & 3)) << 4) + half * 8) =
           make_uint2(hi[0], hi[1]);
-      *reinterpret_cast<uint2*>(qs + 4 * 4096 + rl * 64 + ((piece ^ ((rl >> 1) & 3)) << 4) + half * 8) =
+      *reinterpret_cast<uint2*>(qs + 4 * 4096 * QL + rl * 64 + ((piece ^ ((rl >> 1) & 3)) << 4) + half * 8) =
           make_uint2(lo[0], lo[1]);
     }
   }
@@ -568,9 +612,10 @@ __device__ void run_producer_mx(const DecodeParams& p, SharedState* sh, uint8_t*
   }
 }
 
-template <int KV, bool PG>
+template <int KV, bool PG, int QL>
 __device__ void run_producer(const DecodeParams& p, SharedState* sh, uint8_t* ring, uint8_t* rope, int lane) {
   using C = Cfg<KV>;
+  constexpr int kRing = Geo<KV, QL>::kRing;
   volatile int* abortf = &sh->abort;
   SegIter<PG> it;
   it.init(p, blockIdx.x, sh->seg_total, sh->seg_b0);
@@ -607,7 +652,7 @@ __device__ void run_producer(const DecodeParams& p, SharedState* sh, uint8_t* ri
           box(dst, 128 * c, 16384);
         }
         ++idx;
-        if (++slot == C::kRing) { slot = 0; phase ^= 1; }
+        if (++slot == kRing) { slot = 0; phase ^= 1; }
       }
       if constexpr (C::kRopeSlots > 0) {   // fp8: the rope chunk (64 B of each row) into its own slots
         if (!ok) break;
@@ -625,9 +670,9 @@ __device__ void run_producer(const DecodeParams& p, SharedState* sh, uint8_t* ri
     }
   }
   if (!ok) {  // drain copies already issued so that none lands after the CTA exits
-    const uint32_t first = idx > (uint32_t)C::kRing ? idx - C::kRing : 0u;
+    const uint32_t first = idx > (uint32_t)kRing ? idx - kRing : 0u;
     for (uint32_t j = first; j < idx; ++j)
-      wait_bar(smem_u32(&sh->full[j % C::kRing]), (j / C::kRing) & 1, abortf, p.status, kDrainLimitNs, false);
+      wait_bar(smem_u32(&sh->full[j % kRing]), (j / kRing) & 1, abortf, p.status, kDrainLimitNs, false);
     if constexpr (C::kRopeSlots > 0) {
       const uint32_t rfirst = ridx > (uint32_t)C::kRopeSlots ? ridx - C::kRopeSlots : 0u;
       for (uint32_t j = rfirst; j < ridx; ++j)
@@ -661,7 +706,7 @@ __device__ __forceinline__ void sp_copy(const uint8_t* kv, int row_bytes, const 
   }
 }
 
-template <int KV>
+template <int KV, int QL>
 __device__ void run_producer_sp(const DecodeParams& p, SharedState* sh, uint8_t* ring, uint8_t* rope, uint8_t* slabs,
                                 int lane) {
   using C = Cfg<KV>;
@@ -671,7 +716,7 @@ __device__ void run_producer_sp(const DecodeParams& p, SharedState* sh, uint8_t*
   it.init(p, blockIdx.x, sh->seg_total, sh->seg_b0);
   Seg s;
   uint32_t idx = 0, slot = 0, phase = 0, ridx = 0;
-  constexpr int kSlots = KV == 2 ? kSlabs : C::kRing;
+  constexpr int kSlots = KV == 2 ? kSlabs : Geo<KV, QL>::kRing;
   bool ok = true;
   while (ok && it.next(p, s)) {
     const int n = s.n_hi - s.n_lo;
@@ -964,23 +1009,26 @@ struct Descs {
   uint64_t q_rope;   // K-major SW64 descriptor of the q rope chunk (fp8 / MXFP4)
   uint64_t p;        // MN-major SW32 descriptor of P buffer 0 (sbo = 256)
 };
+template <int QL>
 __device__ __forceinline__ Descs make_descs(uint8_t* ring, uint8_t* rope, uint8_t* qs, uint8_t* ps) {
   Descs d;
   d.ring_k = smem_desc(smem_u32(ring), 16, 1024, kSwizzle128B);
   d.ring_mn = smem_desc(smem_u32(ring), 16384, 1024, kSwizzle128B);
   d.rope = smem_desc(smem_u32(rope), 16, 512, kSwizzle64B);
   d.q = smem_desc(smem_u32(qs), 16, 1024, kSwizzle128B);
-  d.q_rope = smem_desc(smem_u32(qs + 4 * 4096), 16, 512, kSwizzle64B);
-  d.p = smem_desc(smem_u32(ps), 0, 256, kSwizzle32B);
+  d.q_rope = smem_desc(smem_u32(qs + 4 * 4096 * QL), 16, 512, kSwizzle64B);
+  // P^T rows are 32 QL bytes: one SW32 atom (QL = 1) or one SW64 atom (QL = 2) along N.
+  d.p = QL == 1 ? smem_desc(smem_u32(ps), 0, 256, kSwizzle32B) : smem_desc(smem_u32(ps), 0, 512, kSwizzle64B);
   return d;
 }
 // Byte offset -> descriptor start-address increment.
 __device__ __forceinline__ uint64_t dofs(uint32_t bytes) { return static_cast<uint64_t>(bytes >> 4); }
 
-template <int KV, bool PG, bool SP>
+template <int KV, bool PG, bool SP, int QL>
 __device__ void run_mma_qk(const DecodeParams& p, SharedState* sh, const Descs& ds, uint32_t tmem) {
   using C = Cfg<KV>;
-  constexpr uint32_t idq = instr_desc(KV == 0 ? 1u : 0u, 0, 0, 128, C::kN);  // bf16 | e4m3, K-major A and B
+  using G = Geo<KV, QL>;
+  constexpr uint32_t idq = instr_desc(KV == 0 ? 1u : 0u, 0, 0, 128, G::kN);  // bf16 | e4m3, K-major A and B
   volatile int* abortf = &sh->abort;
   SegIter<PG> it;
   it.init(p, blockIdx.x, sh->seg_total, sh->seg_b0);
@@ -998,7 +1046,7 @@ __device__ void run_mma_qk(const DecodeParams& p, SharedState* sh, const Descs& 
       if (g >= 2 && !(ok = wait_bar(smem_u32(&sh->s_free[g & 1]), ((g >> 1) & 1) ^ 1, abortf, p.status,
                                     p.wait_limit_ns)))
         break;
-      const uint32_t d = tmem + (g & 1) * C::kSCols;
+      const uint32_t d = tmem + (g & 1) * G::kSCols;
 #pragma unroll
       for (int i = 0; i < C::kSPT; ++i) {
         const int c = KV == 2 ? mx_chunk(i) : i;                             // MXFP4: the dequantisation order
@@ -1011,21 +1059,21 @@ __device__ void run_mma_qk(const DecodeParams& p, SharedState* sh, const Descs& 
         if constexpr (SP && KV != 2) fence_proxy_async_smem();   // cp.async (generic-proxy) data, read by the MMAs
         const uint64_t a = rope_sep ? ds.rope + dofs(rs * kRopeBytes) : ds.ring_k + dofs(slot * C::kSlotBytes);
         if constexpr (KV == 0) {
-          const uint64_t b = ds.q + dofs(2 * c * 2048);
+          const uint64_t b = ds.q + dofs(2 * c * G::kQChunk);
 #pragma unroll
           for (int k = 0; k < 4; ++k) mma_f16(d, a + dofs(32 * k), b + dofs(32 * k), idq, (c | k) != 0);
           if (c < 4) {
 #pragma unroll
-            for (int k = 0; k < 4; ++k) mma_f16(d, a + dofs(16384 + 32 * k), b + dofs(2048 + 32 * k), idq, 1u);
+            for (int k = 0; k < 4; ++k) mma_f16(d, a + dofs(16384 + 32 * k), b + dofs(G::kQChunk + 32 * k), idq, 1u);
           }
         } else {
-          const uint64_t b = c < 4 ? ds.q + dofs(c * 4096) : ds.q_rope;
+          const uint64_t b = c < 4 ? ds.q + dofs(c * G::kQChunk) : ds.q_rope;
 #pragma unroll
           for (int k = 0; k < (c < 4 ? 4 : 2); ++k) mma_f8(d, a + dofs(32 * k), b + dofs(32 * k), idq, (i | k) != 0);
         }
         if (c == C::kSPT - 1)   // the rope chunk is read by QK only
           mma_commit(rope_sep ? smem_u32(&sh->rope_empty[rs]) : smem_u32(&sh->empty[slot]));
-        if (!rope_sep && ++slot == C::kRing) { slot = 0; phase ^= 1; }
+        if (!rope_sep && ++slot == G::kRing) { slot = 0; phase ^= 1; }
       }
       if (ok) mma_commit(smem_u32(&sh->s_full[g & 1]));
     }
@@ -1036,10 +1084,11 @@ __device__ void run_mma_qk(const DecodeParams& p, SharedState* sh, const Descs& 
 }
 
 // PV issuer `part` (0 or 1) issues the two 128-dim blocks 2*part, 2*part+1 of every tile.
-template <int KV, bool PG, bool SP>
+template <int KV, bool PG, bool SP, int QL>
 __device__ void run_mma_pv(const DecodeParams& p, SharedState* sh, const Descs& ds, uint32_t tmem, int part) {
   using C = Cfg<KV>;
-  constexpr uint32_t idp = instr_desc(KV == 0 ? 1u : 0u, 1, 1, 128, C::kN);  // MN-major A (V^T) and B (P^T)
+  using G = Geo<KV, QL>;
+  constexpr uint32_t idp = instr_desc(KV == 0 ? 1u : 0u, 1, 1, 128, G::kN);  // MN-major A (V^T) and B (P^T)
   volatile int* abortf = &sh->abort;
   SegIter<PG> it;
   it.init(p, blockIdx.x, sh->seg_total, sh->seg_b0);
@@ -1059,26 +1108,27 @@ __device__ void run_mma_pv(const DecodeParams& p, SharedState* sh, const Descs& 
       tc_fence_after();
       if constexpr (SP && KV != 2) fence_proxy_async_smem();     // cp.async (generic-proxy) data, read by the MMAs
       const bool first = (t == 0);
-      const uint64_t b = ds.p + dofs((g & 1) * kPBytes);
+      const uint64_t b = ds.p + dofs((g & 1) * G::kPBuf);
 #pragma unroll
       for (int mm = 0; mm < 2; ++mm) {
         const int m = 2 * part + mm;
         uint32_t slot = slot0 + m;
-        if (slot >= C::kRing) slot -= C::kRing;
+        if (slot >= G::kRing) slot -= G::kRing;
         const uint64_t a = ds.ring_mn + dofs(slot * C::kSlotBytes);
-        const uint32_t d = tmem + 2 * C::kSCols + m * C::kOCols;
+        const uint32_t d = tmem + 2 * G::kSCols + m * G::kOCols;
+        // K steps of the P^T operand: 16 (bf16) or 32 (e4m3) token rows of 32 QL bytes
         if constexpr (KV == 0) {
 #pragma unroll
-          for (int k = 0; k < 8; ++k) mma_f16(d, a + dofs(2048 * k), b + dofs(512 * k), idp, !(first && k == 0));
+          for (int k = 0; k < 8; ++k) mma_f16(d, a + dofs(2048 * k), b + dofs(512 * QL * k), idp, !(first && k == 0));
         } else {
 #pragma unroll
-          for (int k = 0; k < 4; ++k) mma_f8(d, a + dofs(4096 * k), b + dofs(1024 * k), idp, !(first && k == 0));
+          for (int k = 0; k < 4; ++k) mma_f8(d, a + dofs(4096 * k), b + dofs(1024 * QL * k), idp, !(first && k == 0));
         }
         mma_commit(smem_u32(&sh->empty[slot]));
       }
       mma_commit(smem_u32(&sh->pv_done[g & 1]));   // completes once both PV issuers have committed
       slot0 += C::kRingPT;
-      if (slot0 >= C::kRing) slot0 -= C::kRing;
+      if (slot0 >= G::kRing) slot0 -= G::kRing;
     }
     ++kseg;
   }
@@ -1316,12 +1366,19 @@ __device__ void write_empty_result(const DecodeParams& p, const Seg& s, int ts) 
 // per-tile latency of this stage); kSoftWarps = 4 gives each thread all 16 heads.  The two
 // head groups never share a named barrier on a path the other may skip: every named
 // barrier below is reached by all softmax threads once per tile (or once per segment).
-template <int KV, bool PG>
+// QL = 2 (fused multi-token instances): the thread owns its H heads for both query tokens of
+// the segment, K = QL H columns; column k is token k / H, head h0 + k % H.  Token j of a
+// segment of `rows` query rows sees the first n_total - (rows - 1 - j) cached tokens (the
+// causal mask of the multi-token interface); a token with no visible row in the segment
+// gets P = 0 and a piece with log-sum-exp -inf (or a zero output row).
+template <int KV, bool PG, int QL>
 __device__ void run_softmax(const DecodeParams& p, SharedState* sh, uint8_t* qs, uint8_t* ps, uint32_t tmem) {
   using C = Cfg<KV>;
+  using G = Geo<KV, QL>;
   constexpr int NW = C::kSoftWarps;
   constexpr int NT = NW * 32;
   constexpr int H = 64 / NW;                               // heads per thread: 16 or 8
+  constexpr int K = QL * H;                                // columns per thread
   volatile int* abortf = &sh->abort;
   const int ts = threadIdx.x - 128;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1333,6 +1390,8 @@ __device__ void run_softmax(const DecodeParams& p, SharedState* sh, uint8_t* qs,
   float kv_scale = 1.0f;
   if constexpr (KV == 1) kv_scale = __ldg(reinterpret_cast<const float*>(p.kv_scale));
   const float xscale = p.logit_scale_log2 * kv_scale;    // raw dot product -> log2-domain logit
+  // Column k -> index 16 j + h of the per-(token, head) shared arrays.
+  auto cidx = [&](int k) { return 16 * (k / H) + h0 + (k % H); };
 
   SegIter<PG> it;
   it.init(p, blockIdx.x, sh->seg_total, sh->seg_b0);
@@ -1345,11 +1404,19 @@ __device__ void run_softmax(const DecodeParams& p, SharedState* sh, uint8_t* qs,
     if (first != nullptr && first->n_hi > first->n_lo) { sn = *first; found = true; }
     SegIter<PG> look = from;
     while (!found && look.next(p, sn)) found = sn.n_hi > sn.n_lo;
-    if (found && ts < 128) {
-      if constexpr (KV == 0) stage_q_bf16(p, sn.b, qs, ts); else stage_q_fp8(p, sn.b, qs, sh->qscale, ts);
+    if (found && ts < 128 * QL) {
+      if constexpr (KV == 0) stage_q_bf16<QL>(p, sn.b, sn.rows, qs, ts);
+      else stage_q_fp8<QL>(p, sn.b, sn.rows, qs, sh->qscale, ts);
       fence_proxy_async_smem();
       warp_arrive(smem_u32(&sh->q_ready));
     }
+  };
+  // The single-row segment of query token j of `s` (output row, partial slot).
+  auto token_seg = [&](const Seg& s, int j) {
+    Seg r = s;
+    r.b = s.b + j;
+    r.slot = s.slot + j * p.num_splits;
+    return r;
   };
   if (has_cur) stage_next_nonempty(it, &cur);
   bar_sync(1, NT);  // qscale visible to all softmax threads
@@ -1358,32 +1425,50 @@ __device__ void run_softmax(const DecodeParams& p, SharedState* sh, uint8_t* qs,
   while (ok && has_cur) {
     const int n = cur.n_hi - cur.n_lo;
     if (n <= 0) {
-      write_empty_result<KV>(p, cur, ts);
-      if (!cur.direct) finish_piece<KV, PG>(p, sh, cur, ts, NT);
+      for (int j = 0; j < cur.rows; ++j) {
+        const Seg sj = token_seg(cur, j);
+        write_empty_result<KV>(p, sj, ts);
+        if (!sj.direct) finish_piece<KV, PG>(p, sh, sj, ts, NT);
+      }
       has_cur = it.next(p, cur);
       continue;
     }
-    float qx[H];                                           // per-head logit multiplier
+    // Per-column logit multiplier (QL = 2: read from shared memory where it is used, which
+    // keeps 16 registers free in these instances).
+    float qx[QL == 1 ? K : 1];
+    if constexpr (QL == 1) {
 #pragma unroll
-    for (int h = 0; h < H; ++h) qx[h] = (KV == 0) ? xscale : sh->qscale[h0 + h] * xscale;
+      for (int k = 0; k < K; ++k) qx[k] = (KV == 0) ? xscale : sh->qscale[cidx(k)] * xscale;
+    }
     const int ntiles = (n + kBN - 1) / kBN;
-    float mref[H], lpart[H];
+    float mref[K], lpart[K];
     bool has_nxt = false;
     for (int t = 0; t < ntiles; ++t) {
       const Window w = tile_window<KV, PG>(p, cur, t);
       bool okw = wait_bar(smem_u32(&sh->s_full[g & 1]), (g >> 1) & 1, abortf, p.status, p.wait_limit_ns);
       okw = __all_sync(0xffffffffu, okw);
       tc_fence_after();
-      uint32_t rh[H], rl[H];
+      uint32_t rh[QL][H], rl[QL][H];
       if (okw) {
-        const uint32_t ta = tmem + lane_base + (g & 1) * C::kSCols + h0;
-        tmem_ld<H>(ta, rh);
-        if constexpr (KV != 0) tmem_ld<H>(ta + 16, rl);
+#pragma unroll
+        for (int j = 0; j < QL; ++j) {
+          const uint32_t ta = tmem + lane_base + (g & 1) * G::kSCols + j * G::kTokCols + h0;
+          tmem_ld<H>(ta, rh[j]);
+          if constexpr (KV != 0) tmem_ld<H>(ta + 16, rl[j]);
+        }
         tmem_wait_ld();
       }
       tc_fence_before();
       warp_arrive(smem_u32(&sh->s_free[g & 1]));
       const bool valid = okw && row >= w.shift && row < w.shift + w.cnt;
+      bool vtok[QL];
+      vtok[0] = valid;
+      if constexpr (QL == 2) {
+        // token index of this row in the sequence (paged windows start at the tile's token)
+        const int tok = cur.n_lo + t * kBN + row;
+#pragma unroll
+        for (int j = 0; j < QL; ++j) vtok[j] = valid && j < cur.rows && tok < cur.n_total - (cur.rows - 1 - j);
+      }
       // MXFP4 rows carry a power-of-two factor 2^eadd (eadd = e_row - 127): logits are
       // scaled by it, P is weighted by it (w = x + eadd) and the softmax sum is not.
       float eadd = 0.f, rowf = 1.f;
@@ -1394,50 +1479,55 @@ __device__ void run_softmax(const DecodeParams& p, SharedState* sh, uint8_t* qs,
         eadd = static_cast<float>(e - 127);
         rowf = pow2i(e - 127);
       }
-      float x[H];
+      float x[K];
 #pragma unroll
-      for (int h = 0; h < H; ++h) {
+      for (int k = 0; k < K; ++k) {
+        const int j = k / H, h = k % H;
         float sdot;
-        if constexpr (KV == 0) sdot = __uint_as_float(rh[h]);
-        else sdot = fmaf(__uint_as_float(rl[h]), 0.0625f, __uint_as_float(rh[h])) * rowf;
-        x[h] = valid ? fmaf(sdot, qx[h], eadd) : kNegInf;
+        if constexpr (KV == 0) sdot = __uint_as_float(rh[j][h]);
+        else sdot = fmaf(__uint_as_float(rl[j][h]), 0.0625f, __uint_as_float(rh[j][h])) * rowf;
+        float qk;
+        if constexpr (QL == 1) qk = qx[k];
+        else qk = (KV == 0) ? xscale : sh->qscale[cidx(k)] * xscale;
+        x[k] = vtok[j] ? fmaf(sdot, qk, eadd) : kNegInf;
       }
-      float* red = &sh->red[g & 1][quarter][h0];
+      float* red = &sh->red[g & 1][quarter][0];
 #pragma unroll
-      for (int h = 0; h < H; ++h) {
-        const float m = warp_max(x[h]);
-        if (lane == 0) red[h] = m;
+      for (int k = 0; k < K; ++k) {
+        const float m = warp_max(x[k]);
+        if (lane == 0) red[cidx(k)] = m;
       }
       ok = bar_and(1, NT, okw);
       if (!ok) break;
-      float M[H];
+      float M[K];
 #pragma unroll
-      for (int h4 = 0; h4 < H; h4 += 4) {
-        const float4 a = *reinterpret_cast<const float4*>(&sh->red[g & 1][0][h0 + h4]);
-        const float4 b = *reinterpret_cast<const float4*>(&sh->red[g & 1][1][h0 + h4]);
-        const float4 c = *reinterpret_cast<const float4*>(&sh->red[g & 1][2][h0 + h4]);
-        const float4 d = *reinterpret_cast<const float4*>(&sh->red[g & 1][3][h0 + h4]);
-        M[h4 + 0] = fmaxf(fmaxf(a.x, b.x), fmaxf(c.x, d.x));
-        M[h4 + 1] = fmaxf(fmaxf(a.y, b.y), fmaxf(c.y, d.y));
-        M[h4 + 2] = fmaxf(fmaxf(a.z, b.z), fmaxf(c.z, d.z));
-        M[h4 + 3] = fmaxf(fmaxf(a.w, b.w), fmaxf(c.w, d.w));
+      for (int k4 = 0; k4 < K; k4 += 4) {
+        const int c0 = cidx(k4);
+        const float4 a = *reinterpret_cast<const float4*>(&sh->red[g & 1][0][c0]);
+        const float4 b = *reinterpret_cast<const float4*>(&sh->red[g & 1][1][c0]);
+        const float4 c = *reinterpret_cast<const float4*>(&sh->red[g & 1][2][c0]);
+        const float4 d = *reinterpret_cast<const float4*>(&sh->red[g & 1][3][c0]);
+        M[k4 + 0] = fmaxf(fmaxf(a.x, b.x), fmaxf(c.x, d.x));
+        M[k4 + 1] = fmaxf(fmaxf(a.y, b.y), fmaxf(c.y, d.y));
+        M[k4 + 2] = fmaxf(fmaxf(a.z, b.z), fmaxf(c.z, d.z));
+        M[k4 + 3] = fmaxf(fmaxf(a.w, b.w), fmaxf(c.w, d.w));
       }
       bool need = false;
       if (t == 0) {
 #pragma unroll
-        for (int h = 0; h < H; ++h) { mref[h] = M[h]; lpart[h] = 0.f; }
+        for (int k = 0; k < K; ++k) { mref[k] = M[k]; lpart[k] = 0.f; }
       } else {
 #pragma unroll
-        for (int h = 0; h < H; ++h) need |= (M[h] > mref[h] + C::kTau);
+        for (int k = 0; k < K; ++k) need |= (M[k] > mref[k] + C::kTau);
       }
       if (need) {  // lazy rescale of this head group's O^T columns (uniform within the group)
-        float alpha[H];
+        float alpha[K];
 #pragma unroll
-        for (int h = 0; h < H; ++h) {
-          const float nm = fmaxf(mref[h], M[h]);
-          alpha[h] = ex2(mref[h] - nm);
-          mref[h] = nm;
-          lpart[h] *= alpha[h];
+        for (int k = 0; k < K; ++k) {
+          const float nm = fmaxf(mref[k], M[k]);
+          alpha[k] = ex2(mref[k] - nm);
+          mref[k] = nm;
+          lpart[k] *= alpha[k];
         }
         const uint32_t gp = g - 1;
         bool ok2 = wait_bar(smem_u32(&sh->pv_done[gp & 1]), (gp >> 1) & 1, abortf, p.status, p.wait_limit_ns);
@@ -1447,78 +1537,91 @@ __device__ void run_softmax(const DecodeParams& p, SharedState* sh, uint8_t* qs,
 #pragma unroll 1
           for (int m = 0; m < 4; ++m) {
 #pragma unroll
-            for (int part = 0; part < (KV == 0 ? 1 : 2); ++part) {
-              const uint32_t ta = tmem + lane_base + 2 * C::kSCols + m * C::kOCols + part * 16 + h0;
-              uint32_t v[H];
-              tmem_ld<H>(ta, v);
-              tmem_wait_ld();
+            for (int j = 0; j < QL; ++j) {
 #pragma unroll
-              for (int j = 0; j < H; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * alpha[j]);
-              tmem_st<H>(ta, v);
+              for (int part = 0; part < (KV == 0 ? 1 : 2); ++part) {
+                const uint32_t ta =
+                    tmem + lane_base + 2 * G::kSCols + m * G::kOCols + j * G::kTokCols + part * 16 + h0;
+                uint32_t v[H];
+                tmem_ld<H>(ta, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < H; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha[j * H + i]);
+                tmem_st<H>(ta, v);
+              }
             }
           }
           tmem_wait_st();
         }
         okw = okw && ok2;  // a failed wait aborts at the next tile's barrier
       }
-      // P = 2^(w - mref) <= 2^kTau
-      float P[H];
+      // P = 2^(w - mref) <= 2^kTau (QL = 2: a column with no visible row yet has mref = -inf)
+      float P[K];
 #pragma unroll
-      for (int h = 0; h < H; ++h) P[h] = ex2(x[h] - mref[h]);
+      for (int k = 0; k < K; ++k) P[k] = ex2(x[k] - ((QL == 2 && mref[k] == kNegInf) ? 0.f : mref[k]));
       if (g >= 2) wait_bar(smem_u32(&sh->pv_done[g & 1]), ((g >> 1) & 1) ^ 1, abortf, p.status, p.wait_limit_ns);
-      uint8_t* prow = ps + (g & 1) * kPBytes + row * 32;
-      const int sw = (row >> 2) & 1;
+      // P^T row of this token: 32 QL bytes (per query token: 16 heads of hi then of lo e4m3,
+      // or 16 bf16); swizzled in 16-byte chunks, 32-byte (QL = 1) or 64-byte (QL = 2) pattern.
+      uint8_t* prow = ps + (g & 1) * G::kPBuf + row * 32 * QL;
+      const int sw = QL == 1 ? (row >> 2) & 1 : (row >> 1) & 3;
       if constexpr (KV == 0) {
-        uint32_t wv[H / 2];
 #pragma unroll
-        for (int j = 0; j < H / 2; ++j) {
-          const uint16_t b0 = f_to_bf16_bits(P[2 * j]), b1 = f_to_bf16_bits(P[2 * j + 1]);
-          lpart[2 * j] += bf16_bits_to_f(b0);
-          lpart[2 * j + 1] += bf16_bits_to_f(b1);
-          wv[j] = static_cast<uint32_t>(b0) | (static_cast<uint32_t>(b1) << 16);
+        for (int j = 0; j < QL; ++j) {
+          uint32_t wv[H / 2];
+#pragma unroll
+          for (int i = 0; i < H / 2; ++i) {
+            const int k = j * H + 2 * i;
+            const uint16_t b0 = f_to_bf16_bits(P[k]), b1 = f_to_bf16_bits(P[k + 1]);
+            lpart[k] += bf16_bits_to_f(b0);
+            lpart[k + 1] += bf16_bits_to_f(b1);
+            wv[i] = static_cast<uint32_t>(b0) | (static_cast<uint32_t>(b1) << 16);
+          }
+          // heads [h0, h0 + H) of token j are 16-byte chunk(s) 2 j + h0/8 .. of the row
+#pragma unroll
+          for (int c = 0; c < H / 8; ++c)
+            *reinterpret_cast<uint4*>(prow + (((2 * j + h0 / 8 + c) ^ sw) << 4)) =
+                make_uint4(wv[4 * c], wv[4 * c + 1], wv[4 * c + 2], wv[4 * c + 3]);
         }
-        // heads [h0, h0 + H) are 16-byte chunk(s) h0/8 .. of the 32-byte row
-#pragma unroll
-        for (int c = 0; c < H / 8; ++c)
-          *reinterpret_cast<uint4*>(prow + (((h0 / 8 + c) ^ sw) << 4)) =
-              make_uint4(wv[4 * c], wv[4 * c + 1], wv[4 * c + 2], wv[4 * c + 3]);
       } else {
         // Softmax sum: fp8 caches add the e4m3-rounded P (the values the PV MMAs weight V
         // with).  MXFP4 rows add the fp32 P * 2^-eadd: a row of small magnitude (eadd << 0)
         // can carry a large softmax weight with a PV weight too small for e4m3.
         const float einv = pow2i(-static_cast<int>(eadd) - 4);   // 2^-eadd / 16
         const float escale = pow2i(-static_cast<int>(eadd));      // 2^-eadd
-        uint32_t hw[H / 4], lw[H / 4];
 #pragma unroll
-        for (int j = 0; j < H / 4; ++j) {
-          uint32_t a = 0, b = 0;
+        for (int j = 0; j < QL; ++j) {
+          uint32_t hw[H / 4], lw[H / 4];
 #pragma unroll
-          for (int k = 0; k < 4; k += 2) {
-            const int h = 4 * j + k;
-            const float y0 = P[h] * 16.f, y1 = P[h + 1] * 16.f;
-            const uint32_t hp = pack_e4m3x2(y0, y1);
-            const float2 hd = unpack_e4m3x2(hp);
-            const uint32_t lp = pack_e4m3x2((y0 - hd.x) * 16.f, (y1 - hd.y) * 16.f);
-            if constexpr (KV == 2) {
-              lpart[h] = fmaf(P[h], escale, lpart[h]);
-              lpart[h + 1] = fmaf(P[h + 1], escale, lpart[h + 1]);
-            } else {
-              const float2 ld = unpack_e4m3x2(lp);
-              lpart[h] += fmaf(ld.x, 0.0625f, hd.x) * einv;
-              lpart[h + 1] += fmaf(ld.y, 0.0625f, hd.y) * einv;
+          for (int i = 0; i < H / 4; ++i) {
+            uint32_t a = 0, b = 0;
+#pragma unroll
+            for (int kk = 0; kk < 4; kk += 2) {
+              const int k = j * H + 4 * i + kk;
+              const float y0 = P[k] * 16.f, y1 = P[k + 1] * 16.f;
+              const uint32_t hp = pack_e4m3x2(y0, y1);
+              const float2 hd = unpack_e4m3x2(hp);
+              const uint32_t lp = pack_e4m3x2((y0 - hd.x) * 16.f, (y1 - hd.y) * 16.f);
+              if constexpr (KV == 2) {
+                lpart[k] = fmaf(P[k], escale, lpart[k]);
+                lpart[k + 1] = fmaf(P[k + 1], escale, lpart[k + 1]);
+              } else {
+                const float2 ld = unpack_e4m3x2(lp);
+                lpart[k] += fmaf(ld.x, 0.0625f, hd.x) * einv;
+                lpart[k + 1] += fmaf(ld.y, 0.0625f, hd.y) * einv;
+              }
+              a |= hp << (8 * kk);
+              b |= lp << (8 * kk);
             }
-            a |= hp << (8 * k);
-            b |= lp << (8 * k);
+            hw[i] = a;
+            lw[i] = b;
           }
-          hw[j] = a;
-          lw[j] = b;
-        }
-        if constexpr (H == 16) {
-          *reinterpret_cast<uint4*>(prow + ((0 ^ sw) << 4)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-          *reinterpret_cast<uint4*>(prow + ((1 ^ sw) << 4)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-        } else {
-          *reinterpret_cast<uint2*>(prow + ((0 ^ sw) << 4) + h0) = make_uint2(hw[0], hw[1]);
-          *reinterpret_cast<uint2*>(prow + ((1 ^ sw) << 4) + h0) = make_uint2(lw[0], lw[1]);
+          if constexpr (H == 16) {
+            *reinterpret_cast<uint4*>(prow + (((2 * j) ^ sw) << 4)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            *reinterpret_cast<uint4*>(prow + (((2 * j + 1) ^ sw) << 4)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+          } else {
+            *reinterpret_cast<uint2*>(prow + (((2 * j) ^ sw) << 4) + h0) = make_uint2(hw[0], hw[1]);
+            *reinterpret_cast<uint2*>(prow + (((2 * j + 1) ^ sw) << 4) + h0) = make_uint2(lw[0], lw[1]);
+          }
         }
       }
       fence_proxy_async_smem();
@@ -1539,46 +1642,55 @@ __device__ void run_softmax(const DecodeParams& p, SharedState* sh, uint8_t* qs,
     ok4 = __all_sync(0xffffffffu, ok4);
     tc_fence_after();
 #pragma unroll
-    for (int h = 0; h < H; ++h) {
-      float v = lpart[h];
+    for (int k = 0; k < K; ++k) {
+      float v = lpart[k];
       v += __shfl_xor_sync(0xffffffffu, v, 16);
       v += __shfl_xor_sync(0xffffffffu, v, 8);
       v += __shfl_xor_sync(0xffffffffu, v, 4);
       v += __shfl_xor_sync(0xffffffffu, v, 2);
       v += __shfl_xor_sync(0xffffffffu, v, 1);
-      if (lane == 0) sh->lsum[quarter][h0 + h] = v;
+      if (lane == 0) sh->lsum[quarter][cidx(k)] = v;
     }
     ok = bar_and(1, NT, ok4);
     if (!ok) break;
-    float inv[H];
+    float inv[K];
 #pragma unroll
-    for (int h = 0; h < H; ++h) {
-      const float l = sh->lsum[0][h0 + h] + sh->lsum[1][h0 + h] + sh->lsum[2][h0 + h] + sh->lsum[3][h0 + h];
-      inv[h] = __fdividef(KV == 0 ? 1.0f : kv_scale * 0.0625f, l);
-      if (!cur.direct && quarter == 0 && lane == 0) p.part_lse[cur.slot * kHeads + h0 + h] = mref[h] + lg2(l);
+    for (int k = 0; k < K; ++k) {
+      const int c = cidx(k), j = k / H;
+      const float l = sh->lsum[0][c] + sh->lsum[1][c] + sh->lsum[2][c] + sh->lsum[3][c];
+      inv[k] = __fdividef(KV == 0 ? 1.0f : kv_scale * 0.0625f, l);
+      if constexpr (QL == 2) inv[k] = l > 0.f ? inv[k] : 0.f;   // a token with no visible row: zeros
+      if (!cur.direct && quarter == 0 && lane == 0 && j < cur.rows)
+        p.part_lse[(cur.slot + j * p.num_splits) * kHeads + (k % H) + h0] = mref[k] + lg2(l);
     }
 #pragma unroll 1
     for (int m = 0; m < 4; ++m) {
-      const uint32_t ta = tmem + lane_base + 2 * C::kSCols + m * C::kOCols + h0;
-      uint32_t vh[H], vl[H];
-      tmem_ld<H>(ta, vh);
-      if constexpr (KV != 0) tmem_ld<H>(ta + 16, vl);
-      tmem_wait_ld();
-      const int d = 128 * m + row;
 #pragma unroll
-      for (int h = 0; h < H; ++h) {
-        float o = __uint_as_float(vh[h]);
-        if constexpr (KV != 0) o = fmaf(__uint_as_float(vl[h]), 0.0625f, o);
-        o *= inv[h];
-        if (cur.direct)
-          p.out[(static_cast<size_t>(cur.b) * kHeads + h0 + h) * kDimV + d] = f_to_bf16_bits(o);
-        else
-          p.part_o[(static_cast<size_t>(cur.slot) * kHeads + h0 + h) * kDimV + d] = o;
+      for (int j = 0; j < QL; ++j) {
+        const uint32_t ta = tmem + lane_base + 2 * G::kSCols + m * G::kOCols + j * G::kTokCols + h0;
+        uint32_t vh[H], vl[H];
+        tmem_ld<H>(ta, vh);
+        if constexpr (KV != 0) tmem_ld<H>(ta + 16, vl);
+        tmem_wait_ld();
+        if (j >= cur.rows) continue;
+        const int d = 128 * m + row;
+#pragma unroll
+        for (int h = 0; h < H; ++h) {
+          float o = __uint_as_float(vh[h]);
+          if constexpr (KV != 0) o = fmaf(__uint_as_float(vl[h]), 0.0625f, o);
+          o *= inv[j * H + h];
+          if (cur.direct)
+            p.out[(static_cast<size_t>(cur.b + j) * kHeads + h0 + h) * kDimV + d] = f_to_bf16_bits(o);
+          else
+            p.part_o[(static_cast<size_t>(cur.slot + j * p.num_splits) * kHeads + h0 + h) * kDimV + d] = o;
+        }
       }
     }
     tc_fence_before();
     warp_arrive(smem_u32(&sh->o_free));
-    if (!cur.direct) finish_piece<KV, PG>(p, sh, cur, ts, NT);
+    if (!cur.direct) {
+      for (int j = 0; j < cur.rows; ++j) finish_piece<KV, PG>(p, sh, token_seg(cur, j), ts, NT);
+    }
     cur = nxt;
     has_cur = has_nxt;
   }
@@ -1586,21 +1698,23 @@ __device__ void run_softmax(const DecodeParams& p, SharedState* sh, uint8_t* qs,
 
 // ---------------------------------------------------------------- the kernel
 // PG: paged cache.  SP: pages of 1, 2 or 4 rows (copied by the producer warp with cp.async).
-template <int KV, bool PG, bool SP>
+// QL: query tokens decoded together (2: the fused multi-token instances).
+template <int KV, bool PG, bool SP, int QL>
 __global__ void __launch_bounds__(Cfg<KV>::kThreads, 1) mla_split_kernel(const __grid_constant__ DecodeParams p) {
   using C = Cfg<KV>;
+  using G = Geo<KV, QL>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = base;
-  uint8_t* rope = ring + C::kRing * C::kSlotBytes;
+  uint8_t* rope = ring + G::kRing * C::kSlotBytes;
   uint8_t* qs = rope + rope_bytes<KV>();
-  uint8_t* ps = qs + C::kQBytes;
-  uint8_t* slabs = ps + 2 * kPBytes;                 // MXFP4 packed-row staging
+  uint8_t* ps = qs + G::kQBytes;
+  uint8_t* slabs = ps + 2 * G::kPBuf;                // MXFP4 packed-row staging
   SharedState* sh = reinterpret_cast<SharedState*>(slabs + raw_bytes<KV>());
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < C::kRing; ++i) {
+    for (int i = 0; i < G::kRing; ++i) {
       // MXFP4: one arrival per dequant warp; pages of 1-4 rows: one cp.async arrival per producer lane
       mbar_init(smem_u32(&sh->full[i]), KV == 2 ? C::kDeqWarps : (SP ? 32 : 1));
       mbar_init(smem_u32(&sh->empty[i]), 1);
@@ -1614,7 +1728,7 @@ __global__ void __launch_bounds__(Cfg<KV>::kThreads, 1) mla_split_kernel(const _
 
     }
     // softmax-side barriers count warps (one arrival per warp)
-    mbar_init(smem_u32(&sh->q_ready), 4);       // the first four softmax warps stage q
+    mbar_init(smem_u32(&sh->q_ready), 4 * QL);  // four softmax warps per query token stage q
     for (int i = 0; i < C::kRopeSlots; ++i) {
       mbar_init(smem_u32(&sh->rope_full[i]), KV == 2 ? C::kDeqWarps : (SP ? 32 : 1));   // MXFP4: per dequant warp
       mbar_init(smem_u32(&sh->rope_empty[i]), 1);                          // QK commit
@@ -1633,7 +1747,7 @@ __global__ void __launch_bounds__(Cfg<KV>::kThreads, 1) mla_split_kernel(const _
     fence_proxy_async_smem();
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(&sh->tmem_base), C::kTmemCols);
+    tmem_alloc(smem_u32(&sh->tmem_base), G::kTmemCols);
     tmem_relinquish();
   }
   // Programmatic dependent launch: the set-up above (barrier init, TMEM allocation) may run
@@ -1665,19 +1779,19 @@ __global__ void __launch_bounds__(Cfg<KV>::kThreads, 1) mla_split_kernel(const _
     if constexpr (KV == 2) regs_dec<C::kRegsIssue>();
     if (warp == 0) {
       if (PG || lane == 0) {   // paged: the whole warp (one lane per page)
-        if constexpr (SP) run_producer_sp<KV>(p, sh, ring, rope, slabs, lane);
+        if constexpr (SP) run_producer_sp<KV, QL>(p, sh, ring, rope, slabs, lane);
         else if constexpr (KV == 2) run_producer_mx<PG>(p, sh, slabs, lane);
-        else run_producer<KV, PG>(p, sh, ring, rope, lane);
+        else run_producer<KV, PG, QL>(p, sh, ring, rope, lane);
       }
     } else if (warp == 1) {
-      if (lane == 0) run_mma_qk<KV, PG, SP>(p, sh, make_descs(ring, rope, qs, ps), tmem);
+      if (lane == 0) run_mma_qk<KV, PG, SP, QL>(p, sh, make_descs<QL>(ring, rope, qs, ps), tmem);
     } else {
-      if (lane == 0) run_mma_pv<KV, PG, SP>(p, sh, make_descs(ring, rope, qs, ps), tmem, warp - 2);
+      if (lane == 0) run_mma_pv<KV, PG, SP, QL>(p, sh, make_descs<QL>(ring, rope, qs, ps), tmem, warp - 2);
     }
     __syncwarp();
   } else if (warp < 4 + C::kSoftWarps) {
     if constexpr (KV == 2) regs_inc<C::kRegsSoft>();
-    run_softmax<KV, PG>(p, sh, qs, ps, tmem);
+    run_softmax<KV, PG, QL>(p, sh, qs, ps, tmem);
   } else {
     if constexpr (KV == 2) {
       regs_dec<C::kRegsDeq>();
@@ -1688,7 +1802,7 @@ __global__ void __launch_bounds__(Cfg<KV>::kThreads, 1) mla_split_kernel(const _
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, C::kTmemCols);
+    tmem_dealloc(tmem, G::kTmemCols);
   }
 }
 
@@ -1697,18 +1811,18 @@ constexpr int kMaxDevices = 64;
 // Per-device, once: the kernel's dynamic shared-memory limit (a per-function attribute
 // that each device context keeps) and, for MXFP4, the register-split check.  Thread-safe;
 // the outcome of the first attempt on a device is kept.
-template <int KV, bool PG, bool SP>
+template <int KV, bool PG, bool SP, int QL>
 cudaError_t configure_once(int dev) {
   static std::once_flag once[kMaxDevices];
   static cudaError_t result[kMaxDevices];
   std::call_once(once[dev], [dev] {
-    cudaError_t e = cudaFuncSetAttribute(mla_split_kernel<KV, PG, SP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem_bytes<KV>()));
+    cudaError_t e = cudaFuncSetAttribute(mla_split_kernel<KV, PG, SP, QL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem_bytes<KV, QL>()));
     if (e == cudaSuccess && KV == 2) {
       // The register split's increases only complete if the CTA launched with at least the
       // registers the split hands out: refuse to launch otherwise.
       cudaFuncAttributes fa;
-      e = cudaFuncGetAttributes(&fa, mla_split_kernel<KV, PG, SP>);
+      e = cudaFuncGetAttributes(&fa, mla_split_kernel<KV, PG, SP, QL>);
       if (e == cudaSuccess && fa.numRegs * Cfg<KV>::kThreads < Cfg<2>::kRegsNeeded) e = cudaErrorInvalidConfiguration;
     }
     result[dev] = e;
@@ -1716,26 +1830,26 @@ cudaError_t configure_once(int dev) {
   return result[dev];
 }
 
-template <int KV, bool PG, bool SP>
+template <int KV, bool PG, bool SP, int QL = 1>
 cudaError_t launch_split_t(const DecodeParams& p, int grid, cudaStream_t stream) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  if ((e = configure_once<KV, PG, SP>(dev)) != cudaSuccess) return e;
+  if ((e = configure_once<KV, PG, SP, QL>(dev)) != cudaSuccess) return e;
   // Launched with programmatic stream serialisation: the kernel's set-up overlaps the tail
   // of the previous kernel in the stream (see grid_dep_wait in the kernel).
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
   cfg.blockDim = dim3(Cfg<KV>::kThreads);
-  cfg.dynamicSmemBytes = smem_bytes<KV>();
+  cfg.dynamicSmemBytes = smem_bytes<KV, QL>();
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, mla_split_kernel<KV, PG, SP>, p);
+  e = cudaLaunchKernelEx(&cfg, mla_split_kernel<KV, PG, SP, QL>, p);
   if (e != cudaSuccess) cudaGetLastError();
   return e;
 }
@@ -1750,6 +1864,12 @@ cudaError_t launch_split(int kv_dtype, const DecodeParams& p, int grid, cudaStre
 }
 
 cudaError_t launch_split_paged(int kv_dtype, const DecodeParams& p, int grid, cudaStream_t stream) {
+  if (p.pair_rows) {              // several query tokens per sequence, two decoded together
+    const bool sp = p.page_size < kMinPage;
+    if (kv_dtype == 0) return sp ? launch_split_t<0, true, true, 2>(p, grid, stream) : launch_split_t<0, true, false, 2>(p, grid, stream);
+    if (kv_dtype == 1) return sp ? launch_split_t<1, true, true, 2>(p, grid, stream) : launch_split_t<1, true, false, 2>(p, grid, stream);
+    return cudaErrorNotSupported;
+  }
   if (p.page_size < kMinPage) {   // pages of 1, 2 or 4 rows: cp.async producer
     if (kv_dtype == 0) return launch_split_t<0, true, true>(p, grid, stream);
     if (kv_dtype == 1) return launch_split_t<1, true, true>(p, grid, stream);
