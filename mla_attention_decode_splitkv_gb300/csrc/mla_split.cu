@@ -1479,65 +1479,71 @@ __device__ void run_softmax(const DecodeParams& p, SharedState* sh, uint8_t* qs,
         eadd = static_cast<float>(e - 127);
         rowf = pow2i(e - 127);
       }
-      float x[K];
+      // One pass per query token: its logits, the row maximum across the tile (warp max and
+      // the cross-warp exchange), the lazy rescale of its O columns, its P.  (QL = 2: the
+      // two passes keep half the per-column state live at a time.)
+      bool okt = okw;
 #pragma unroll
-      for (int k = 0; k < K; ++k) {
-        const int j = k / H, h = k % H;
-        float sdot;
-        if constexpr (KV == 0) sdot = __uint_as_float(rh[j][h]);
-        else sdot = fmaf(__uint_as_float(rl[j][h]), 0.0625f, __uint_as_float(rh[j][h])) * rowf;
-        float qk;
-        if constexpr (QL == 1) qk = qx[k];
-        else qk = (KV == 0) ? xscale : sh->qscale[cidx(k)] * xscale;
-        x[k] = vtok[j] ? fmaf(sdot, qk, eadd) : kNegInf;
-      }
-      float* red = &sh->red[g & 1][quarter][0];
+      for (int j = 0; j < QL; ++j) {
+        float x[H];
 #pragma unroll
-      for (int k = 0; k < K; ++k) {
-        const float m = warp_max(x[k]);
-        if (lane == 0) red[cidx(k)] = m;
-      }
-      ok = bar_and(1, NT, okw);
-      if (!ok) break;
-      float M[K];
-#pragma unroll
-      for (int k4 = 0; k4 < K; k4 += 4) {
-        const int c0 = cidx(k4);
-        const float4 a = *reinterpret_cast<const float4*>(&sh->red[g & 1][0][c0]);
-        const float4 b = *reinterpret_cast<const float4*>(&sh->red[g & 1][1][c0]);
-        const float4 c = *reinterpret_cast<const float4*>(&sh->red[g & 1][2][c0]);
-        const float4 d = *reinterpret_cast<const float4*>(&sh->red[g & 1][3][c0]);
-        M[k4 + 0] = fmaxf(fmaxf(a.x, b.x), fmaxf(c.x, d.x));
-        M[k4 + 1] = fmaxf(fmaxf(a.y, b.y), fmaxf(c.y, d.y));
-        M[k4 + 2] = fmaxf(fmaxf(a.z, b.z), fmaxf(c.z, d.z));
-        M[k4 + 3] = fmaxf(fmaxf(a.w, b.w), fmaxf(c.w, d.w));
-      }
-      bool need = false;
-      if (t == 0) {
-#pragma unroll
-        for (int k = 0; k < K; ++k) { mref[k] = M[k]; lpart[k] = 0.f; }
-      } else {
-#pragma unroll
-        for (int k = 0; k < K; ++k) need |= (M[k] > mref[k] + C::kTau);
-      }
-      if (need) {  // lazy rescale of this head group's O^T columns (uniform within the group)
-        float alpha[K];
-#pragma unroll
-        for (int k = 0; k < K; ++k) {
-          const float nm = fmaxf(mref[k], M[k]);
-          alpha[k] = ex2(mref[k] - nm);
-          mref[k] = nm;
-          lpart[k] *= alpha[k];
+        for (int h = 0; h < H; ++h) {
+          const int k = j * H + h;
+          float sdot;
+          if constexpr (KV == 0) sdot = __uint_as_float(rh[j][h]);
+          else sdot = fmaf(__uint_as_float(rl[j][h]), 0.0625f, __uint_as_float(rh[j][h])) * rowf;
+          float qk;
+          if constexpr (QL == 1) qk = qx[k];
+          else qk = (KV == 0) ? xscale : sh->qscale[cidx(k)] * xscale;
+          x[h] = vtok[j] ? fmaf(sdot, qk, eadd) : kNegInf;
         }
-        const uint32_t gp = g - 1;
-        bool ok2 = wait_bar(smem_u32(&sh->pv_done[gp & 1]), (gp >> 1) & 1, abortf, p.status, p.wait_limit_ns);
-        ok2 = __all_sync(0xffffffffu, ok2);
-        if (ok2) {
-          tc_fence_after();
-#pragma unroll 1
-          for (int m = 0; m < 4; ++m) {
+        float* red = &sh->red[g & 1][quarter][16 * j + h0];
 #pragma unroll
-            for (int j = 0; j < QL; ++j) {
+        for (int h = 0; h < H; ++h) {
+          const float m = warp_max(x[h]);
+          if (lane == 0) red[h] = m;
+        }
+        okt = bar_and(1, NT, okt);
+        if (!okt) break;
+        float M[H];
+#pragma unroll
+        for (int h4 = 0; h4 < H; h4 += 4) {
+          const int c0 = 16 * j + h0 + h4;
+          const float4 a = *reinterpret_cast<const float4*>(&sh->red[g & 1][0][c0]);
+          const float4 b = *reinterpret_cast<const float4*>(&sh->red[g & 1][1][c0]);
+          const float4 c = *reinterpret_cast<const float4*>(&sh->red[g & 1][2][c0]);
+          const float4 d = *reinterpret_cast<const float4*>(&sh->red[g & 1][3][c0]);
+          M[h4 + 0] = fmaxf(fmaxf(a.x, b.x), fmaxf(c.x, d.x));
+          M[h4 + 1] = fmaxf(fmaxf(a.y, b.y), fmaxf(c.y, d.y));
+          M[h4 + 2] = fmaxf(fmaxf(a.z, b.z), fmaxf(c.z, d.z));
+          M[h4 + 3] = fmaxf(fmaxf(a.w, b.w), fmaxf(c.w, d.w));
+        }
+        float* mr = &mref[j * H];
+        float* lp = &lpart[j * H];
+        bool need = false;
+        if (t == 0) {
+#pragma unroll
+          for (int h = 0; h < H; ++h) { mr[h] = M[h]; lp[h] = 0.f; }
+        } else {
+#pragma unroll
+          for (int h = 0; h < H; ++h) need |= (M[h] > mr[h] + C::kTau);
+        }
+        if (need) {  // lazy rescale of this head group's O^T columns of token j (uniform within the group)
+          float alpha[H];
+#pragma unroll
+          for (int h = 0; h < H; ++h) {
+            const float nm = fmaxf(mr[h], M[h]);
+            alpha[h] = ex2(mr[h] - nm);
+            mr[h] = nm;
+            lp[h] *= alpha[h];
+          }
+          const uint32_t gp = g - 1;
+          bool ok2 = wait_bar(smem_u32(&sh->pv_done[gp & 1]), (gp >> 1) & 1, abortf, p.status, p.wait_limit_ns);
+          ok2 = __all_sync(0xffffffffu, ok2);
+          if (ok2) {
+            tc_fence_after();
+#pragma unroll 1
+            for (int m = 0; m < 4; ++m) {
 #pragma unroll
               for (int part = 0; part < (KV == 0 ? 1 : 2); ++part) {
                 const uint32_t ta =
@@ -1546,34 +1552,31 @@ __device__ void run_softmax(const DecodeParams& p, SharedState* sh, uint8_t* qs,
                 tmem_ld<H>(ta, v);
                 tmem_wait_ld();
 #pragma unroll
-                for (int i = 0; i < H; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha[j * H + i]);
+                for (int i = 0; i < H; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha[i]);
                 tmem_st<H>(ta, v);
               }
             }
+            tmem_wait_st();
           }
-          tmem_wait_st();
+          okt = okt && ok2;  // a failed wait aborts at the next barrier
         }
-        okw = okw && ok2;  // a failed wait aborts at the next tile's barrier
-      }
-      // P = 2^(w - mref) <= 2^kTau (QL = 2: a column with no visible row yet has mref = -inf)
-      float P[K];
+        // P = 2^(w - mref) <= 2^kTau (QL = 2: a column with no visible row yet has mref = -inf)
+        float P[H];
 #pragma unroll
-      for (int k = 0; k < K; ++k) P[k] = ex2(x[k] - ((QL == 2 && mref[k] == kNegInf) ? 0.f : mref[k]));
-      if (g >= 2) wait_bar(smem_u32(&sh->pv_done[g & 1]), ((g >> 1) & 1) ^ 1, abortf, p.status, p.wait_limit_ns);
-      // P^T row of this token: 32 QL bytes (per query token: 16 heads of hi then of lo e4m3,
-      // or 16 bf16); swizzled in 16-byte chunks, 32-byte (QL = 1) or 64-byte (QL = 2) pattern.
-      uint8_t* prow = ps + (g & 1) * G::kPBuf + row * 32 * QL;
-      const int sw = QL == 1 ? (row >> 2) & 1 : (row >> 1) & 3;
-      if constexpr (KV == 0) {
-#pragma unroll
-        for (int j = 0; j < QL; ++j) {
+        for (int h = 0; h < H; ++h) P[h] = ex2(x[h] - ((QL == 2 && mr[h] == kNegInf) ? 0.f : mr[h]));
+        if (j == 0 && g >= 2)
+          wait_bar(smem_u32(&sh->pv_done[g & 1]), ((g >> 1) & 1) ^ 1, abortf, p.status, p.wait_limit_ns);
+        // P^T row of this token: 32 QL bytes (per query token: 16 heads of hi then of lo e4m3,
+        // or 16 bf16); swizzled in 16-byte chunks, 32-byte (QL = 1) or 64-byte (QL = 2) pattern.
+        uint8_t* prow = ps + (g & 1) * G::kPBuf + row * 32 * QL;
+        const int sw = QL == 1 ? (row >> 2) & 1 : (row >> 1) & 3;
+        if constexpr (KV == 0) {
           uint32_t wv[H / 2];
 #pragma unroll
           for (int i = 0; i < H / 2; ++i) {
-            const int k = j * H + 2 * i;
-            const uint16_t b0 = f_to_bf16_bits(P[k]), b1 = f_to_bf16_bits(P[k + 1]);
-            lpart[k] += bf16_bits_to_f(b0);
-            lpart[k + 1] += bf16_bits_to_f(b1);
+            const uint16_t b0 = f_to_bf16_bits(P[2 * i]), b1 = f_to_bf16_bits(P[2 * i + 1]);
+            lp[2 * i] += bf16_bits_to_f(b0);
+            lp[2 * i + 1] += bf16_bits_to_f(b1);
             wv[i] = static_cast<uint32_t>(b0) | (static_cast<uint32_t>(b1) << 16);
           }
           // heads [h0, h0 + H) of token j are 16-byte chunk(s) 2 j + h0/8 .. of the row
@@ -1581,36 +1584,33 @@ __device__ void run_softmax(const DecodeParams& p, SharedState* sh, uint8_t* qs,
           for (int c = 0; c < H / 8; ++c)
             *reinterpret_cast<uint4*>(prow + (((2 * j + h0 / 8 + c) ^ sw) << 4)) =
                 make_uint4(wv[4 * c], wv[4 * c + 1], wv[4 * c + 2], wv[4 * c + 3]);
-        }
-      } else {
-        // Softmax sum: fp8 caches add the e4m3-rounded P (the values the PV MMAs weight V
-        // with).  MXFP4 rows add the fp32 P * 2^-eadd: a row of small magnitude (eadd << 0)
-        // can carry a large softmax weight with a PV weight too small for e4m3.
-        const float einv = pow2i(-static_cast<int>(eadd) - 4);   // 2^-eadd / 16
-        const float escale = pow2i(-static_cast<int>(eadd));      // 2^-eadd
-#pragma unroll
-        for (int j = 0; j < QL; ++j) {
+        } else {
+          // Softmax sum: fp8 caches add the e4m3-rounded P (the values the PV MMAs weight V
+          // with).  MXFP4 rows add the fp32 P * 2^-eadd: a row of small magnitude (eadd << 0)
+          // can carry a large softmax weight with a PV weight too small for e4m3.
+          const float einv = pow2i(-static_cast<int>(eadd) - 4);   // 2^-eadd / 16
+          const float escale = pow2i(-static_cast<int>(eadd));      // 2^-eadd
           uint32_t hw[H / 4], lw[H / 4];
 #pragma unroll
           for (int i = 0; i < H / 4; ++i) {
             uint32_t a = 0, b = 0;
 #pragma unroll
             for (int kk = 0; kk < 4; kk += 2) {
-              const int k = j * H + 4 * i + kk;
-              const float y0 = P[k] * 16.f, y1 = P[k + 1] * 16.f;
+              const int h = 4 * i + kk;
+              const float y0 = P[h] * 16.f, y1 = P[h + 1] * 16.f;
               const uint32_t hp = pack_e4m3x2(y0, y1);
               const float2 hd = unpack_e4m3x2(hp);
-              const uint32_t lp = pack_e4m3x2((y0 - hd.x) * 16.f, (y1 - hd.y) * 16.f);
+              const uint32_t lpk = pack_e4m3x2((y0 - hd.x) * 16.f, (y1 - hd.y) * 16.f);
               if constexpr (KV == 2) {
-                lpart[k] = fmaf(P[k], escale, lpart[k]);
-                lpart[k + 1] = fmaf(P[k + 1], escale, lpart[k + 1]);
+                lp[h] = fmaf(P[h], escale, lp[h]);
+                lp[h + 1] = fmaf(P[h + 1], escale, lp[h + 1]);
               } else {
-                const float2 ld = unpack_e4m3x2(lp);
-                lpart[k] += fmaf(ld.x, 0.0625f, hd.x) * einv;
-                lpart[k + 1] += fmaf(ld.y, 0.0625f, hd.y) * einv;
+                const float2 ld = unpack_e4m3x2(lpk);
+                lp[h] += fmaf(ld.x, 0.0625f, hd.x) * einv;
+                lp[h + 1] += fmaf(ld.y, 0.0625f, hd.y) * einv;
               }
               a |= hp << (8 * kk);
-              b |= lp << (8 * kk);
+              b |= lpk << (8 * kk);
             }
             hw[i] = a;
             lw[i] = b;
@@ -1624,6 +1624,8 @@ __device__ void run_softmax(const DecodeParams& p, SharedState* sh, uint8_t* qs,
           }
         }
       }
+      ok = okt;
+      if (!ok) break;
       fence_proxy_async_smem();
       tc_fence_before();
       warp_arrive(smem_u32(&sh->p_full[g & 1]));
