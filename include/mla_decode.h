@@ -72,9 +72,14 @@ typedef enum {
  *  num_splits >= 1: cut every sequence into that many splits (BN = 128-token-rounded
  *             chunks, submission 727205 `mla_s1` split rule; splits past the end are
  *             empty; num_splits = 1 writes out directly with no merge).
- *             <= 0: the library balances the total token count of the batch evenly over
- *             the GPU's SMs (one persistent CTA per SM, contiguous token ranges that may
- *             span several sequences) and merges the pieces of each sequence.
+ *             <= 0: the library balances the batch over the GPU's SMs (one persistent CTA
+ *             per SM, contiguous token ranges that may span several sequences) and merges
+ *             the pieces of each sequence.  The ranges split the batch's cost evenly: its
+ *             tokens plus, for every sequence start after the first, the rows a CTA gets
+ *             through in the time it loses moving to the next sequence (the split model's
+ *             x of mla_decode_pick_splits: 521 fp8 rows, 260 bf16 rows; for MXFP4, whose
+ *             CTAs run at 0.275 of the HBM rate, 270 rows), so that a CTA that crosses
+ *             sequence boundaries is given fewer tokens.
  *             At most 4096 splits.  mla_decode_pick_splits returns a good value.
  *  kv_dtype   an mla_kv_dtype value.
  *  stream     cudaStream_t or NULL.
@@ -118,8 +123,9 @@ int mla_decode(const void* q, const void* kv, const void* kv_scale, const int32_
  *  num_splits       as mla_decode.  In the balanced mode (<= 0) the token positions are
  *                   those of the page space (sequence b starts at kv_page_indptr[b] *
  *                   page_size; the unused rows of its last page belong to no CTA's work)
- *                   and the CTAs' cut points are rounded down to multiples of 128, so that
- *                   every 128-token tile starts on a page boundary.
+ *                   and the CTAs' cut points, which split the token count evenly (no
+ *                   crossing cost), are rounded down to multiples of 128, so that every
+ *                   128-token tile starts on a page boundary.
  * Every page number times page_size plus page_size must be a row inside kv, and every
  * index read must lie inside kv_page_indices; violations are undefined behaviour, as with
  * kv_indptr.  Errors: as mla_decode, plus MLA_ERR_INVALID_ARG for a page_size that is not
@@ -215,6 +221,12 @@ void mla_decode_set_wait_limit_ns(unsigned long long ns);
  * limit, the device status reads MLA_ERR_TIMEOUT and the kernel returns.  Never set outside
  * tests; mla_decode_noalloc ignores it. */
 void mla_decode_set_test_stall(int on);
+
+/* Test hook: the crossing cost, in cache rows, that the balanced mode of mla_decode and
+ * mla_decode_noalloc charges per sequence start when it cuts the batch (rows >= 0; a large
+ * value leaves CTAs whose range lies inside one crossing, with no work).  rows < 0 restores
+ * the default, x of the split model (mla_decode_pick_splits) for the call's cache dtype. */
+void mla_decode_set_cross_rows(int rows);
 
 /* Timing hooks.  Between begin and end, every mla_decode call records CUDA events on its
  * stream around its split kernel and around the whole call.  end() waits for those events

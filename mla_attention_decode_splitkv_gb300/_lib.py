@@ -28,6 +28,7 @@ EXPORTED = (
     "mla_decode_device_status",
     "mla_decode_set_wait_limit_ns",
     "mla_decode_set_test_stall",
+    "mla_decode_set_cross_rows",
     "mla_decode_profile_begin",
     "mla_decode_profile_end",
     "mla_decode_noalloc",
@@ -78,6 +79,8 @@ def load(path: str = LIB_PATH):
         lib.mla_decode_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
         lib.mla_decode_set_test_stall.restype = None
         lib.mla_decode_set_test_stall.argtypes = [c_int]
+        lib.mla_decode_set_cross_rows.restype = None
+        lib.mla_decode_set_cross_rows.argtypes = [c_int]
         lib.mla_decode_profile_begin.restype = c_int
         lib.mla_decode_profile_begin.argtypes = []
         lib.mla_decode_profile_end.restype = c_int
@@ -220,6 +223,11 @@ def set_wait_limit_ns(ns: int) -> None:
 def set_test_stall(on: bool) -> None:
     """Test hook: make every mla_decode call's pipeline wait run past its limit."""
     load().mla_decode_set_test_stall(1 if on else 0)
+
+
+def set_cross_rows(rows: int) -> None:
+    """Test hook: the balanced mode's crossing cost in cache rows (< 0: the default)."""
+    load().mla_decode_set_cross_rows(int(rows))
 
 
 def profile_begin() -> None:

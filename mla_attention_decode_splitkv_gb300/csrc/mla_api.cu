@@ -33,6 +33,17 @@ std::atomic<int> g_sm_count[kMaxDevices];
 std::atomic<int> g_cc[kMaxDevices];
 std::atomic<unsigned long long> g_wait_limit_ns{2000000000ull};
 std::atomic<int> g_test_stall{0};
+std::atomic<int> g_cross_rows{-1};
+
+// Costs of the split model, in bytes (mla_decode_pick_splits; the header derives them).
+constexpr double kPieceBytes = static_cast<double>(mla::kHeads) * (mla::kDimV + 1) * 4.0;  // 32,832
+constexpr double kWaveBytes = 222e3;
+constexpr double kCrossBytes = 300e3;
+double row_bytes(int kv_dtype) {
+  return kv_dtype == MLA_KV_BF16 ? 2.0 * mla::kDim
+         : kv_dtype == MLA_KV_FP8_E4M3 ? 1.0 * mla::kDim
+         : static_cast<double>(mla::kMxPacked + mla::kMxScales);
+}
 thread_local const char* t_last_cuda_error = "";
 
 // Optional timing of each call's split kernel (events recorded on the call's stream).
@@ -155,6 +166,16 @@ static int encode_map(CUtensorMap* map, const void* kv, int kv_dtype, bool rope,
 
 unsigned long long pipeline_wait_limit_ns() { return g_wait_limit_ns.load(); }
 
+// The crossing's time (kCrossBytes is that time times one SM's HBM share) in the rows a CTA
+// gets through in that time: bf16 and fp8 CTAs stream at the HBM rate; an MXFP4 CTA is
+// bound by its dequantisation at 0.275 of it (1.86 of the 6.76 TB/s measured on GB300).
+int balance_cross_rows(int kv_dtype) {
+  const int r = g_cross_rows.load();
+  if (r >= 0) return r;
+  const double rate = kv_dtype == MLA_KV_MXFP4 ? 0.275 : 1.0;
+  return static_cast<int>(kCrossBytes / row_bytes(kv_dtype) * rate + 0.5);
+}
+
 int encode_kv_map(CUtensorMap* map, const void* kv, int kv_dtype) { return encode_map(map, kv, kv_dtype, false); }
 int encode_rope_map(CUtensorMap* map, const void* kv) { return encode_map(map, kv, MLA_KV_FP8_E4M3, true); }
 int encode_kv_map_rows(CUtensorMap* map, const void* kv, int kv_dtype, int box_rows) {
@@ -186,6 +207,8 @@ void mla_decode_set_wait_limit_ns(unsigned long long ns) { g_wait_limit_ns.store
 
 void mla_decode_set_test_stall(int on) { g_test_stall = on ? 1 : 0; }
 
+void mla_decode_set_cross_rows(int rows) { g_cross_rows = rows < 0 ? -1 : rows; }
+
 int mla_decode_pick_splits(int batch, int kv_len_hint, int num_sms, int kv_dtype) {
   if (batch <= 0 || kv_len_hint < 0 || num_sms <= 0 || kv_dtype < 0 || kv_dtype > 2) return MLA_ERR_INVALID_ARG;
   // The split model of amd-mixed-mla submission 700955 (`_compute_custom_splits`: score =
@@ -206,12 +229,7 @@ int mla_decode_pick_splits(int batch, int kv_len_hint, int num_sms, int kv_dtype
   //                sequences touched by a CTA, p = ceil(L / R) + 1 pieces per sequence.
   // The best uniform split count is returned, or 0 when the balanced mode is faster.
   // kv_dtype sets the row size, hence c, w and x in rows.
-  static constexpr double kPieceBytes = static_cast<double>(mla::kHeads) * (mla::kDimV + 1) * 4.0;  // 32,832
-  static constexpr double kWaveBytes = 222e3;
-  static constexpr double kCrossBytes = 300e3;
-  const double row = kv_dtype == MLA_KV_BF16 ? 2.0 * mla::kDim
-                     : kv_dtype == MLA_KV_FP8_E4M3 ? 1.0 * mla::kDim
-                     : static_cast<double>(mla::kMxPacked + mla::kMxScales);
+  const double row = row_bytes(kv_dtype);
   const double c = kPieceBytes / row, w = kWaveBytes / row, x = kCrossBytes / row;
   const long long L = std::max(kv_len_hint, 1), B = batch, S = num_sms, BN = mla::kBN;
   const long long ns_max = std::min<long long>(mla::kMaxSplits, (L + BN - 1) / BN);
@@ -346,6 +364,7 @@ static int decode_impl(const void* q, const void* kv, const void* kv_scale, cons
   p.logit_scale_log2 = static_cast<float>((1.0 / std::sqrt(static_cast<double>(mla::kDim))) * 1.4426950408889634);
   p.wait_limit_ns = g_wait_limit_ns.load();
   p.test_stall = g_test_stall.load();
+  p.cross_rows = mla::balance_cross_rows(kv_dtype);
 
   ProfRecord rec{nullptr, nullptr, nullptr};
   bool prof = false;

@@ -48,6 +48,9 @@ struct DecodeParams {
   const int32_t* qo_indptr;
   int num_seqs;
   int pair_rows;                   // fused multi-token instances: a CTA decodes query rows t, t + 1 together
+  // Balanced mode, contiguous cache: the cost in rows of each sequence start after the first
+  // (see balanced_cost_total in the kernel; 0 cuts by rows alone).
+  int cross_rows;
 };
 
 
@@ -63,6 +66,10 @@ int encode_rope_map(CUtensorMap* map, const void* kv);
 
 // The pipeline wait limit set by mla_decode_set_wait_limit_ns (default 2 s).
 unsigned long long pipeline_wait_limit_ns();
+
+// DecodeParams::cross_rows for a cache dtype: the split model's crossing cost in rows of that
+// cache (or the value set by mla_decode_set_cross_rows).
+int balance_cross_rows(int kv_dtype);
 
 // Launches the split kernel for kv_dtype (geometry per dtype is internal to mla_split.cu).
 cudaError_t launch_split(int kv_dtype, const DecodeParams& p, int grid, cudaStream_t stream);

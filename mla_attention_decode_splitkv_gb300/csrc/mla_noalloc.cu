@@ -127,6 +127,7 @@ extern "C" int mla_decode_noalloc(const void* q, const void* kv, const void* kv_
   p.qo_indptr = nullptr;
   p.num_seqs = 0;
   p.pair_rows = 0;
+  p.cross_rows = mla::balance_cross_rows(kv_dtype);
   if (mla::launch_split(kv_dtype, p, static_cast<int>(grid), st) != cudaSuccess) { cudaGetLastError(); return MLA_ERR_CUDA; }
   return MLA_OK;
 }

@@ -155,6 +155,7 @@ struct SharedState {
   int sp_rows[128];                // pages of 1-4 rows: the cache row of each window row of a tile
   uint2 lut[kLutCount];            // 8 e4m3 bytes per block shift
   long long seg_total;              // kv_indptr[batch] (balanced mode)
+  long long seg_lo, seg_hi;        // this CTA's position range (balanced mode)
   int seg_b0;                      // first sequence of this CTA (balanced mode)
   int merge_slot0;                 // fused merge: first slot and piece count to merge
   int merge_pieces;
@@ -266,6 +267,51 @@ __device__ int warp_first_seq(const int32_t* ip, int batch, long long lo) {
   return m ? base + __ffs(m) - 1 : base + count;
 }
 
+// Contiguous cache, balanced mode: the CTAs share the batch's cost, not its rows.  Every
+// sequence start after the first costs X rows more (X = cross_rows: the time a CTA loses
+// when it moves from one sequence to the next, as the split model states it), so position
+// r of sequence b sits at cost r + X b and the batch costs Tc = total + X (batch - 1).  CTA
+// c owns costs [c Tc / Ge, (c + 1) Tc / Ge); a cost inside sequence b maps back to the
+// position cost - X b, a cost in the X-gap before sequence b + 1 to that sequence's first
+// position.  The map is monotone, so ranges stay contiguous and ordered; a range that lies
+// inside one gap is empty (its CTA has no work).
+__device__ __forceinline__ long long balanced_cost_total(long long total, int batch, long long X) {
+  return total + X * (batch - 1);
+}
+// Largest CTA c < Ge with c Tc / Ge <= cost (the CTA that owns a position of that cost).
+__device__ __forceinline__ int cta_of_cost(long long cost, long long Tc, int Ge) {
+  const long long c = ((cost + 1) * Ge - 1) / Tc;
+  return static_cast<int>(c < Ge - 1 ? c : Ge - 1);
+}
+// For two costs at once: the first b in [0, batch) with kv_indptr[b + 1] + X (b + 1) > C,
+// i.e. the sequence whose cost range (with the gap after it) holds C (batch if none).
+// Called by a full warp; each round probes 32 evenly spaced entries per cost, and the two
+// searches' loads are issued together.
+__device__ void warp_first_seq_cost2(const int32_t* ip, int batch, long long X, long long C0, long long C1,
+                                     int* out0, int* out1) {
+  const int lane = threadIdx.x & 31;
+  const long long C[2] = {C0, C1};
+  int base[2] = {0, 0}, count[2] = {batch, batch}, res[2] = {batch, batch};
+  bool fin[2] = {false, false};
+  while (!(fin[0] && fin[1])) {
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      if (fin[k]) continue;
+      const int step = count[k] > 32 ? (count[k] + 31) / 32 : 1;
+      const int bi = base[k] + min(count[k] - 1, lane * step + step - 1);
+      const bool f = lane * step < count[k] && static_cast<long long>(ip[bi + 1]) + X * (bi + 1) > C[k];
+      const unsigned m = __ballot_sync(0xffffffffu, f);
+      if (m == 0) { res[k] = base[k] + count[k]; fin[k] = true; continue; }
+      const int c = __ffs(m) - 1;
+      if (step == 1) { res[k] = base[k] + c; fin[k] = true; continue; }
+      base[k] += c * step;
+      count[k] = min(step, count[k] - c * step);
+    }
+  }
+  *out0 = res[0];
+  *out1 = res[1];
+}
+
 // Enumerates the (sequence, token range) segments one CTA works on.
 //  uniform (num_splits >= 1): CTA = b * ns + s, one segment (possibly empty), chunk rule
 //     chunk = ceil(ceil(L/ns)/BN)*BN (amd-mixed-mla submission 727205, `mla_s1`).
@@ -278,9 +324,9 @@ struct SegIter {
   int b, split, ns, cta;
   bool uniform, done, last_cta;
 
-  // total / b0: kv_indptr[batch] and the CTA's first sequence (balanced mode), found once
-  // per CTA by warp_first_seq at kernel start.
-  __device__ void init(const DecodeParams& p, int c, long long total, int b0) {
+  // Balanced mode: the CTA's position range and first sequence, found once per CTA at
+  // kernel start (balanced_range) and read from shared memory by every role.
+  __device__ void init(const DecodeParams& p, int c, const SharedState* sh) {
     cta = c;
     done = false;
     if (p.num_splits >= 1) {
@@ -291,12 +337,12 @@ struct SegIter {
       return;
     }
     uniform = false;
-    int Ge = balanced_ctas(total, p.num_ctas);
+    int Ge = balanced_ctas(sh->seg_total, p.num_ctas);
     if (c >= Ge) { done = true; return; }
-    lo = cta_lo<PG>(c, total, Ge);
-    hi = cta_lo<PG>(c + 1, total, Ge);
+    lo = sh->seg_lo;
+    hi = sh->seg_hi;
     last_cta = (c == Ge - 1);
-    b = b0;
+    b = sh->seg_b0;
   }
 
   __device__ bool next(const DecodeParams& p, Seg& s) {
@@ -579,7 +625,7 @@ template <bool PG>
 __device__ void run_producer_mx(const DecodeParams& p, SharedState* sh, uint8_t* slabs, int lane) {
   volatile int* abortf = &sh->abort;
   SegIter<PG> it;
-  it.init(p, blockIdx.x, sh->seg_total, sh->seg_b0);
+  it.init(p, blockIdx.x, sh);
   Seg s;
   uint32_t idx = 0, slot = 0, phase = 0;
   bool ok = true;
@@ -618,7 +664,7 @@ __device__ void run_producer(const DecodeParams& p, SharedState* sh, uint8_t* ri
   constexpr int kRing = Geo<KV, QL>::kRing;
   volatile int* abortf = &sh->abort;
   SegIter<PG> it;
-  it.init(p, blockIdx.x, sh->seg_total, sh->seg_b0);
+  it.init(p, blockIdx.x, sh);
   Seg s;
   uint32_t idx = 0, slot = 0, phase = 0, ridx = 0;
   bool ok = true;
@@ -713,7 +759,7 @@ __device__ void run_producer_sp(const DecodeParams& p, SharedState* sh, uint8_t*
   volatile int* abortf = &sh->abort;
   const int rb = KV == 0 ? 2 * kDim : (KV == 1 ? kDim : kMxPacked);   // bytes per cache row
   SegIter<true> it;
-  it.init(p, blockIdx.x, sh->seg_total, sh->seg_b0);
+  it.init(p, blockIdx.x, sh);
   Seg s;
   uint32_t idx = 0, slot = 0, phase = 0, ridx = 0;
   constexpr int kSlots = KV == 2 ? kSlabs : Geo<KV, QL>::kRing;
@@ -851,7 +897,7 @@ __device__ void run_dequant(const DecodeParams& p, SharedState* sh, uint8_t* rin
   bar_sync(2, C::kDeqWarps * 32);
   const int ssw = (di >> 1) & 3;           // SW64 piece swizzle of this row in a slab
   SegIter<PG> it;
-  it.init(p, blockIdx.x, sh->seg_total, sh->seg_b0);
+  it.init(p, blockIdx.x, sh);
   Seg s;
   uint32_t g = 0, slab_i = 0, slab_ph = 0;
   bool ok = true;
@@ -1031,7 +1077,7 @@ __device__ void run_mma_qk(const DecodeParams& p, SharedState* sh, const Descs& 
   constexpr uint32_t idq = instr_desc(KV == 0 ? 1u : 0u, 0, 0, 128, G::kN);  // bf16 | e4m3, K-major A and B
   volatile int* abortf = &sh->abort;
   SegIter<PG> it;
-  it.init(p, blockIdx.x, sh->seg_total, sh->seg_b0);
+  it.init(p, blockIdx.x, sh);
   Seg s;
   uint32_t g = 0, slot = 0, phase = 0;
   int kseg = 0;
@@ -1091,7 +1137,7 @@ __device__ void run_mma_pv(const DecodeParams& p, SharedState* sh, const Descs& 
   constexpr uint32_t idp = instr_desc(KV == 0 ? 1u : 0u, 1, 1, 128, G::kN);  // MN-major A (V^T) and B (P^T)
   volatile int* abortf = &sh->abort;
   SegIter<PG> it;
-  it.init(p, blockIdx.x, sh->seg_total, sh->seg_b0);
+  it.init(p, blockIdx.x, sh);
   Seg s;
   uint32_t g = 0, slot0 = 0;                      // ring slot of chunk 0 of tile g
   int kseg = 0;
@@ -1146,12 +1192,17 @@ __device__ __forceinline__ int seq_pieces(const DecodeParams& p, int b, long lon
   }
   const int Ge = balanced_ctas(total, p.num_ctas);
   long long r0 = p.kv_indptr[b], r1 = p.kv_indptr[b + 1];   // a merged sequence is non-empty
+  int cf, cl;
   if constexpr (PG) {
     r1 = r0 * p.page_size + (r1 - r0 - 1) * p.page_size + p.last_page_len[b];
     r0 *= p.page_size;
+    cf = cta_of_token<PG>(r0, total, Ge);
+    cl = cta_of_token<PG>(r1 - 1, total, Ge);
+  } else {
+    const long long X = p.cross_rows, Tc = balanced_cost_total(total, p.batch, X);
+    cf = cta_of_cost(r0 + X * b, Tc, Ge);
+    cl = cta_of_cost(r1 - 1 + X * b, Tc, Ge);
   }
-  const int cf = cta_of_token<PG>(r0, total, Ge);
-  const int cl = cta_of_token<PG>(r1 - 1, total, Ge);
   *slot0 = b + cf;
   return cl - cf + 1;
 }
@@ -1394,7 +1445,7 @@ __device__ void run_softmax(const DecodeParams& p, SharedState* sh, uint8_t* qs,
   auto cidx = [&](int k) { return 16 * (k / H) + h0 + (k % H); };
 
   SegIter<PG> it;
-  it.init(p, blockIdx.x, sh->seg_total, sh->seg_b0);
+  it.init(p, blockIdx.x, sh);
   Seg cur, nxt;
   bool has_cur = it.next(p, cur);
   // Stage q of the first non-empty segment (the iterator may first yield empty ones).
@@ -1759,16 +1810,31 @@ __global__ void __launch_bounds__(Cfg<KV>::kThreads, 1) mla_split_kernel(const _
   grid_dep_launch_dependents();
   grid_dep_wait();
   if (warp == 0 && p.num_splits < 1) {
+    // Balanced mode: this CTA's position range [lo, hi) and its first sequence b0, the first
+    // b with kv_indptr[b+1] >= lo (paged: kv_indptr[b+1] * P >= lo): empty sequences sitting
+    // at lo are this CTA's too.
     const long long total = static_cast<long long>(p.kv_indptr[p.batch]) * (PG ? p.page_size : 1);
     const int Ge = balanced_ctas(total, p.num_ctas);
+    const int c = static_cast<int>(blockIdx.x);
     int b0 = p.batch;
-    // first b with kv_indptr[b+1] >= lo (paged: kv_indptr[b+1] * P >= lo): empty sequences
-    // sitting at lo are this CTA's too
-    if (static_cast<int>(blockIdx.x) < Ge) {
-      const long long lo = cta_lo<PG>(blockIdx.x, total, Ge);
-      b0 = warp_first_seq(p.kv_indptr, p.batch, PG ? (lo + p.page_size - 1) / p.page_size - 1 : lo - 1);
+    long long lo = total, hi = total;
+    if (c < Ge) {
+      if constexpr (PG) {   // row cuts rounded to whole tiles (cta_lo)
+        lo = cta_lo<PG>(c, total, Ge);
+        hi = cta_lo<PG>(c + 1, total, Ge);
+        b0 = warp_first_seq(p.kv_indptr, p.batch, (lo + p.page_size - 1) / p.page_size - 1);
+      } else {              // cost cuts (balanced_cost_total)
+        const long long X = p.cross_rows, Tc = balanced_cost_total(total, p.batch, X);
+        const long long clo = static_cast<long long>(c) * Tc / Ge, chi = static_cast<long long>(c + 1) * Tc / Ge;
+        int blo, bhi;
+        warp_first_seq_cost2(p.kv_indptr, p.batch, X, clo, chi, &blo, &bhi);
+        if (blo < p.batch) lo = min(clo - X * blo, static_cast<long long>(p.kv_indptr[blo + 1]));
+        if (c + 1 < Ge && bhi < p.batch) hi = min(chi - X * bhi, static_cast<long long>(p.kv_indptr[bhi + 1]));
+        b0 = blo;
+        while (b0 > 0 && p.kv_indptr[b0] >= lo) --b0;
+      }
     }
-    if (lane == 0) { sh->seg_total = total; sh->seg_b0 = b0; }
+    if (lane == 0) { sh->seg_total = total; sh->seg_b0 = b0; sh->seg_lo = lo; sh->seg_hi = hi; }
   }
   tc_fence_before();
   __syncthreads();

@@ -273,6 +273,31 @@ def test_empty_sequences_anywhere_in_balanced_mode(pkg, kv_dtype, lens):
     _check(out, ref, f"empty-anywhere {lens}")
 
 
+@pytest.mark.parametrize("kv_dtype", DTYPES)
+@pytest.mark.parametrize("cross_rows", [0, 37, 5000, 10 ** 7])
+def test_balanced_cost_cuts_any_crossing_cost(pkg, kv_dtype, cross_rows):
+    # The balanced mode cuts the batch by tokens plus a crossing cost per sequence start.
+    # Any cost gives a valid partition: 0 cuts by tokens alone, 37 and 5000 move the cuts
+    # around short and empty sequences, 10^7 leaves most CTAs with a range inside one
+    # crossing (no work) and a few CTAs with many sequences each.
+    lens = [0, 1, 700, 0, 0, 2, 130, 4000, 1, 0, 257, 3000, 5, 128, 129, 0, 2500, 64, 1, 1000]
+    inp = synth.make_inputs(len(lens), lens, kv_dtype, seed=83 + cross_rows % 97)
+    ref, _ = oracle.decode(inp.q, inp.kv, inp.kv_scale, inp.kv_indptr, kv_dtype)
+    g = inp.to("cuda")
+    out = torch.full((len(lens), 16, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+    try:
+        pkg._lib.set_cross_rows(cross_rows)
+        pkg.decode(g.q, g.kv, g.kv_scale, g.kv_indptr, kv_dtype, num_splits=0, out=out)
+        torch.cuda.synchronize()
+    finally:
+        pkg._lib.set_cross_rows(-1)
+    assert pkg.device_status(clear=True) == pkg.MLA_OK
+    _check(out, ref, f"cross_rows {cross_rows}")
+    for b, n in enumerate(lens):
+        if n == 0:
+            assert torch.count_nonzero(out[b]) == 0
+
+
 @pytest.mark.parametrize("ns", [0, 5])
 def test_repeated_calls_give_identical_results(pkg, ns):
     # The merge step re-arms its per-sequence counters at the end of every call.
