@@ -870,12 +870,12 @@ __device__ __forceinline__ void deq_block(const uint4 v, const uint2 lut, uint4&
   e2m1x8_to_e4m3x8(v.w, lut, hi.z, hi.w);
 }
 
-// Tile g, chunk c: the packed bytes come from slab 5g + c of the slab ring (freed right
-// after they are read); value chunk c (128 dims) goes to ring slot 4 * (g & 1) + c (the
-// ring holds the value chunks of exactly two tiles, so dequantising tile g + 2 only waits
-// for the PV MMAs of tile g); the rope chunk goes to its own SW64 buffer.  Each chunk is
-// published (full barrier) as soon as it is written.  Window rows before cached row 0
-// hold zeros (TMA fill) and get no scale: they decode to zeros.
+// Tile g, chunk c: the packed bytes come from slab 5g + c of the slab ring; value chunk c
+// (128 dims) goes to ring slot 4 * (g & 1) + c (the ring holds the value chunks of exactly
+// two tiles, so dequantising tile g + 2 only waits for the PV MMAs of tile g); the rope
+// chunk goes to its own SW64 buffer and is published (and its slab freed) as soon as it is
+// done; the four value chunks are published, and their slabs freed, together.  Window rows
+// before cached row 0 hold zeros (TMA fill) and get no scale: they decode to zeros.
 template <bool PG>
 __device__ void run_dequant(const DecodeParams& p, SharedState* sh, uint8_t* ring, uint8_t* rope, uint8_t* slabs) {
   using C = Cfg<2>;
@@ -1005,6 +1005,12 @@ __device__ void run_dequant(const DecodeParams& p, SharedState* sh, uint8_t* rin
         if (!ok) break;
       }
       const uint32_t vslot0 = (g & 1) * C::kRingPT;
+      // The four value chunks are converted back to back and handed over together: one proxy
+      // fence orders this thread's generic reads of the four slabs (before their next
+      // async-proxy fills) and its carrier stores (before the MMAs read them), then the four
+      // slabs go back to the producer and the four chunks are published.  The QK MMAs of a
+      // tile wait for its last chunk in any case.
+      const uint32_t si0 = slab_i;
 #pragma unroll 1
       for (int c = 0; c < C::kRingPT; ++c) {
         const uint32_t si = slab_i, sph = slab_ph;
@@ -1019,8 +1025,6 @@ __device__ void run_dequant(const DecodeParams& p, SharedState* sh, uint8_t* rin
         uint4 v[kB];
 #pragma unroll
         for (int q = 0; q < kB; ++q) v[q] = ld_shared_v4_volatile(srow + (((b0 + q) ^ ssw) << 4));
-        fence_proxy_async_smem();   // generic reads before the slab's next async-proxy fill (above)
-        warp_arrive(smem_u32(&sh->slab_empty[si]));
         uint8_t* dst = ring + (vslot0 + c) * C::kSlotBytes + di * 128;       // [128 x 128 B] SW128
         const uint32_t kc = static_cast<uint32_t>(kv64 >> (16 * c + 4 * b0)); // blocks 4c + b0 ..
 #pragma unroll
@@ -1031,10 +1035,15 @@ __device__ void run_dequant(const DecodeParams& p, SharedState* sh, uint8_t* rin
           *reinterpret_cast<uint4*>(dst + (((2 * bk) ^ (di & 7)) << 4)) = lo;
           *reinterpret_cast<uint4*>(dst + (((2 * bk + 1) ^ (di & 7)) << 4)) = hi;
         }
-        fence_proxy_async_smem();
-        warp_arrive(smem_u32(&sh->full[vslot0 + c]));
       }
       if (!ok) break;
+      fence_proxy_async_smem();
+#pragma unroll
+      for (int c = 0; c < C::kRingPT; ++c) {
+        const uint32_t si = (si0 + c) % kSlabs;
+        warp_arrive(smem_u32(&sh->slab_empty[si]));
+        warp_arrive(smem_u32(&sh->full[vslot0 + c]));
+      }
       warp_arrive(smem_u32(&sh->etok_full[g & 3]));
       ++g;
     }
