@@ -325,6 +325,9 @@ def measure_workload(pkg, index, dev, steps, flush_l2, with_oracle=True):
             worst = max(worst, float(np.abs(got_all[b] - o).max()))
         res["max_abs_err_vs_oracle"] = worst
         res["oracle_rows_checked"] = len(rows)
+        # the CPU oracle's own rate on this workload (whole batch rows, about 1.5 s of wall time)
+        r, t, n, threads = oracle_sample_rate(inp, 1.5)
+        res["cpu_oracle"] = {"gbs": r, "cores": threads, "rows": n, "seconds": t}
     del inp, out
     torch.cuda.empty_cache()
     return res
