@@ -298,6 +298,23 @@ def test_balanced_cost_cuts_any_crossing_cost(pkg, kv_dtype, cross_rows):
             assert torch.count_nonzero(out[b]) == 0
 
 
+@pytest.mark.parametrize("kv_dtype", DTYPES)
+def test_balanced_many_short_sequences(pkg, kv_dtype):
+    # 3,000 sequences of 0-300 tokens in the balanced mode: the cut-point search runs three
+    # rounds over kv_indptr, each CTA walks about twenty sequences, and one in ten is empty.
+    # Every row is checked.
+    rng = np.random.default_rng(77 + kv_dtype)
+    lens = rng.integers(0, 301, size=3000)
+    lens[rng.random(3000) < 0.1] = 0
+    lens = [int(n) for n in lens]
+    inp = synth.make_inputs(len(lens), lens, kv_dtype, seed=91 + kv_dtype)
+    ref, _ = oracle.decode(inp.q, inp.kv, inp.kv_scale, inp.kv_indptr, kv_dtype)
+    out = _run(pkg, inp, 0)
+    _check(out, ref, f"3000 short sequences, dtype {kv_dtype}")
+    empty = [b for b, n in enumerate(lens) if n == 0]
+    assert torch.count_nonzero(out[empty]) == 0
+
+
 @pytest.mark.parametrize("ns", [0, 5])
 def test_repeated_calls_give_identical_results(pkg, ns):
     # The merge step re-arms its per-sequence counters at the end of every call.
