@@ -1235,8 +1235,9 @@ __device__ __forceinline__ float warp_sum(float t) {
   return t;
 }
 
-// kTwoPiece compiles the two-piece path (left out of the MXFP4 kernel, whose softmax warps
-// share the instruction cache with the dequantisation loop).
+// kTwoPiece compiles the two-piece path and the skipping of empty pieces' partial loads (both
+// left out of the MXFP4 kernel, whose softmax warps share the instruction cache with the
+// dequantisation loop; its balanced pieces are never empty).
 template <bool kTwoPiece>
 __device__ void merge_pieces(const DecodeParams& p, int b, int slot0, int pieces, int ts, int nt) {
   const int warp = ts >> 5, lane = ts & 31, nw = nt >> 5;
@@ -1311,6 +1312,7 @@ __device__ void merge_pieces(const DecodeParams& p, int b, int slot0, int pieces
 #pragma unroll 2
     for (int k = 0; k < pieces; ++k) {
       const float ua = __shfl_sync(0xffffffffu, wa, k), ub = __shfl_sync(0xffffffffu, wb, k);
+      if (kTwoPiece && ua == 0.f && ub == 0.f) continue;   // (warp-uniform) empty piece: no partial to read
       const float4* srca = reinterpret_cast<const float4*>(p.part_o + (static_cast<size_t>(slot0 + k) * kHeads + ha) * kDimV);
       const float4* srcb = reinterpret_cast<const float4*>(p.part_o + (static_cast<size_t>(slot0 + k) * kHeads + hb) * kDimV);
 #pragma unroll
@@ -1359,6 +1361,7 @@ __device__ void merge_pieces(const DecodeParams& p, int b, int slot0, int pieces
 #pragma unroll 4
         for (int k = 0; k < cnt; ++k) {
           const float w = __shfl_sync(0xffffffffu, myw, k);
+          if (kTwoPiece && w == 0.f) continue;   // (warp-uniform) empty piece: no partial to read
           const float4* src =
               reinterpret_cast<const float4*>(p.part_o + (static_cast<size_t>(slot0 + s0 + k) * kHeads + h) * kDimV);
 #pragma unroll
