@@ -119,7 +119,8 @@ int mla_decode(const void* q, const void* kv, const void* kv_scale, const int32_
  *                   Sequence b has (npages_b - 1) * page_size + kv_last_page_len[b] tokens.
  *  page_size        1, 2, 4, 8, 16, 32, 64 or 128.  Pages of 8 rows and more are loaded one
  *                   TMA box per page; pages of 1, 2 or 4 rows (fewer than a box's 8-row swizzle
- *                   atom; the pages' persistent default is 2) are copied 16 bytes at a time.
+ *                   atom; the pages' persistent default is 2) four rows per TMA gather (bf16,
+ *                   fp8) or 16 bytes at a time (MXFP4).
  *  num_splits       as mla_decode.  In the balanced mode (<= 0) the token positions are
  *                   those of the page space (sequence b starts at kv_page_indptr[b] *
  *                   page_size; the unused rows of its last page belong to no CTA's work)

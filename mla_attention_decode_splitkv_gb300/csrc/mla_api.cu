@@ -334,7 +334,9 @@ static int decode_impl(const void* q, const void* kv, const void* kv_scale, cons
   const Workspace ws = g_ws[dev];
 
   mla::DecodeParams p;
-  const int box_rows = page_size >= mla::kMinPage ? page_size : mla::kBN;   // (pages below 8 rows use no TMA box)
+  // Tiled boxes of one page (8+ rows), of one row for the four-row gathers of smaller pages,
+  // of 128 rows for a contiguous cache.
+  const int box_rows = page_size >= mla::kMinPage ? page_size : (page_size > 0 ? 1 : mla::kBN);
   rc = mla::encode_kv_map_rows(&p.tmap, kv, kv_dtype, box_rows);
   if (rc) return rc;
   if (kv_dtype == MLA_KV_FP8_E4M3) {

@@ -10,7 +10,7 @@ constexpr int kHeads = 16;
 constexpr int kDim = 576;
 constexpr int kDimV = 512;
 constexpr int kBN = 128;           // cached tokens per tile (= UMMA M)
-constexpr int kMinPage = 8;        // smallest page (rows) a TMA box loads whole: one swizzle atom; 1-4 use cp.async
+constexpr int kMinPage = 8;        // smallest page (rows) a TMA box loads whole: one swizzle atom; 1-4: see run_producer_sp
 constexpr int kMxBlock = 32;
 constexpr int kMxPacked = 288;     // bytes of e2m1 nibbles per row
 constexpr int kMxScales = 18;      // e8m0 scales per row
@@ -74,7 +74,7 @@ int balance_cross_rows(int kv_dtype);
 // Launches the split kernel for kv_dtype (geometry per dtype is internal to mla_split.cu).
 cudaError_t launch_split(int kv_dtype, const DecodeParams& p, int grid, cudaStream_t stream);
 // The same for a paged cache (page size 1 .. 128, a power of two; TMA boxes of page_size rows
-// from 8 rows up, 16-byte cp.async copies below).
+// from 8 rows up; four-row gathers (bf16, fp8) or 16-byte cp.async copies (MXFP4) below).
 cudaError_t launch_split_paged(int kv_dtype, const DecodeParams& p, int grid, cudaStream_t stream);
 // Tensor maps with boxes of `box_rows` rows (paged caches: box_rows = page size).
 int encode_kv_map_rows(CUtensorMap* map, const void* kv, int kv_dtype, int box_rows);

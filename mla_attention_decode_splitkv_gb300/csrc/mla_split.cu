@@ -152,7 +152,7 @@ struct SharedState {
   uint64_t rope_full[2];           // rope slots (fp8: TMA, MXFP4: dequant) / consumed by QK
   uint64_t rope_empty[2];
   int etok[4][128];                // per-row max block exponent of the last 4 tiles
-  int sp_rows[128];                // pages of 1-4 rows: the cache row of each window row of a tile
+  int sp_rows[128];                // MXFP4, pages of 1-4 rows: the cache row of each window row of a tile
   uint2 lut[kLutCount];            // 8 e4m3 bytes per block shift
   long long seg_total;              // kv_indptr[batch] (balanced mode)
   long long seg_lo, seg_hi;        // this CTA's position range (balanced mode)
@@ -729,13 +729,17 @@ __device__ void run_producer(const DecodeParams& p, SharedState* sh, uint8_t* ri
 }
 
 // ---------------------------------------------------------------- producer for pages of 1-4 rows (1 warp)
-// A TMA box of fewer than 8 rows would not fill whole 8-row swizzle atoms, so pages of 1, 2
-// or 4 rows are copied with 16-byte cp.async straight into the slot's swizzled layout (the
-// image a 128-row box would write): piece j of window row r lands at r * PITCH + ((j ^ s) <<
-// 4), s = r mod 8 (128-byte swizzle, PITCH 128) or (r / 2) mod 4 (64-byte swizzle, PITCH 64).
-// Every lane then arrives on the slot's full barrier when its own copies have landed (32
-// arrivals complete it).  These are generic-proxy writes: the MMA issuers that read such a
-// slot put a proxy fence after their wait.
+// A tiled TMA box of fewer than 8 rows would not fill whole 8-row swizzle atoms, so bf16 and
+// fp8 pages of 1, 2 or 4 rows are fetched with four-row gathers (tile::gather4) from maps
+// whose box is one row high: lane k gathers window rows 4k..4k+3 (their cache rows through
+// the page list) to rows 4k..4k+3 of the slot, where the copy engine swizzles each row by its
+// own shared address, as a 128-row box would be laid out.  Lane 0 sets the slot's expected
+// bytes first; the slot completes on bytes, like the tiled loads.  (MXFP4 slabs: cp.async,
+// below.)
+// MXFP4 slabs are 64 bytes wide, and a gather of four such rows moves too little per copy
+// engine operation: their pages of 1-4 rows are copied with 16-byte cp.async straight into
+// the slab's SW64 layout instead (piece j of window row r at r * 64 + ((j ^ (r / 2) mod 4)
+// << 4)), every lane arriving on the slab's full barrier when its own copies have landed.
 // Bytes [byte0, byte0 + W) of each of the tile's 128 window rows, whose cache rows are in
 // `rows`; lane = (row, piece) so that each warp-wide copy reads whole 32-byte sectors.
 template <int W, int PITCH>
@@ -757,7 +761,6 @@ __device__ void run_producer_sp(const DecodeParams& p, SharedState* sh, uint8_t*
                                 int lane) {
   using C = Cfg<KV>;
   volatile int* abortf = &sh->abort;
-  const int rb = KV == 0 ? 2 * kDim : (KV == 1 ? kDim : kMxPacked);   // bytes per cache row
   SegIter<true> it;
   it.init(p, blockIdx.x, sh);
   Seg s;
@@ -770,15 +773,24 @@ __device__ void run_producer_sp(const DecodeParams& p, SharedState* sh, uint8_t*
     const int ntiles = (n + kBN - 1) / kBN;
     const int np = (s.n_total + p.page_size - 1) >> p.page_shift;
     for (int t = 0; t < ntiles && ok; ++t) {
-      // Cache row of every window row (rows past the sequence reuse its last page; masked).
-      __syncwarp();
-      for (int r = lane; r < kBN; r += 32) {
-        const int tok = s.n_lo + t * kBN + r;
-        sh->sp_rows[r] = (p.page_indices[s.row0 + min(tok >> p.page_shift, np - 1)] << p.page_shift) +
-                         (tok & (p.page_size - 1));
+      // Cache rows of this lane's four window rows (rows past the sequence reuse its last
+      // page; they are masked).  MXFP4: every window row's, in shared memory for sp_copy.
+      int y[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int tok = s.n_lo + t * kBN + 4 * lane + i;
+        y[i] = (p.page_indices[s.row0 + min(tok >> p.page_shift, np - 1)] << p.page_shift) + (tok & (p.page_size - 1));
       }
-      __syncwarp();
-      const int* rows = sh->sp_rows;
+      if constexpr (KV == 2) {
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 4; ++i) sh->sp_rows[4 * lane + i] = y[i];
+        __syncwarp();
+      }
+      // Four rows of `pitch` bytes per lane at column x of `map`, into the slot image at dst.
+      auto gather = [&](uint32_t dst, const CUtensorMap* map, int x, int pitch, uint32_t fb) {
+        tma_gather4(dst + 4 * lane * pitch, map, x, y[0], y[1], y[2], y[3], fb);
+      };
       for (int c0 = 0; c0 < (KV == 2 ? 5 : C::kRingPT); ++c0) {
         const uint32_t eb = KV == 2 ? smem_u32(&sh->slab_empty[slot]) : smem_u32(&sh->empty[slot]);
         if (!producer_wait<true>(eb, phase ^ 1, abortf, p.status, p.wait_limit_ns)) {
@@ -788,22 +800,25 @@ __device__ void run_producer_sp(const DecodeParams& p, SharedState* sh, uint8_t*
         if constexpr (KV == 2) {
           const int c = mx_chunk(c0);
           const uint32_t dst = smem_u32(slabs + slot * kSlabBytes);
-          if (c < 4) sp_copy<64, 64>(p.kv, rb, rows, dst, 64 * c, lane);
-          else sp_copy<32, 64>(p.kv, rb, rows, dst, 4 * 64, lane);   // the rope's 32 bytes (the rest unused)
+          if (c < 4) sp_copy<64, 64>(p.kv, kMxPacked, sh->sp_rows, dst, 64 * c, lane);
+          else sp_copy<32, 64>(p.kv, kMxPacked, sh->sp_rows, dst, 4 * 64, lane);   // the rope's 32 bytes (the rest unused)
           cp_async_mbar_arrive(smem_u32(&sh->slab_full[slot]));
         } else {
           const uint32_t dst = smem_u32(ring + slot * C::kSlotBytes);
-          if constexpr (KV == 0) {
+          const uint32_t fb = smem_u32(&sh->full[slot]);
+          if constexpr (KV == 0) {   // x in bf16 elements; value slots hold two 64-column boxes
             if (c0 < 4) {
-              sp_copy<128, 128>(p.kv, rb, rows, dst, 256 * c0, lane);
-              sp_copy<128, 128>(p.kv, rb, rows, dst + 16384, 256 * c0 + 128, lane);
+              expect_slot<true>(fb, 32768, lane);
+              gather(dst, &p.tmap, 128 * c0, 128, fb);
+              gather(dst + 16384, &p.tmap, 128 * c0 + 64, 128, fb);
             } else {
-              sp_copy<128, 128>(p.kv, rb, rows, dst, 2 * kDimV, lane);
+              expect_slot<true>(fb, 16384, lane);
+              gather(dst, &p.tmap, kDimV, 128, fb);
             }
           } else {
-            sp_copy<128, 128>(p.kv, rb, rows, dst, 128 * c0, lane);
+            expect_slot<true>(fb, 16384, lane);
+            gather(dst, &p.tmap, 128 * c0, 128, fb);
           }
-          cp_async_mbar_arrive(smem_u32(&sh->full[slot]));
         }
         ++idx;
         if (++slot == static_cast<uint32_t>(kSlots)) { slot = 0; phase ^= 1; }
@@ -816,8 +831,9 @@ __device__ void run_producer_sp(const DecodeParams& p, SharedState* sh, uint8_t*
           ok = false;
           break;
         }
-        sp_copy<64, 64>(p.kv, rb, rows, smem_u32(rope + rs * kRopeBytes), kDimV, lane);
-        cp_async_mbar_arrive(smem_u32(&sh->rope_full[rs]));
+        const uint32_t fb = smem_u32(&sh->rope_full[rs]);
+        expect_slot<true>(fb, kRopeBytes, lane);
+        gather(smem_u32(rope + rs * kRopeBytes), &p.tmap_rope, kDimV, 64, fb);
         ++ridx;
       }
     }
@@ -1111,7 +1127,6 @@ __device__ void run_mma_qk(const DecodeParams& p, SharedState* sh, const Descs& 
         const uint32_t fb = rope_sep ? smem_u32(&sh->rope_full[rs]) : smem_u32(&sh->full[slot]);
         if (!(ok = wait_bar(fb, rope_sep ? rph : phase, abortf, p.status, p.wait_limit_ns))) break;
         tc_fence_after();
-        if constexpr (SP && KV != 2) fence_proxy_async_smem();   // cp.async (generic-proxy) data, read by the MMAs
         const uint64_t a = rope_sep ? ds.rope + dofs(rs * kRopeBytes) : ds.ring_k + dofs(slot * C::kSlotBytes);
         if constexpr (KV == 0) {
           const uint64_t b = ds.q + dofs(2 * c * G::kQChunk);
@@ -1161,7 +1176,6 @@ __device__ void run_mma_pv(const DecodeParams& p, SharedState* sh, const Descs& 
           !(ok = wait_bar(smem_u32(&sh->o_free), (kseg - 1) & 1, abortf, p.status, p.wait_limit_ns)))
         break;
       tc_fence_after();
-      if constexpr (SP && KV != 2) fence_proxy_async_smem();     // cp.async (generic-proxy) data, read by the MMAs
       const bool first = (t == 0);
       const uint64_t b = ds.p + dofs((g & 1) * G::kPBuf);
 #pragma unroll
@@ -1762,7 +1776,7 @@ __device__ void run_softmax(const DecodeParams& p, SharedState* sh, uint8_t* qs,
 }
 
 // ---------------------------------------------------------------- the kernel
-// PG: paged cache.  SP: pages of 1, 2 or 4 rows (copied by the producer warp with cp.async).
+// PG: paged cache.  SP: pages of 1, 2 or 4 rows (four-row gathers; MXFP4 slabs: cp.async).
 // QL: query tokens decoded together (2: the fused multi-token instances).
 template <int KV, bool PG, bool SP, int QL>
 __global__ void __launch_bounds__(Cfg<KV>::kThreads, 1) mla_split_kernel(const __grid_constant__ DecodeParams p) {
@@ -1780,13 +1794,13 @@ __global__ void __launch_bounds__(Cfg<KV>::kThreads, 1) mla_split_kernel(const _
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < G::kRing; ++i) {
-      // MXFP4: one arrival per dequant warp; pages of 1-4 rows: one cp.async arrival per producer lane
-      mbar_init(smem_u32(&sh->full[i]), KV == 2 ? C::kDeqWarps : (SP ? 32 : 1));
+      // MXFP4: one arrival per dequant warp; otherwise the producer's expected-bytes arrival
+      mbar_init(smem_u32(&sh->full[i]), KV == 2 ? C::kDeqWarps : 1);
       mbar_init(smem_u32(&sh->empty[i]), 1);
     }
     if (KV == 2) {
       for (int i = 0; i < kSlabs; ++i) {
-        mbar_init(smem_u32(&sh->slab_full[i]), SP ? 32 : 1);
+        mbar_init(smem_u32(&sh->slab_full[i]), SP ? 32 : 1);   // pages of 1-4 rows: one cp.async arrival per producer lane
         mbar_init(smem_u32(&sh->slab_empty[i]), C::kDeqWarps);   // one arrival per dequant warp
       }
       for (int i = 0; i < 4; ++i) mbar_init(smem_u32(&sh->etok_full[i]), C::kDeqWarps);
@@ -1795,7 +1809,7 @@ __global__ void __launch_bounds__(Cfg<KV>::kThreads, 1) mla_split_kernel(const _
     // softmax-side barriers count warps (one arrival per warp)
     mbar_init(smem_u32(&sh->q_ready), 4 * QL);  // four softmax warps per query token stage q
     for (int i = 0; i < C::kRopeSlots; ++i) {
-      mbar_init(smem_u32(&sh->rope_full[i]), KV == 2 ? C::kDeqWarps : (SP ? 32 : 1));   // MXFP4: per dequant warp
+      mbar_init(smem_u32(&sh->rope_full[i]), KV == 2 ? C::kDeqWarps : 1);   // MXFP4: per dequant warp
       mbar_init(smem_u32(&sh->rope_empty[i]), 1);                          // QK commit
     }
     for (int i = 0; i < 2; ++i) {
@@ -1950,7 +1964,7 @@ cudaError_t launch_split_paged(int kv_dtype, const DecodeParams& p, int grid, cu
     if (kv_dtype == 1) return sp ? launch_split_t<1, true, true, 2>(p, grid, stream) : launch_split_t<1, true, false, 2>(p, grid, stream);
     return cudaErrorNotSupported;
   }
-  if (p.page_size < kMinPage) {   // pages of 1, 2 or 4 rows: cp.async producer
+  if (p.page_size < kMinPage) {   // pages of 1, 2 or 4 rows (run_producer_sp)
     if (kv_dtype == 0) return launch_split_t<0, true, true>(p, grid, stream);
     if (kv_dtype == 1) return launch_split_t<1, true, true>(p, grid, stream);
     if (kv_dtype == 2) return launch_split_t<2, true, true>(p, grid, stream);

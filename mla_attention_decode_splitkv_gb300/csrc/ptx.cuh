@@ -107,6 +107,20 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int3
       : "memory");
 }
 
+// Gather of four rows (tile::gather4, 2D map whose box is one row high): columns [x, x + box
+// width) of rows y0..y3 land one after another at dst, each row swizzled by its own shared
+// address as a tiled copy would place it (checked on GB300 for the 64- and 128-byte
+// swizzles), so four gathers to rows 4k..4k+3 build a 128-row box image.  Signals `bar`
+// with its bytes.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const void* tmap, int32_t x, int32_t y0, int32_t y1,
+                                            int32_t y2, int32_t y3, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, "
+      "%5, %6}], [%7];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(bar)
+      : "memory");
+}
+
 // ---------------------------------------------------------------- cp.async (16-byte copies)
 // Copies 16 bytes global -> shared (cached in L2 only).  Generic-proxy writes.
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
