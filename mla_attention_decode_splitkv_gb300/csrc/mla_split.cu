@@ -1635,7 +1635,9 @@ __device__ void run_softmax(const DecodeParams& p, SharedState* sh, uint8_t* qs,
             }
             tmem_wait_st();
           }
-          okt = okt && ok2;  // a failed wait aborts at the next barrier
+          // A failed wait has set the abort flag and the status word.  The warp carries on: the
+          // softmax warps learn of the abort at their next waits and leave together at the next
+          // named barrier (a warp leaving alone would strand the others there).
         }
         // P = 2^(w - mref) <= 2^kTau (QL = 2: a column with no visible row yet has mref = -inf)
         float P[H];
