@@ -337,6 +337,18 @@ def test_maximum_split_count(pkg, kv_dtype):
     _check(_run(pkg, inp, 4096), ref, f"4096 splits dtype {kv_dtype}")
 
 
+@pytest.mark.parametrize("kv_dtype", DTYPES)
+def test_one_long_sequence_over_every_cta(pkg, kv_dtype):
+    # Balanced mode on a batch of one 300,001-token sequence: every CTA streams a piece of it
+    # (2,344 tiles and a one-row tail over one CTA per SM), and the last finisher merges as
+    # many pieces as there are SMs.  A uniform split into 300 pieces checks the same sequence.
+    lens = [300_001]
+    inp = synth.make_inputs(1, lens, kv_dtype, seed=300)
+    ref, _ = oracle.decode(inp.q, inp.kv, inp.kv_scale, inp.kv_indptr, kv_dtype)
+    for ns in (0, 300):
+        _check(_run(pkg, inp, ns), ref, f"one long sequence dtype {kv_dtype} ns {ns}")
+
+
 def test_split_count_above_the_limit_is_rejected(pkg):
     inp = synth.make_inputs(1, [10], synth.KV_FP8, seed=1).to("cuda")
     out = torch.empty((1, 16, 512), dtype=torch.bfloat16, device="cuda")
