@@ -181,9 +181,13 @@ struct Geo {
   static constexpr int kQBytes = C::kQBytes * QL;
   static constexpr int kQChunk = (KV == 0 ? 2048 : 4096) * QL;   // one K-major q chunk [rows x 128 B]
   static constexpr int kPBuf = kPBytes * QL;            // one P^T buffer: [128 tokens x 32 QL B]
-  // The second query token's q and P^T buffers take ring slots: fp8 keeps 9 (2.25 tiles),
-  // bf16 one tile's 5.
-  static constexpr int kRing = QL == 1 ? C::kRing : (KV == 1 ? 9 : C::kRingPT);
+  // P^T buffers: two (tile parity), or one in the fused two-token fp8 instance, whose softmax
+  // writes P of tile g after the PV MMAs of tile g - 1 have read theirs (they complete well
+  // before the softmax of tile g gets that far), so that its ring keeps a tenth slot.
+  static constexpr int kPBufs = (QL == 2 && KV == 1) ? 1 : 2;
+  // The second query token's q (and P^T) take ring slots: fp8 keeps 10 (2.5 tiles), bf16 one
+  // tile's 5.
+  static constexpr int kRing = QL == 1 ? C::kRing : (KV == 1 ? 10 : C::kRingPT);
 };
 
 template <int KV>
@@ -197,7 +201,7 @@ __host__ __device__ constexpr size_t rope_bytes() {
 template <int KV, int QL = 1>
 __host__ __device__ constexpr size_t smem_bytes() {
   using G = Geo<KV, QL>;
-  return 1024 + (size_t)G::kRing * Cfg<KV>::kSlotBytes + rope_bytes<KV>() + G::kQBytes + 2 * G::kPBuf +
+  return 1024 + (size_t)G::kRing * Cfg<KV>::kSlotBytes + rope_bytes<KV>() + G::kQBytes + G::kPBufs * G::kPBuf +
          raw_bytes<KV>() + sizeof(SharedState);
 }
 static_assert(smem_bytes<2>() <= 232448, "MXFP4 shared memory exceeds 227 KB");
@@ -1177,7 +1181,7 @@ __device__ void run_mma_pv(const DecodeParams& p, SharedState* sh, const Descs& 
         break;
       tc_fence_after();
       const bool first = (t == 0);
-      const uint64_t b = ds.p + dofs((g & 1) * G::kPBuf);
+      const uint64_t b = ds.p + dofs((G::kPBufs == 2 ? (g & 1) : 0u) * G::kPBuf);
 #pragma unroll
       for (int mm = 0; mm < 2; ++mm) {
         const int m = 2 * part + mm;
@@ -1643,11 +1647,17 @@ __device__ void run_softmax(const DecodeParams& p, SharedState* sh, uint8_t* qs,
         float P[H];
 #pragma unroll
         for (int h = 0; h < H; ++h) P[h] = ex2(x[h] - ((QL == 2 && mr[h] == kNegInf) ? 0.f : mr[h]));
-        if (j == 0 && g >= 2)
-          wait_bar(smem_u32(&sh->pv_done[g & 1]), ((g >> 1) & 1) ^ 1, abortf, p.status, p.wait_limit_ns);
+        // The P^T buffer was last read by the PV MMAs of tile g - 2 (two buffers) or g - 1 (one).
+        if constexpr (G::kPBufs == 2) {
+          if (j == 0 && g >= 2)
+            wait_bar(smem_u32(&sh->pv_done[g & 1]), ((g >> 1) & 1) ^ 1, abortf, p.status, p.wait_limit_ns);
+        } else {
+          if (j == 0 && g >= 1)
+            wait_bar(smem_u32(&sh->pv_done[(g - 1) & 1]), ((g - 1) >> 1) & 1, abortf, p.status, p.wait_limit_ns);
+        }
         // P^T row of this token: 32 QL bytes (per query token: 16 heads of hi then of lo e4m3,
         // or 16 bf16); swizzled in 16-byte chunks, 32-byte (QL = 1) or 64-byte (QL = 2) pattern.
-        uint8_t* prow = ps + (g & 1) * G::kPBuf + row * 32 * QL;
+        uint8_t* prow = ps + (G::kPBufs == 2 ? (g & 1) : 0u) * G::kPBuf + row * 32 * QL;
         const int sw = QL == 1 ? (row >> 2) & 1 : (row >> 1) & 3;
         if constexpr (KV == 0) {
           uint32_t wv[H / 2];
@@ -1790,7 +1800,7 @@ __global__ void __launch_bounds__(Cfg<KV>::kThreads, 1) mla_split_kernel(const _
   uint8_t* rope = ring + G::kRing * C::kSlotBytes;
   uint8_t* qs = rope + rope_bytes<KV>();
   uint8_t* ps = qs + G::kQBytes;
-  uint8_t* slabs = ps + 2 * G::kPBuf;                // MXFP4 packed-row staging
+  uint8_t* slabs = ps + G::kPBufs * G::kPBuf;        // MXFP4 packed-row staging
   SharedState* sh = reinterpret_cast<SharedState*>(slabs + raw_bytes<KV>());
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
