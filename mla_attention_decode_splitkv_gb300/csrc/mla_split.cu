@@ -110,10 +110,11 @@ struct Cfg<2> {                    // MXFP4 cache: dequantised to an e4m3 carrie
   static constexpr int kThreads = 32 * (4 + kSoftWarps + kDeqWarps);   // issuers, softmax, dequant
   // Registers per thread after the role split (launch: 128 each): the issuer and dequant
   // warpgroups give registers up to the softmax warpgroups.
-  // 32 * (4 * 80 + 8 * 168 + 4 * 96) = 65536 = 512 * 128.
-  static constexpr int kRegsIssue = 80;
-  static constexpr int kRegsSoft = 168;
-  static constexpr int kRegsDeq = 96;
+  // 32 * (4 * 72 + 8 * 160 + 4 * 120) = 65536 = 512 * 128.  (The dequantisation loop gains
+  // from the larger budget: 256 x 8192 at 80 / 168 / 96 took 327 us, at 72 / 160 / 120 318.)
+  static constexpr int kRegsIssue = 72;
+  static constexpr int kRegsSoft = 160;
+  static constexpr int kRegsDeq = 120;
   static constexpr int kRegsNeeded = 32 * (4 * kRegsIssue + kSoftWarps * kRegsSoft + kDeqWarps * kRegsDeq);
 };
 static_assert(Cfg<2>::kRegsNeeded <= 65536, "MXFP4 register split exceeds the register file");
@@ -921,12 +922,19 @@ __device__ void run_dequant(const DecodeParams& p, SharedState* sh, uint8_t* rin
   Seg s;
   uint32_t g = 0, slab_i = 0, slab_ph = 0;
   bool ok = true;
+  // Barrier tests issued ahead of the work they gate (their shared-memory round trips overlap
+  // the conversion; a test that finds the phase incomplete falls back to the bounded wait).
+  bool pre_slab = false;   // the next slab to read has landed
   while (ok && it.next(p, s)) {
     const int n = s.n_hi - s.n_lo;
     if (n <= 0) continue;
     const int ntiles = (n + kBN - 1) / kBN;
     uint32_t scn[9];   // block scales of the segment's next tile, loaded one tile ahead
     for (int t = 0; t < ntiles; ++t) {
+      // Rope carrier slot g mod 2 was last read by the QK MMAs of tile g - 2; the value slots
+      // by the PV MMAs of tile g - 2.
+      const bool pre_rope = mbar_test_wait(smem_u32(&sh->rope_empty[g & 1]), ((g >> 1) & 1) ^ 1);
+      const bool pre_pv = g < 2 || mbar_test_wait(smem_u32(&sh->pv_done[g & 1]), ((g >> 1) & 1) ^ 1);
       const Window w = tile_window<2, PG>(p, s, t);
       // e_i = max_j E_j and the shift-table index min(e_i - E_j, 13) of each block, packed
       // as 4-bit fields (block j in bits 4 (j % 8) of kpk[j / 8]).
@@ -977,8 +985,10 @@ __device__ void run_dequant(const DecodeParams& p, SharedState* sh, uint8_t* rin
       {
         const uint32_t si = slab_i, sph = slab_ph;
         if (++slab_i == kSlabs) { slab_i = 0; slab_ph ^= 1u; }
-        ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&sh->slab_full[si]), sph, abortf, p.status, p.wait_limit_ns));
-        if (!ok) break;
+        if (!__all_sync(0xffffffffu, pre_slab)) {
+          ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&sh->slab_full[si]), sph, abortf, p.status, p.wait_limit_ns));
+          if (!ok) break;
+        }
         const uint32_t srow = smem_u32(slabs + si * kSlabBytes + di * 64);
         uint4 v0, v1;
         if constexpr (kRT == 1) {
@@ -994,10 +1004,12 @@ __device__ void run_dequant(const DecodeParams& p, SharedState* sh, uint8_t* rin
         // segments read a few MX blocks of a value chunk from the slab's next fill.)
         fence_proxy_async_smem();
         warp_arrive(smem_u32(&sh->slab_empty[si]));
-        // Rope carrier slot g mod 2 was last read by the QK MMAs of tile g - 2.
-        ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&sh->rope_empty[g & 1]), ((g >> 1) & 1) ^ 1, abortf, p.status,
-                                              p.wait_limit_ns));
-        if (!ok) break;
+        pre_slab = mbar_test_wait(smem_u32(&sh->slab_full[slab_i]), slab_ph);   // value chunk 0's slab
+        if (!__all_sync(0xffffffffu, pre_rope)) {
+          ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&sh->rope_empty[g & 1]), ((g >> 1) & 1) ^ 1, abortf,
+                                                p.status, p.wait_limit_ns));
+          if (!ok) break;
+        }
         uint8_t* dst = rope + (g & 1) * kRopeBytes + di * 64;                 // [128 x 64 B] SW64
         uint4 lo, hi;
         if constexpr (kRT == 1) {
@@ -1019,7 +1031,7 @@ __device__ void run_dequant(const DecodeParams& p, SharedState* sh, uint8_t* rin
       // The value slots of tile g were last read by tile g - 2: one wait on its PV completion
       // covers all four (QK of g - 2 completed before its softmax, hence before its PV).
       static_assert(C::kRing == 2 * C::kRingPT, "the MXFP4 value ring holds exactly two tiles");
-      if (g >= 2) {
+      if (!__all_sync(0xffffffffu, pre_pv)) {
         ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&sh->pv_done[g & 1]), ((g >> 1) & 1) ^ 1, abortf, p.status,
                                               p.wait_limit_ns));
         if (!ok) break;
@@ -1035,8 +1047,10 @@ __device__ void run_dequant(const DecodeParams& p, SharedState* sh, uint8_t* rin
       for (int c = 0; c < C::kRingPT; ++c) {
         const uint32_t si = slab_i, sph = slab_ph;
         if (++slab_i == kSlabs) { slab_i = 0; slab_ph ^= 1u; }
-        ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&sh->slab_full[si]), sph, abortf, p.status, p.wait_limit_ns));
-        if (!ok) break;
+        if (!__all_sync(0xffffffffu, pre_slab)) {
+          ok = __all_sync(0xffffffffu, wait_bar(smem_u32(&sh->slab_full[si]), sph, abortf, p.status, p.wait_limit_ns));
+          if (!ok) break;
+        }
         // The packed words are read with volatile loads, which ptxas schedules better here
         // (256 x 8192: 376 -> 345 us).
         const uint32_t srow = smem_u32(slabs + si * kSlabBytes + di * 64);
@@ -1045,6 +1059,8 @@ __device__ void run_dequant(const DecodeParams& p, SharedState* sh, uint8_t* rin
         uint4 v[kB];
 #pragma unroll
         for (int q = 0; q < kB; ++q) v[q] = ld_shared_v4_volatile(srow + (((b0 + q) ^ ssw) << 4));
+        // The next slab: value chunk c + 1, or the next tile's rope chunk.
+        pre_slab = mbar_test_wait(smem_u32(&sh->slab_full[slab_i]), slab_ph);
         uint8_t* dst = ring + (vslot0 + c) * C::kSlotBytes + di * 128;       // [128 x 128 B] SW128
         const uint32_t kc = static_cast<uint32_t>(kv64 >> (16 * c + 4 * b0)); // blocks 4c + b0 ..
 #pragma unroll
@@ -1059,11 +1075,9 @@ __device__ void run_dequant(const DecodeParams& p, SharedState* sh, uint8_t* rin
       if (!ok) break;
       fence_proxy_async_smem();
 #pragma unroll
-      for (int c = 0; c < C::kRingPT; ++c) {
-        const uint32_t si = (si0 + c) % kSlabs;
-        warp_arrive(smem_u32(&sh->slab_empty[si]));
-        warp_arrive(smem_u32(&sh->full[vslot0 + c]));
-      }
+      for (int c = 0; c < C::kRingPT; ++c) warp_arrive(smem_u32(&sh->slab_empty[(si0 + c) % kSlabs]));
+      // The QK MMAs take the four value chunks together, on the last chunk's barrier.
+      warp_arrive(smem_u32(&sh->full[vslot0 + C::kRingPT - 1]));
       warp_arrive(smem_u32(&sh->etok_full[g & 3]));
       ++g;
     }
@@ -1129,7 +1143,13 @@ __device__ void run_mma_qk(const DecodeParams& p, SharedState* sh, const Descs& 
         const uint32_t rs = C::kRopeSlots > 0 ? g % (C::kRopeSlots > 0 ? C::kRopeSlots : 1) : 0;
         const uint32_t rph = C::kRopeSlots > 0 ? (g / (C::kRopeSlots > 0 ? C::kRopeSlots : 1)) & 1 : 0;
         const uint32_t fb = rope_sep ? smem_u32(&sh->rope_full[rs]) : smem_u32(&sh->full[slot]);
-        if (!(ok = wait_bar(fb, rope_sep ? rph : phase, abortf, p.status, p.wait_limit_ns))) break;
+        // MXFP4: the dequantisation publishes a tile's four value chunks together, on the last
+        // chunk's barrier (the first value chunk's slot is 4 (g mod 2), so that one is slot + 3).
+        const bool mx_value = KV == 2 && !rope_sep;
+        if ((!mx_value || c == 0) &&
+            !(ok = wait_bar(mx_value ? smem_u32(&sh->full[slot + 3]) : fb, rope_sep ? rph : phase, abortf, p.status,
+                            p.wait_limit_ns)))
+          break;
         tc_fence_after();
         const uint64_t a = rope_sep ? ds.rope + dofs(rs * kRopeBytes) : ds.ring_k + dofs(slot * C::kSlotBytes);
         if constexpr (KV == 0) {
@@ -1806,7 +1826,8 @@ __global__ void __launch_bounds__(Cfg<KV>::kThreads, 1) mla_split_kernel(const _
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < G::kRing; ++i) {
-      // MXFP4: one arrival per dequant warp; otherwise the producer's expected-bytes arrival
+      // MXFP4: one arrival per dequant warp (on the last value slot of each tile); otherwise
+      // the producer's expected-bytes arrival
       mbar_init(smem_u32(&sh->full[i]), KV == 2 ? C::kDeqWarps : 1);
       mbar_init(smem_u32(&sh->empty[i]), 1);
     }
