@@ -189,6 +189,13 @@ struct Geo {
   // The second query token's q (and P^T) take ring slots: fp8 keeps 10 (2.5 tiles), bf16 one
   // tile's 5.
   static constexpr int kRing = QL == 1 ? C::kRing : (KV == 1 ? 10 : C::kRingPT);
+  // Register split (setmaxnreg) after the role dispatch: MXFP4 (issuers / softmax / dequant)
+  // and the fused two-token fp8 instance, whose softmax holds both tokens' hi and lo columns
+  // (issuers / softmax: 128 * 88 + 256 * 208 = 64512 = 384 * 168).
+  static constexpr bool kSplitRegs = KV == 2 || (KV == 1 && QL == 2);
+  static constexpr int kRegsIssue = KV == 2 ? Cfg<2>::kRegsIssue : 88;
+  static constexpr int kRegsSoft = KV == 2 ? Cfg<2>::kRegsSoft : 208;
+  static constexpr int kRegsNeeded = KV == 2 ? Cfg<2>::kRegsNeeded : 32 * (4 * kRegsIssue + C::kSoftWarps * kRegsSoft);
 };
 
 template <int KV>
@@ -1903,7 +1910,7 @@ __global__ void __launch_bounds__(Cfg<KV>::kThreads, 1) mla_split_kernel(const _
   // register-budget change sits at the top of its warpgroup's branch, so that the role's
   // code is compiled for that budget.
   if (warp < 4) {
-    if constexpr (KV == 2) regs_dec<C::kRegsIssue>();
+    if constexpr (G::kSplitRegs) regs_dec<G::kRegsIssue>();
     if (warp == 0) {
       if (PG || lane == 0) {   // paged: the whole warp (one lane per page)
         if constexpr (SP) run_producer_sp<KV, QL>(p, sh, ring, rope, slabs, lane);
@@ -1917,7 +1924,7 @@ __global__ void __launch_bounds__(Cfg<KV>::kThreads, 1) mla_split_kernel(const _
     }
     __syncwarp();
   } else if (warp < 4 + C::kSoftWarps) {
-    if constexpr (KV == 2) regs_inc<C::kRegsSoft>();
+    if constexpr (G::kSplitRegs) regs_inc<G::kRegsSoft>();
     run_softmax<KV, PG, QL>(p, sh, qs, ps, tmem);
   } else {
     if constexpr (KV == 2) {
@@ -1936,7 +1943,7 @@ __global__ void __launch_bounds__(Cfg<KV>::kThreads, 1) mla_split_kernel(const _
 constexpr int kMaxDevices = 64;
 
 // Per-device, once: the kernel's dynamic shared-memory limit (a per-function attribute
-// that each device context keeps) and, for MXFP4, the register-split check.  Thread-safe;
+// that each device context keeps) and, for the instances with a register split, its check.  Thread-safe;
 // the outcome of the first attempt on a device is kept.
 template <int KV, bool PG, bool SP, int QL>
 cudaError_t configure_once(int dev) {
@@ -1945,12 +1952,13 @@ cudaError_t configure_once(int dev) {
   std::call_once(once[dev], [dev] {
     cudaError_t e = cudaFuncSetAttribute(mla_split_kernel<KV, PG, SP, QL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem_bytes<KV, QL>()));
-    if (e == cudaSuccess && KV == 2) {
+    if (e == cudaSuccess && Geo<KV, QL>::kSplitRegs) {
       // The register split's increases only complete if the CTA launched with at least the
       // registers the split hands out: refuse to launch otherwise.
       cudaFuncAttributes fa;
       e = cudaFuncGetAttributes(&fa, mla_split_kernel<KV, PG, SP, QL>);
-      if (e == cudaSuccess && fa.numRegs * Cfg<KV>::kThreads < Cfg<2>::kRegsNeeded) e = cudaErrorInvalidConfiguration;
+      if (e == cudaSuccess && fa.numRegs * Cfg<KV>::kThreads < Geo<KV, QL>::kRegsNeeded)
+        e = cudaErrorInvalidConfiguration;
     }
     result[dev] = e;
   });
