@@ -902,7 +902,8 @@ __device__ __forceinline__ void deq_block(const uint4 v, const uint2 lut, uint4&
 // (128 dims) goes to ring slot 4 * (g & 1) + c (the ring holds the value chunks of exactly
 // two tiles, so dequantising tile g + 2 only waits for the PV MMAs of tile g); the rope
 // chunk goes to its own SW64 buffer and is published (and its slab freed) as soon as it is
-// done; the four value chunks are published, and their slabs freed, together.  Window rows
+// done; the four value chunks are published (on the last one's barrier, the one the QK
+// issuer waits for), and their slabs freed, together.  Window rows
 // before cached row 0 hold zeros (TMA fill) and get no scale: they decode to zeros.
 template <bool PG>
 __device__ void run_dequant(const DecodeParams& p, SharedState* sh, uint8_t* ring, uint8_t* rope, uint8_t* slabs) {
@@ -1092,9 +1093,9 @@ __device__ void run_dequant(const DecodeParams& p, SharedState* sh, uint8_t* rin
 }
 
 // ---------------------------------------------------------------- MMA issuer (1 thread)
-// MMA issue.  Two single-thread issuers on separate warps keep the tensor core fed: one
-// issues every QK^T group, the other every PV group (independent accumulators), each
-// blocking only on its own barriers.  Shared-memory descriptors are built once; per MMA
+// MMA issue.  Single-thread issuers on separate warps keep the tensor core fed: one issues
+// every QK^T group, two share the PV groups (two 128-dim blocks of O each; independent
+// accumulators), each blocking only on its own barriers.  Shared-memory descriptors are built once; per MMA
 // only the 14-bit start-address field advances (one 64-bit add), so an MMA costs a few
 // instructions of issue.
 struct Descs {
