@@ -332,16 +332,13 @@ def measure_workload(pkg, index, dev, steps, flush_l2, with_oracle=True):
     return res
 
 
-def config_dict(spec, inp, ns=None):
-    """ns: the num_splits the timed calls use (None: not applicable, e.g. the oracle arm)."""
+def config_dict(spec, inp):
+    """The workload, the same for both arms (the GPU arm's launch shape is in its `launch` key)."""
     from mla_attention_decode_splitkv_gb300 import synth
     lens = inp.lens
     return {"workload": spec.name, "batch": spec.batch,
             "kv_len": spec.kv_len if spec.kv_len else f"ragged U[1,8192], mean {sum(lens) / len(lens):.0f}",
             "kv_dtype": synth.DTYPE_NAMES[spec.kv_dtype],
-            "num_splits": ("as the GPU arm" if ns is None else
-                           (f"{ns} per sequence (uniform)" if ns else "balanced (persistent, one CTA per SM)")
-                           + ("" if spec.num_splits is not None else ", chosen by mla_decode_pick_splits")),
             "heads": 16, "head_dim": 576, "v_dim": 512, "kv_bytes_per_call": inp.kv_bytes(),
             "l2": "flushed between timed calls (256 MiB write, then 256 MiB read to retire the dirty lines)",
             "headline": "value and roofline are this workload's; the metric is per workload, and all five "
@@ -524,7 +521,9 @@ def main():
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": {0: "bf16", 1: "e4m3", 2: "e4m3"}[spec.kv_dtype],
         "data": "synthetic (seeded N(0,1) q and KV, stored per the workload's cache encoding)",
-        "config": config_dict(spec, inp, ns),
+        "config": config_dict(spec, inp),
+        "launch": {"num_splits": (f"{ns} per sequence (uniform)" if ns else "balanced (persistent, one CTA per SM)")
+                                 + ("" if spec.num_splits is not None else ", chosen by mla_decode_pick_splits")},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_kind": f"{peak_kind} (burst copy)", "kernel": "mla_split_kernel",
                      "split_kernel_us": split_ms * 1e3, "algorithmic_bytes_per_launch": kv_bytes,
