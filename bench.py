@@ -95,12 +95,14 @@ def peaks():
 
 
 def kernel_source_hash() -> str:
+    """Hash of the split kernel's translation unit: mla_split.cu and the headers it includes
+    (the device code the committed ncu counters were taken on; the host-only sources of the
+    library do not enter)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "mla_attention_decode_splitkv_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            h.update(name.encode())
-            h.update(open(os.path.join(csrc, name), "rb").read())
+    for name in ("mla_internal.h", "mla_split.cu", "ptx.cuh"):
+        h.update(name.encode())
+        h.update(open(os.path.join(csrc, name), "rb").read())
     return h.hexdigest()[:16]
 
 

@@ -77,8 +77,8 @@ typedef enum {
  *             the pieces of each sequence.  The ranges split the batch's cost evenly: its
  *             tokens plus, for every sequence start after the first, the rows a CTA gets
  *             through in the time it loses moving to the next sequence (the split model's
- *             x of mla_decode_pick_splits: 521 fp8 rows, 260 bf16 rows; for MXFP4, whose
- *             CTAs run at 0.275 of the HBM rate, 270 rows), so that a CTA that crosses
+ *             x of mla_decode_pick_splits: 521 fp8 rows, 260 bf16 rows, 294 MXFP4 rows),
+ *             so that a CTA that crosses
  *             sequence boundaries is given fewer tokens.
  *             At most 4096 splits.  mla_decode_pick_splits returns a good value.
  *  kv_dtype   an mla_kv_dtype value.
@@ -176,7 +176,8 @@ int mla_decode_paged_multi(const void* q, const int32_t* qo_indptr, int total_q,
  * The split model of amd-mixed-mla submission 700955 (`_compute_custom_splits`: utilisation
  * of the CTA slots times L / (L + per-split overhead)), with this kernel's own costs counted
  * in cache rows (a row = the bytes of one cached token: 1152 bf16, 576 fp8, 306 MXFP4, which
- * is why kv_dtype is an argument):
+ * is why kv_dtype is an argument; an MXFP4 CTA is bound by its dequantisation at 0.30 of the
+ * HBM rate, measured, so an MXFP4 row counts 306 / 0.30 bytes below):
  *   c = 32,832 / row   one piece (16 x 513 fp32 partial output and log-sum-exp), written once
  *                      and read once by the CTA that merges the sequence's ns pieces;
  *   w = 222,000 / row  one wave of CTAs: a CTA's start-up and final drain (about 2 + 3 us,

@@ -44,6 +44,11 @@ double row_bytes(int kv_dtype) {
          : kv_dtype == MLA_KV_FP8_E4M3 ? 1.0 * mla::kDim
          : static_cast<double>(mla::kMxPacked + mla::kMxScales);
 }
+// A CTA's rate through the cache relative to the HBM rate: bf16 and fp8 CTAs stream at it; an
+// MXFP4 CTA is bound by its dequantisation at 0.30 of it (2.02 of the 6.76 TB/s measured on
+// GB300 at 256 x 8192).  The split model's costs (latencies and piece bytes at the HBM rate)
+// count in the rows a CTA gets through in the same time: bytes x rate / row bytes.
+double row_rate(int kv_dtype) { return kv_dtype == MLA_KV_MXFP4 ? 0.30 : 1.0; }
 thread_local const char* t_last_cuda_error = "";
 
 // Optional timing of each call's split kernel (events recorded on the call's stream).
@@ -167,13 +172,11 @@ static int encode_map(CUtensorMap* map, const void* kv, int kv_dtype, bool rope,
 unsigned long long pipeline_wait_limit_ns() { return g_wait_limit_ns.load(); }
 
 // The crossing's time (kCrossBytes is that time times one SM's HBM share) in the rows a CTA
-// gets through in that time: bf16 and fp8 CTAs stream at the HBM rate; an MXFP4 CTA is
-// bound by its dequantisation at 0.275 of it (1.86 of the 6.76 TB/s measured on GB300).
+// gets through in that time (row_rate).
 int balance_cross_rows(int kv_dtype) {
   const int r = g_cross_rows.load();
   if (r >= 0) return r;
-  const double rate = kv_dtype == MLA_KV_MXFP4 ? 0.275 : 1.0;
-  return static_cast<int>(kCrossBytes / row_bytes(kv_dtype) * rate + 0.5);
+  return static_cast<int>(kCrossBytes / row_bytes(kv_dtype) * row_rate(kv_dtype) + 0.5);
 }
 
 int encode_kv_map(CUtensorMap* map, const void* kv, int kv_dtype) { return encode_map(map, kv, kv_dtype, false); }
@@ -228,8 +231,9 @@ int mla_decode_pick_splits(int batch, int kv_len_hint, int num_sms, int kv_dtype
   //   balanced:    R + w + s c + (s - 1) x + p c,  R = B L / SMs rows per CTA, s = ceil(R / L) + 1
   //                sequences touched by a CTA, p = ceil(L / R) + 1 pieces per sequence.
   // The best uniform split count is returned, or 0 when the balanced mode is faster.
-  // kv_dtype sets the row size, hence c, w and x in rows.
-  const double row = row_bytes(kv_dtype);
+  // kv_dtype sets the row size and the CTAs' rate through the rows (row_rate), hence c, w and
+  // x in rows.
+  const double row = row_bytes(kv_dtype) / row_rate(kv_dtype);
   const double c = kPieceBytes / row, w = kWaveBytes / row, x = kCrossBytes / row;
   const long long L = std::max(kv_len_hint, 1), B = batch, S = num_sms, BN = mla::kBN;
   const long long ns_max = std::min<long long>(mla::kMaxSplits, (L + BN - 1) / BN);

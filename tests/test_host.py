@@ -134,12 +134,14 @@ ROW_BYTES = {0: 576 * 2, 1: 576, 2: 288 + 18}          # bf16, fp8, MXFP4 cache 
 PIECE_BYTES = 16 * (512 + 1) * 4                          # fp32 partial output + log-sum-exp of 16 heads
 WAVE_BYTES = 222e3                                        # per-wave start-up + drain latency x one SM's HBM share
 CROSS_BYTES = 300e3                                       # crossing latency x one SM's HBM share
+ROW_RATE = {0: 1.0, 1: 1.0, 2: 0.30}                      # a CTA's rate through the rows / the HBM rate
 
 
 def _model_splits(batch, L, sms, dtype):
     """The split model as the header states it: cache-row costs c (a piece) and x (a sequence
     crossing), time of the slowest CTA for each uniform split count and for the balanced mode."""
-    c, w, x = PIECE_BYTES / ROW_BYTES[dtype], WAVE_BYTES / ROW_BYTES[dtype], CROSS_BYTES / ROW_BYTES[dtype]
+    row = ROW_BYTES[dtype] / ROW_RATE[dtype]
+    c, w, x = PIECE_BYTES / row, WAVE_BYTES / row, CROSS_BYTES / row
     L = max(L, 1)
     best_ns, best_t = 1, None
     for ns in range(1, min(4096, -(-L // 128)) + 1):
@@ -176,7 +178,10 @@ def test_pick_splits_reproduces_the_measured_choices(lib):
     #   fp8  256 x 4096: balanced 123.6, ns 1 125.6, ns 2 144.0, ns 4 154.3 us
     #   fp8  256 x 8192: balanced 211.6, ns 1 219.8, ns 2 242.3, ns 4 244.4
     #   MXFP4 256 x 8192: balanced 344.7, ns 1 379.5, ns 2 402.1, ns 4 385.7
-    #   fp8  64 x 8192: ns 2 72.4, balanced 82.5;  MXFP4: ns 2 105.2, balanced 109.2
+    #   fp8  64 x 8192: ns 2 72.4, balanced 82.5
+    #   MXFP4 (current dequantisation, 0.30 of the HBM rate): 64 x 8192 balanced 99.0, ns 2 101.0;
+    #   4 x 8192 ns 16 31.4, ns 8 37.5;  16 x 8192 ns 8 39.6, balanced 45.7, ns 16 51.9;
+    #   32 x 8192 ns 4 60.1, balanced 64.2
     #   bf16 64 x 8192: balanced 139.9, ns 2 142.0
     #   fp8  152 x 8192: ns 1 129.7, balanced 131.7, ns 2 139.9
     #   fp8  16 x 8192: ns 8 = ns 9 33.4, balanced 43.7;  4 x 8192: ns 13 = ns 16 25.2, ns 32 27.3
@@ -187,7 +192,10 @@ def test_pick_splits_reproduces_the_measured_choices(lib):
     assert pick(256, 8192, 1) == 0
     assert pick(256, 8192, 2) == 0
     assert pick(64, 8192, 1) == 2
-    assert pick(64, 8192, 2) == 2
+    assert pick(64, 8192, 2) == 0
+    assert pick(4, 8192, 2) == 16
+    assert pick(16, 8192, 2) == 8
+    assert pick(32, 8192, 2) == 4
     assert pick(64, 8192, 0) == 0
     assert pick(152, 8192, 1) == 1
     assert pick(16, 8192, 1) in (8, 9)
